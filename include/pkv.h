@@ -1,0 +1,213 @@
+/*
+ * pkv.h — C ABI of a paged-KV attention library for one NVIDIA GB300 (sm_103a).
+ *
+ * The calls follow the attention-backend interface described in
+ * "--attention-backend" (SGLang manual), section "What an attention backend is":
+ * a backend computes attention over the paged KV cache for one batch; it builds
+ * per-batch metadata (page tables, index buffers), keeps state that CUDA-graph
+ * capture and replay can reuse, and runs forward_extend (prefill) and
+ * forward_decode (decode). The ForwardMode dispatch follows "[SGLang] Hybrid
+ * Attention: Dense-Sparse 동적 전환 전략", section "_select_backend: ForwardMode 기반
+ * 동적 전환", and the save_kv_cache step its section "forward: 선형 어텐션까지
+ * 지원하는 범용 위임".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every function returns an int status (PKV_OK == 0, or a PKV_ERR_* code).
+ *   Nothing throws, aborts or prints. Arguments are checked on the host before
+ *   anything is launched; a failed check launches nothing.
+ * - Pointers named d_* are DEVICE pointers into memory the caller owns (for
+ *   example PyTorch tensors). The library never allocates or frees device
+ *   memory: its only device state lives in the workspace the caller passes to
+ *   pkv_create. Host-side, pkv_create allocates one small context object.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream). Work is enqueued asynchronously on it; no call below synchronises
+ *   except pkv_get_device_error. pkv_build_metadata, pkv_set_kv_buffer and the
+ *   forward calls read lengths only on the device, so a sequence of them can be
+ *   captured into a CUDA graph and replayed with new lengths of the same batch
+ *   size.
+ * - KV pool layout ("NHD"): one pool for K and one for V per layer, each
+ *   [num_pages * page_size slots][num_kv_heads][head_dim], row-major, with
+ *   slot = page * page_size + offset. Elements are bf16, or FP8 E4M3FN bytes
+ *   with one fp32 scale per pool (value = code * scale).
+ * - Queries and outputs are bf16 [tokens][num_q_heads][head_dim]; LSE is fp32
+ *   [tokens][num_q_heads], the natural log of sum_j exp(sm_scale * q . k_j).
+ *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ * - Request b has seq_lens[b] = L_b KV tokens (prefix plus this step's new
+ *   tokens, whose K/V pkv_set_kv_buffer has already stored) and qo_len_b query
+ *   rows; its i-th query row sees keys 0 .. L_b - qo_len_b + i (causal,
+ *   aligned to the end). Decode is qo_len_b == 1. A request with L_b == 0 is
+ *   padding: its rows get output 0 and LSE -inf.
+ * - Device-side faults in the data (a page id outside the pool, a slot outside
+ *   the pool, lengths beyond the configured capacities) are never turned into
+ *   out-of-bounds accesses: the kernel skips the offending work and records the
+ *   first error in a word of the workspace, read by pkv_get_device_error.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG 1 /* null pointer, negative size, bad enum, misaligned pointer */
+#define PKV_ERR_UNSUPPORTED 2 /* shape or feature this build does not implement */
+#define PKV_ERR_CAPACITY 3    /* batch or workspace larger than the configured capacity */
+#define PKV_ERR_CUDA 4        /* a CUDA runtime / driver call failed */
+#define PKV_ERR_DEVICE 5      /* the device recorded a data error (see pkv_get_device_error) */
+
+/* Device error word values (pkv_get_device_error). */
+#define PKV_DEV_OK 0
+#define PKV_DEV_BAD_LENGTH 1   /* seq_len < 0, qo_len < 0 or qo_len > seq_len */
+#define PKV_DEV_BAD_PAGE 2     /* page id outside [0, num_pages) */
+#define PKV_DEV_CAPACITY 3     /* total pages / query rows beyond the configured capacity */
+#define PKV_DEV_BAD_SLOT 4     /* set_kv_buffer loc outside [0, num_pages * page_size) */
+#define PKV_DEV_QO_TOO_LONG 5  /* decode path: qo_len beyond config.max_qo_len */
+
+/* ---- enumerations -------------------------------------------------------- */
+/* ForwardMode of the batch ("[SGLang] Hybrid Attention", section
+ * "_select_backend: ForwardMode 기반 동적 전환"). */
+typedef enum {
+  PKV_MODE_EXTEND = 0,        /* prefill / extend */
+  PKV_MODE_DECODE = 1,
+  PKV_MODE_IDLE = 2,          /* empty batch on this rank */
+  PKV_MODE_TARGET_VERIFY = 3, /* speculative verify of draft tokens */
+  PKV_MODE_DRAFT_EXTEND = 4
+} pkv_forward_mode;
+
+/* --speculative-attention-mode ("--attention-backend", section "Two backends in
+ * one server"): which path runs the verify pass; the default is prefill. */
+typedef enum { PKV_SPEC_PREFILL = 0, PKV_SPEC_DECODE = 1 } pkv_spec_mode;
+
+typedef enum { PKV_PATH_INVALID = -1, PKV_PATH_DECODE = 0, PKV_PATH_EXTEND = 1 } pkv_path;
+
+typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
+
+/* ---- configuration --------------------------------------------------------
+ * Fixed for the life of a context; every capacity bounds a fixed-size
+ * metadata buffer in the workspace, so captured graphs can be replayed.
+ * Supported: head_dim 64 or 128; page_size 16; num_q_heads a multiple of
+ * num_kv_heads with a group size num_q_heads / num_kv_heads of at most 16;
+ * FP8 KV on the decode path only (forward_extend with an FP8 pool returns
+ * PKV_ERR_UNSUPPORTED). */
+typedef struct {
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t kv_dtype;        /* pkv_kv_dtype */
+  int32_t num_pages;       /* pool capacity in pages (pool = num_pages * page_size slots) */
+  int32_t max_batch;       /* max requests in one batch */
+  int32_t max_pages_total; /* max sum over requests of ceil(seq_len / page_size) */
+  int32_t max_q_tokens;    /* max sum over requests of qo_len */
+  int32_t max_qo_len;      /* max qo_len of one request on the decode path (verify drafts); 1 for plain decode */
+} pkv_config;
+
+typedef struct pkv_ctx pkv_ctx;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* pkv_status_string(int status);
+
+/* Bytes of device workspace a context with this configuration needs.
+ * Errors: INVALID_ARG (null), UNSUPPORTED (shape outside the supported set). */
+int pkv_workspace_bytes(const pkv_config* cfg, size_t* bytes_out);
+
+/* Bytes of ONE pool (K or V) of one layer: num_pages * page_size * num_kv_heads
+ * * head_dim * element size. */
+int pkv_pool_bytes(const pkv_config* cfg, size_t* bytes_out);
+
+/* Create a context over caller-owned device workspace (256-byte aligned, at
+ * least pkv_workspace_bytes). The context keeps the pointer; the caller keeps
+ * the memory alive until pkv_destroy and must not use it for anything else.
+ * Reads the current CUDA device's SM count. Errors: INVALID_ARG, UNSUPPORTED,
+ * CAPACITY (workspace too small), CUDA. */
+int pkv_create(const pkv_config* cfg, void* d_workspace, size_t workspace_bytes, pkv_ctx** ctx_out);
+
+/* Free the host-side context (never the workspace). NULL is accepted. */
+int pkv_destroy(pkv_ctx* ctx);
+
+/* HybridAttnBackend._select_backend as a pure host function:
+ * DECODE, IDLE -> PKV_PATH_DECODE; TARGET_VERIFY, DRAFT_EXTEND -> PKV_PATH_DECODE
+ * when spec_mode == PKV_SPEC_DECODE, else PKV_PATH_EXTEND; EXTEND ->
+ * PKV_PATH_EXTEND. Out-of-range arguments -> PKV_PATH_INVALID. */
+int pkv_select_backend(int forward_mode, int spec_mode);
+
+/* Per-batch metadata ("--attention-backend", section "What an attention backend
+ * is"), built on the device into the workspace:
+ *   kv_indptr[b+1]   = kv_indptr[b] + ceil(seq_lens[b] / page_size)
+ *   kv_indices       = page_table rows b, entries 0 .. ceil(seq_lens[b]/page_size)-1, concatenated
+ *   kv_last_page_len = seq_lens[b] - (pages_b - 1) * page_size (0 for an empty request)
+ *   qo_indptr[b+1]   = qo_indptr[b] + qo_lens[b]
+ * plus the split-KV work list of the decode path and the query-tile list of
+ * the extend path. d_seq_lens, d_qo_lens: int32[batch] (d_qo_lens NULL means
+ * one query row per request, as in decode). d_page_table: int32 rows of
+ * page_table_stride entries. forward_mode selects nothing here (both paths'
+ * plans are built); it is checked for validity, and IDLE (or batch == 0)
+ * builds an empty plan. Errors: INVALID_ARG, CAPACITY (batch > max_batch),
+ * CUDA. Data errors are recorded on the device. */
+int pkv_build_metadata(pkv_ctx* ctx, int forward_mode, int32_t batch, const int32_t* d_seq_lens,
+                       const int32_t* d_qo_lens, const int32_t* d_page_table, int32_t page_table_stride,
+                       void* stream);
+
+/* Device pointers to the metadata of the last pkv_build_metadata (valid once
+ * that call's work has run on its stream). Any out pointer may be NULL. */
+int pkv_get_metadata(pkv_ctx* ctx, const int32_t** kv_indptr, const int32_t** kv_indices,
+                     const int32_t** kv_last_page_len, const int32_t** qo_indptr);
+
+/* save_kv_cache: store this step's new K/V rows into the pools,
+ *   pool[d_loc[i], h, :] = new[i, h, :]   for i < n_tokens, every KV head h.
+ * d_k, d_v: bf16 [n_tokens][num_kv_heads][head_dim]; d_loc: int32 slots.
+ * bf16 pools receive the same bits; E4M3 pools receive
+ * e4m3_rn_satfinite(float(x) * inv_scale) (one fp32 multiply, round to nearest
+ * even, finite values beyond +-448 saturate). Slots outside the pool are
+ * skipped and recorded as PKV_DEV_BAD_SLOT. Duplicate slots: unspecified
+ * winner. Pointers must be 16-byte aligned. */
+int pkv_set_kv_buffer(pkv_ctx* ctx, void* d_k_pool, void* d_v_pool, const int32_t* d_loc, const void* d_k,
+                      const void* d_v, int32_t n_tokens, float k_inv_scale, float v_inv_scale, void* stream);
+
+/* forward_decode: attention of every query row against its request's paged
+ * keys, using the metadata of the last pkv_build_metadata. Split-KV: each
+ * (request, KV head) range is cut into chunks processed in parallel and merged
+ * by their log-sum-exp. Handles qo_len up to config.max_qo_len per request
+ * (target-verify on the decode path) with the causal rule above.
+ * d_q: bf16 [T][num_q_heads][head_dim] (T = sum of qo_len), d_out: bf16 of the
+ * same shape, d_lse: fp32 [T][num_q_heads] or NULL. k_scale / v_scale multiply
+ * E4M3 codes (ignored for bf16 pools). Pointers must be 16-byte aligned.
+ * Errors: INVALID_ARG, UNSUPPORTED (group size with max_qo_len beyond one
+ * 128-row tile), CUDA. */
+int pkv_forward_decode(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, const void* d_v_pool, float sm_scale,
+                       float k_scale, float v_scale, void* d_out, float* d_lse, void* stream);
+
+/* forward_extend: causal attention of each request's query block (its
+ * qo_len new tokens) against its cached prefix plus the new tokens, on the
+ * tensor cores. Same arguments and layouts as pkv_forward_decode; bf16 pools
+ * only (UNSUPPORTED for E4M3). */
+int pkv_forward_extend(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, const void* d_v_pool, float sm_scale,
+                       float k_scale, float v_scale, void* d_out, float* d_lse, void* stream);
+
+/* The hybrid backend's forward: pkv_select_backend(forward_mode, spec_mode)
+ * picks pkv_forward_decode or pkv_forward_extend; IDLE returns PKV_OK and
+ * launches nothing. forward_mode must be compatible with the metadata built
+ * (DECODE needs one query row per request). */
+int pkv_forward(pkv_ctx* ctx, int forward_mode, int spec_mode, const void* d_q, const void* d_k_pool,
+                const void* d_v_pool, float sm_scale, float k_scale, float v_scale, void* d_out, float* d_lse,
+                void* stream);
+
+/* Synchronise `stream`, read the device error word into *code (PKV_DEV_*) and
+ * clear it. Returns PKV_ERR_DEVICE when *code != PKV_DEV_OK. */
+int pkv_get_device_error(pkv_ctx* ctx, int32_t* code, void* stream);
+
+/* Write a one-line description of the context (paths, tile shapes, split
+ * policy, SM count) into buf (always NUL-terminated when n > 0). */
+int pkv_describe(pkv_ctx* ctx, char* buf, size_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

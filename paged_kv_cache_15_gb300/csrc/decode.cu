@@ -1,0 +1,730 @@
+// forward_decode over the paged KV cache ("--attention-backend", section "What an
+// attention backend is": forward_decode runs one query token per request against
+// its cached keys; section "Two backends in one server": decode reads one query
+// against a long cache, so it is bound by memory traffic).
+//
+// Split-KV flash decoding:
+//   * The metadata build cut every (request, KV head) key range into chunks of
+//     chunk_pages pages; one work unit = (request, split, KV head). A persistent
+//     grid walks the units with a grid stride.
+//   * GQA packing: the group's query heads (times the request's query tokens on
+//     the verify path) form the rows of one 16-row MMA tile per row-warp, so every
+//     K/V byte fetched from HBM is used by all heads of its group.
+//   * A producer warp gathers pages with TMA (one 2-D box of 16 token rows x 128
+//     bytes per page, 128-byte swizzle) into a ring of shared-memory stages; the
+//     consumer warps wait on the stage's mbarrier, compute S = Q K^T and O += P V
+//     with m16n8k16 tensor-core MMAs, and keep an online softmax per row
+//     (running max m, running sum l) in registers, in the log2 domain.
+//   * Each unit ends with its normalised output and LSE. A request with one split
+//     writes the final bf16 output directly; otherwise the unit writes an fp32
+//     partial row that the merge kernel combines:
+//        lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s.
+//   * FP8 E4M3 pools: codes are widened to f16 in registers (cvt e4m3x2 -> f16x2,
+//     exact), the MMAs run in f16 (Q and P rounded to f16), and the per-pool
+//     scales are folded into the score scale and the output.
+// Keys past the request's length inside its last page are zeroed in shared
+// memory before use, and every other key outside the visible range is masked
+// to -inf, so unused pool slots never reach the result.
+#include <math.h>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D_, bool FP8_, int WR_, int WK_, int KPW_, int STAGES_>
+struct DecodeCfg {
+  static constexpr int D = D_;
+  static constexpr bool FP8 = FP8_;
+  static constexpr int WR = WR_;  // row warps (16 rows each)
+  static constexpr int WK = WK_;  // key warps (split each stage's keys)
+  static constexpr int KPW = KPW_;  // keys per key-warp per stage (multiple of 16)
+  static constexpr int STAGES = STAGES_;
+  static constexpr int kConsumerWarps = WR * WK;
+  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static constexpr int kRows = 16 * WR;
+  static constexpr int kStageKeys = WK * KPW;
+  static constexpr int kStagePages = kStageKeys / kPageSize;
+  static constexpr int kElem = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElem;
+  static constexpr int kColBlocks = kRowBytes / 128;
+  static constexpr int kTileBytes = kStageKeys * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kNT = D / 8;  // n-tiles of the output
+  static constexpr int kBarOffset = STAGES * kStageBytes;
+  static constexpr int kMlOffset = kBarOffset + 2 * STAGES * 8;
+  static constexpr int kAbortOffset = kMlOffset + WK * 16 * 2 * 4;
+  static constexpr int kSmemBytes = kAbortOffset + 16 + 1024;  // + alignment slack
+  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
+  static_assert(KPW % 16 == 0 && kStageKeys % kPageSize == 0, "stage must hold whole pages");
+  static_assert(!(WK > 1) || (WK * 16 * D * 4 <= kStageBytes), "merge scratch must fit in one stage");
+};
+
+struct DecodeArgs {
+  Meta m;
+  const uint16_t* q;  // bf16 [T][Hq][D]
+  uint16_t* out;      // bf16 [T][Hq][D]
+  float* lse;         // fp32 [T][Hq] or null
+  int num_q_heads, num_kv_heads, group;
+  float scale_log2;  // sm_scale * k_scale * log2(e)
+  float v_scale;     // multiplies the output (E4M3 pools), 1 for bf16
+};
+
+// Byte offset of (row, 16-byte chunk) inside a swizzled [rows][128 B] column block.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Output column of accumulator element e (0/1) of n-tile nt for quad lane q.
+template <bool FP8>
+__device__ __forceinline__ int ocol(int nt, int q, int e) {
+  if constexpr (FP8) {
+    return (nt >> 1) * 16 + 4 * q + 2 * e + (nt & 1);
+  } else {
+    return nt * 8 + 2 * q + e;
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                                                     const __grid_constant__ CUtensorMap tmap_v,
+                                                                     DecodeArgs a) {
+  constexpr int D = C::D;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  uint64_t* empty = full + C::STAGES;
+  float* s_ml = reinterpret_cast<float*>(smem + C::kMlOffset);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kAbortOffset);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* plan = a.m.plan;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::kConsumerWarps);
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  // Stage buffers start as zeros: rows of a partly filled stage are then always
+  // finite (zeros or earlier valid keys) and their zero weights stay zero.
+  for (int i = tid; i < C::STAGES * C::kStageBytes / 16; i += C::kThreads)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  const int n_units = plan[kDecodeItems] * a.num_kv_heads;
+
+  if (warp == C::kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmap_k);
+      prefetch_tmap(&tmap_v);
+      const uint64_t pol = policy_evict_first();
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_phase = 0;  // per-slot: issued at least once / parity of last fill
+      for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
+        const DecodeItem it = a.m.decode_items[w / a.num_kv_heads];
+        const int g = w % a.num_kv_heads;
+        const int base = a.m.kv_indptr[it.b] + it.p0;
+        const int npages = it.p1 - it.p0;
+        const int nst = (npages + C::kStagePages - 1) / C::kStagePages;
+        for (int st = 0; st < nst; ++st) {
+          if (!mbar_wait(&empty[slot], phase ^ 1, plan)) {
+            *s_abort = 1;
+            break;
+          }
+          const int np = min(C::kStagePages, npages - st * C::kStagePages);
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(np * kPageSize * C::kRowBytes * 2));
+          uint8_t* kdst = smem + slot * C::kStageBytes;
+          uint8_t* vdst = kdst + C::kTileBytes;
+          for (int p = 0; p < np; ++p) {
+            const int page = a.m.kv_indices[base + st * C::kStagePages + p];
+#pragma unroll
+            for (int cb = 0; cb < C::kColBlocks; ++cb) {
+              const int x = g * D + cb * (128 / C::kElem);
+              const int off = cb * C::kStageKeys * 128 + p * kPageSize * 128;
+              tma_load_2d_hint(kdst + off, &tmap_k, x, page * kPageSize, &full[slot], pol);
+              tma_load_2d_hint(vdst + off, &tmap_v, x, page * kPageSize, &full[slot], pol);
+            }
+          }
+          armed |= 1u << slot;
+          armed_phase = (armed_phase & ~(1u << slot)) | (phase << slot);
+          if (++slot == C::STAGES) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // never leave the CTA with a TMA still writing into shared memory
+      for (int s = 0; s < C::STAGES; ++s)
+        if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1, plan);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int cw = warp;  // consumer warp
+  const int wr = cw / C::WK, wk = cw % C::WK;
+  const int qd = lane & 3;   // quad lane
+  const int rq = lane >> 2;  // row within the 8-row half
+  const int G = a.group;
+  int slot = 0;
+  uint32_t phase = 0;
+
+  for (int w = blockIdx.x; w < n_units; w += gridDim.x) {
+    if (*s_abort) break;
+    const DecodeItem it = a.m.decode_items[w / a.num_kv_heads];
+    const int g = w % a.num_kv_heads;
+    const int b = it.b;
+    const int L = a.m.kv_len[b];
+    const int q0 = a.m.qo_indptr[b];
+    const int qo = a.m.qo_indptr[b + 1] - q0;
+    const int nsplit = a.m.n_splits[b];
+    const int np_req = a.m.kv_indptr[b + 1] - a.m.kv_indptr[b];
+    const int rows_valid = qo * G;
+    const bool skip = rows_valid > C::kRows;  // tile too small: recorded, pipeline still drained
+    if (skip && lane == 0 && wr == 0 && wk == 0) record_error(plan, PKV_DEV_QO_TOO_LONG, b);
+    const int key_begin = it.p0 * kPageSize;
+    const int key_end = min(it.p1 * kPageSize, L);
+    const int npages = it.p1 - it.p0;
+    const int nst = (npages + C::kStagePages - 1) / C::kStagePages;
+
+    // rows of this thread: ra = wr*16 + rq, rb = ra + 8 -> (token i, head-in-group)
+    const int ra = wr * 16 + rq, rb = ra + 8;
+    const bool va = ra < rows_valid, vb = rb < rows_valid;
+    const int prefix = L - qo;
+    const int lim_a = prefix + min(ra / G, qo - 1);
+    const int lim_b = prefix + min(rb / G, qo - 1);
+    const long long qrow_a = ((long long)(q0 + ra / G) * a.num_q_heads + g * G + ra % G) * D;
+    const long long qrow_b = ((long long)(q0 + rb / G) * a.num_q_heads + g * G + rb % G) * D;
+
+    // Q fragments (A operand), D/16 k-steps x 4 registers
+    uint32_t qf[D / 16][4];
+    if constexpr (!C::FP8) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int c0 = kk * 16 + 2 * qd;
+        qf[kk][0] = va ? *reinterpret_cast<const uint32_t*>(a.q + qrow_a + c0) : 0u;
+        qf[kk][1] = vb ? *reinterpret_cast<const uint32_t*>(a.q + qrow_b + c0) : 0u;
+        qf[kk][2] = va ? *reinterpret_cast<const uint32_t*>(a.q + qrow_a + c0 + 8) : 0u;
+        qf[kk][3] = vb ? *reinterpret_cast<const uint32_t*>(a.q + qrow_b + c0 + 8) : 0u;
+      }
+    } else {
+      // permuted contraction order matching the 8-byte K loads below:
+      // k-step 2p  : logical k {2q,2q+1} <- D 32p+8q+{0,1}, {2q+8,2q+9} <- D 32p+8q+{2,3}
+      // k-step 2p+1: logical k {2q,2q+1} <- D 32p+8q+{4,5}, {2q+8,2q+9} <- D 32p+8q+{6,7}
+#pragma unroll
+      for (int p = 0; p < D / 32; ++p) {
+        const int c0 = p * 32 + 8 * qd;
+        uint4 xa = va ? *reinterpret_cast<const uint4*>(a.q + qrow_a + c0) : make_uint4(0, 0, 0, 0);
+        uint4 xb = vb ? *reinterpret_cast<const uint4*>(a.q + qrow_b + c0) : make_uint4(0, 0, 0, 0);
+        qf[2 * p][0] = pack_f16(bf16lo(xa.x), bf16hi(xa.x));
+        qf[2 * p][1] = pack_f16(bf16lo(xb.x), bf16hi(xb.x));
+        qf[2 * p][2] = pack_f16(bf16lo(xa.y), bf16hi(xa.y));
+        qf[2 * p][3] = pack_f16(bf16lo(xb.y), bf16hi(xb.y));
+        qf[2 * p + 1][0] = pack_f16(bf16lo(xa.z), bf16hi(xa.z));
+        qf[2 * p + 1][1] = pack_f16(bf16lo(xb.z), bf16hi(xb.z));
+        qf[2 * p + 1][2] = pack_f16(bf16lo(xa.w), bf16hi(xa.w));
+        qf[2 * p + 1][3] = pack_f16(bf16lo(xb.w), bf16hi(xb.w));
+      }
+    }
+
+    float o[C::kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+    bool aborted = false;
+    for (int st = 0; st < nst; ++st) {
+      if (!mbar_wait(&full[slot], phase, plan)) {
+        *s_abort = 1;
+        aborted = true;
+        break;
+      }
+      const uint32_t kbase = smem_u32(smem + slot * C::kStageBytes);
+      const uint32_t vbase = kbase + C::kTileBytes;
+      const int stage_key0 = key_begin + st * C::kStageKeys;
+      // last page of the request with a partial fill: zero the V rows past L
+      const bool tail = (it.p1 == np_req) && (st == nst - 1) && (L % kPageSize) != 0;
+      if (tail) {
+        const int r0 = L - stage_key0;
+        const int r1 = min(C::kStagePages, npages - st * C::kStagePages) * kPageSize;
+        uint8_t* vb8 = smem + slot * C::kStageBytes + C::kTileBytes;
+        const int n16 = (r1 - r0) * C::kColBlocks * 8;
+        for (int i = cw * 32 + lane; i < n16; i += C::kConsumerWarps * 32) {
+          const int row = r0 + i / (C::kColBlocks * 8);
+          const int rest = i % (C::kColBlocks * 8);
+          const int cb = rest / 8, ch = rest % 8;
+          *reinterpret_cast<uint4*>(vb8 + cb * C::kStageKeys * 128 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, C::kConsumerWarps * 32);
+      }
+
+      if (!skip) {
+#pragma unroll
+        for (int kb = 0; kb < C::KPW / 16; ++kb) {
+          const int kr0 = wk * C::KPW + kb * 16;  // first stage row of this 16-key block
+          const int abs0 = stage_key0 + kr0;
+          if (abs0 >= key_end) break;
+          // ---- S = Q K^T for 16 keys (two n-tiles of 8) ----
+          float s[2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+          if constexpr (!C::FP8) {
+            const int key = kr0 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int chunk = 2 * kk + ((lane >> 3) & 1);
+              const uint32_t addr = kbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
+              uint32_t b00, b01, b10, b11;
+              ldsm_x4(addr, b00, b01, b10, b11);
+              mma_bf16(s[0], qf[kk], b00, b01);
+              mma_bf16(s[1], qf[kk], b10, b11);
+            }
+          } else {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              const int key = kr0 + nt * 8 + rq;
+#pragma unroll
+              for (int p = 0; p < D / 32; ++p) {
+                const int byte = p * 32 + 8 * qd;
+                const uint32_t addr = kbase + swz(key, byte >> 4) + (byte & 15);
+                uint32_t x0, x1;
+                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x0), "=r"(x1) : "r"(addr));
+                mma_f16(s[nt], qf[2 * p], e4m3x2_to_f16x2((uint16_t)(x0 & 0xffff)),
+                        e4m3x2_to_f16x2((uint16_t)(x0 >> 16)));
+                mma_f16(s[nt], qf[2 * p + 1], e4m3x2_to_f16x2((uint16_t)(x1 & 0xffff)),
+                        e4m3x2_to_f16x2((uint16_t)(x1 >> 16)));
+              }
+            }
+          }
+          // ---- mask, online softmax (log2 domain) ----
+          float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int kp = abs0 + nt * 8 + 2 * qd + e;
+              const bool ok = kp < key_end;
+              s[nt][e] = (ok && kp <= lim_a) ? s[nt][e] * a.scale_log2 : -INFINITY;
+              s[nt][2 + e] = (ok && kp <= lim_b) ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
+              mx_a = fmaxf(mx_a, s[nt][e]);
+              mx_b = fmaxf(mx_b, s[nt][2 + e]);
+            }
+          }
+          mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+          mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+          mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+          mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+          const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+          const float ref_a = mn_a == -INFINITY ? 0.f : mn_a;
+          const float ref_b = mn_b == -INFINITY ? 0.f : mn_b;
+          const float al_a = fast_exp2(m_a - ref_a), al_b = fast_exp2(m_b - ref_b);
+          m_a = mn_a;
+          m_b = mn_b;
+          float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              s[nt][e] = fast_exp2(s[nt][e] - ref_a);
+              s[nt][2 + e] = fast_exp2(s[nt][2 + e] - ref_b);
+              ps_a += s[nt][e];
+              ps_b += s[nt][2 + e];
+            }
+          }
+          l_a = l_a * al_a + ps_a;
+          l_b = l_b * al_b + ps_b;
+          if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {
+#pragma unroll
+            for (int nt = 0; nt < C::kNT; ++nt) {
+              o[nt][0] *= al_a;
+              o[nt][1] *= al_a;
+              o[nt][2] *= al_b;
+              o[nt][3] *= al_b;
+            }
+          }
+          // ---- O += P V ----
+          uint32_t pf[4];
+          if constexpr (!C::FP8) {
+            pf[0] = pack_bf16(s[0][0], s[0][1]);
+            pf[1] = pack_bf16(s[0][2], s[0][3]);
+            pf[2] = pack_bf16(s[1][0], s[1][1]);
+            pf[3] = pack_bf16(s[1][2], s[1][3]);
+            const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int jj = 0; jj < D / 16; ++jj) {
+              const int chunk = 2 * jj + (lane >> 4);
+              const uint32_t addr = vbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
+              uint32_t b0e, b1e, b0o, b1o;
+              ldsm_x4_t(addr, b0e, b1e, b0o, b1o);
+              mma_bf16(o[2 * jj], pf, b0e, b1e);
+              mma_bf16(o[2 * jj + 1], pf, b0o, b1o);
+            }
+          } else {
+            pf[0] = pack_f16(s[0][0], s[0][1]);
+            pf[1] = pack_f16(s[0][2], s[0][3]);
+            pf[2] = pack_f16(s[1][0], s[1][1]);
+            pf[3] = pack_f16(s[1][2], s[1][3]);
+            const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int jp = 0; jp < D / 32; ++jp) {
+              // 16-byte chunks 2jp (D 32jp..+15) and 2jp+1 (D 32jp+16..+31)
+              const int chunk = 2 * jp + (lane >> 4);
+              const uint32_t addr = vbase + swz(key, chunk);
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4_t(addr, r0, r1, r2, r3);
+              // r0: keys 0-7 / chunk 2jp, r1: keys 8-15 / chunk 2jp, r2, r3: chunk 2jp+1.
+              // bytes of r: V[2q][2c], V[2q][2c+1], V[2q+1][2c], V[2q+1][2c+1]
+              const uint32_t e0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0020));
+              const uint32_t o0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0031));
+              const uint32_t e1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0020));
+              const uint32_t o1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0031));
+              const uint32_t e2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0020));
+              const uint32_t o2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0031));
+              const uint32_t e3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0020));
+              const uint32_t o3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0031));
+              mma_f16(o[4 * jp + 0], pf, e0, e1);
+              mma_f16(o[4 * jp + 1], pf, o0, o1);
+              mma_f16(o[4 * jp + 2], pf, e2, e3);
+              mma_f16(o[4 * jp + 3], pf, o2, o3);
+            }
+          }
+        }
+      }
+      const bool hold = (C::WK > 1) && (st == nst - 1);  // last stage doubles as merge scratch
+      if (!hold) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == C::STAGES) {
+          slot = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (aborted) break;
+
+    // ---------------------------------------------------------- epilogue
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+
+    const bool direct = nsplit == 1;
+    const int split = it.split;
+    auto out_row = [&](int r, float*& prow, uint16_t*& orow, float*& lrow) {
+      const int i = r / G, h = g * G + r % G;
+      const long long t = q0 + i;
+      if (direct) {
+        orow = a.out + (t * a.num_q_heads + h) * D;
+        lrow = a.lse ? a.lse + t * a.num_q_heads + h : nullptr;
+        prow = nullptr;
+      } else {
+        const long long pr = (long long)a.m.partial_indptr[b] + (long long)split * qo + i;
+        prow = a.m.partial_o + (pr * a.num_q_heads + h) * D;
+        lrow = a.m.partial_lse + pr * a.num_q_heads + h;
+        orow = nullptr;
+      }
+    };
+
+    if constexpr (C::WK == 1) {
+      if (!skip) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int r = half ? rb : ra;
+          const bool v = half ? vb : va;
+          const float m = half ? m_b : m_a, l = half ? l_b : l_a;
+          if (!v) continue;
+          float* prow;
+          uint16_t* orow;
+          float* lrow;
+          out_row(r, prow, orow, lrow);
+          const float inv = l > 0.f ? a.v_scale / l : 0.f;
+          const float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < C::kNT; ++nt) {
+            const float x0 = o[nt][2 * half] * inv, x1 = o[nt][2 * half + 1] * inv;
+            const int c0 = ocol<C::FP8>(nt, qd, 0), c1 = ocol<C::FP8>(nt, qd, 1);
+            if (orow) {
+              if constexpr (!C::FP8) {
+                *reinterpret_cast<uint32_t*>(orow + c0) = pack_bf16(x0, x1);
+              } else {
+                uint32_t pk = pack_bf16(x0, x1);
+                orow[c0] = (uint16_t)(pk & 0xffff);
+                orow[c1] = (uint16_t)(pk >> 16);
+              }
+            } else {
+              prow[c0] = x0;
+              prow[c1] = x1;
+            }
+          }
+          if (qd == 0 && lrow) *lrow = lse;
+        }
+      }
+    } else {
+      // combine the WK key-warps of each row through shared memory
+      if (nst == 0) {
+        // empty key range (padding request): zero output, -inf LSE
+        if (wk == 0) {
+          for (int half = 0; half < 2; ++half) {
+            const int r = half ? rb : ra;
+            if (!(half ? vb : va) || skip) continue;
+            float* prow;
+            uint16_t* orow;
+            float* lrow;
+            out_row(r, prow, orow, lrow);
+            for (int c = qd; c < D; c += 4) {
+              if (orow) orow[c] = 0;
+              else prow[c] = 0.f;
+            }
+            if (qd == 0 && lrow) *lrow = -INFINITY;
+          }
+        }
+      } else {
+        named_bar_sync(1, C::kConsumerWarps * 32);  // everyone done reading the held stage
+        float* scr = reinterpret_cast<float*>(smem + slot * C::kStageBytes);  // [WK][16][D]
+        float* my = scr + wk * 16 * D;
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = ocol<C::FP8>(nt, qd, e);
+            my[rq * D + c] = o[nt][e];
+            my[(rq + 8) * D + c] = o[nt][2 + e];
+          }
+        }
+        if (qd == 0) {
+          s_ml[(wk * 16 + rq) * 2 + 0] = m_a;
+          s_ml[(wk * 16 + rq) * 2 + 1] = l_a;
+          s_ml[(wk * 16 + rq + 8) * 2 + 0] = m_b;
+          s_ml[(wk * 16 + rq + 8) * 2 + 1] = l_b;
+        }
+        named_bar_sync(1, C::kConsumerWarps * 32);
+        // each consumer thread finishes float4 pieces of the 16 x D tile
+        const int nthr = C::kConsumerWarps * 32;
+        const int ctid = cw * 32 + lane;
+        for (int idx = ctid; idx < 16 * (D / 4); idx += nthr) {
+          const int r = idx / (D / 4), c4 = idx % (D / 4);
+          if (r >= rows_valid || skip) continue;
+          float mw[C::WK], lw[C::WK];
+          float M = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < C::WK; ++k) {
+            mw[k] = s_ml[(k * 16 + r) * 2 + 0];
+            lw[k] = s_ml[(k * 16 + r) * 2 + 1];
+            M = fmaxf(M, mw[k]);
+          }
+          float Lsum = 0.f, wgt[C::WK];
+#pragma unroll
+          for (int k = 0; k < C::WK; ++k) {
+            wgt[k] = (M == -INFINITY) ? 0.f : fast_exp2(mw[k] - M);
+            Lsum += lw[k] * wgt[k];
+          }
+          const float inv = Lsum > 0.f ? a.v_scale / Lsum : 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < C::WK; ++k) {
+            const float4 x = *reinterpret_cast<const float4*>(scr + (k * 16 + r) * D + c4 * 4);
+            acc.x += x.x * wgt[k];
+            acc.y += x.y * wgt[k];
+            acc.z += x.z * wgt[k];
+            acc.w += x.w * wgt[k];
+          }
+          acc.x *= inv;
+          acc.y *= inv;
+          acc.z *= inv;
+          acc.w *= inv;
+          float* prow;
+          uint16_t* orow;
+          float* lrow;
+          out_row(r, prow, orow, lrow);
+          if (orow) {
+            *reinterpret_cast<uint2*>(orow + c4 * 4) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+          } else {
+            *reinterpret_cast<float4*>(prow + c4 * 4) = acc;
+          }
+          if (c4 == 0 && lrow) *lrow = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, C::kConsumerWarps * 32);  // scratch reads done before the stage is refilled
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == C::STAGES) {
+          slot = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  }
+}
+
+// LSE merge of split partials: one warp per (token, q-head) of requests with
+// more than one split.
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(Meta m, uint16_t* out, float* lse, int num_q_heads,
+                                                           int max_rows) {
+  const int total_q = m.plan[kTotalQ];
+  const int n_rows = min(total_q, max_rows) * num_q_heads;
+  const int lane = threadIdx.x & 31;
+  for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < n_rows; row += gridDim.x * 8) {
+    const int t = row / num_q_heads, h = row % num_q_heads;
+    const int b = m.token_req[t];
+    const int ns = m.n_splits[b];
+    if (ns <= 1) continue;
+    const int q0 = m.qo_indptr[b];
+    const int qo = m.qo_indptr[b + 1] - q0;
+    const long long base = (long long)m.partial_indptr[b] + (t - q0);
+    float M = -INFINITY;
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, m.partial_lse[(base + (long long)s * qo) * num_q_heads + h]);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Z = 0.f;
+    for (int s = lane; s < ns; s += 32) {
+      const float ls = m.partial_lse[(base + (long long)s * qo) * num_q_heads + h];
+      Z += (M == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
+    }
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+    const float invZ = Z > 0.f ? 1.f / Z : 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const long long pr = base + (long long)s * qo;
+      const float ls = m.partial_lse[pr * num_q_heads + h];
+      if (ls == -INFINITY) continue;
+      const float wgt = fast_exp2((ls - M) * kLog2e) * invZ;
+      const float* src = m.partial_o + (pr * num_q_heads + h) * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += wgt * x.x;
+        acc[1] += wgt * x.y;
+        acc[2] += wgt * x.z;
+        acc[3] += wgt * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += wgt * x.x;
+        acc[1] += wgt * x.y;
+      }
+    }
+    uint16_t* dst = out + ((long long)t * num_q_heads + h) * D + lane * PER;
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
+    }
+    if (lse && lane == 0) lse[(long long)t * num_q_heads + h] = Z > 0.f ? M + __logf(Z) : -INFINITY;
+  }
+}
+
+template <class C>
+int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+               float v_scale, void* out, float* lse, cudaStream_t st) {
+  CUtensorMap tk, tv;
+  const CUtensorMapDataType dt = C::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t inner = (uint64_t)c.cfg.num_kv_heads * C::D;
+  const uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
+  const uint32_t box_inner = 128 / C::kElem;
+  if (encode_tmap_2d(&tk, dt, const_cast<void*>(k_pool), inner, slots, inner * C::kElem, box_inner, kPageSize,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+    return PKV_ERR_CUDA;
+  if (encode_tmap_2d(&tv, dt, const_cast<void*>(v_pool), inner, slots, inner * C::kElem, box_inner, kPageSize,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+    return PKV_ERR_CUDA;
+  DecodeArgs a;
+  a.m = make_meta(c);
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.num_q_heads = c.cfg.num_q_heads;
+  a.num_kv_heads = c.cfg.num_kv_heads;
+  a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
+  const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
+  a.scale_log2 = sm_scale * (fp8 ? k_scale : 1.f) * kLog2e;
+  a.v_scale = fp8 ? v_scale : 1.f;
+  static bool attr_set[8] = {false};  // per device is enough: the attribute is per function
+  (void)attr_set;
+  cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  decode_splitkv_kernel<C><<<c.decode_ctas, C::kThreads, C::kSmemBytes, st>>>(tk, tv, a);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  const int rows = c.cfg.max_q_tokens * c.cfg.num_q_heads;
+  int grid = (rows + 7) / 8;
+  if (grid > c.num_sms * 8) grid = c.num_sms * 8;
+  if (grid < 1) grid = 1;
+  decode_merge_kernel<C::D><<<grid, 256, 0, st>>>(a.m, a.out, lse, c.cfg.num_q_heads, c.cfg.max_q_tokens);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Tile shapes: decode packs one 16-row tile per unit and splits each stage's
+// keys over four warps; the verify shape gives each of up to eight warps its
+// own 16 rows and all keys of a stage.
+using DecBf16D128 = DecodeCfg<128, false, 1, 4, 16, 3>;
+using DecBf16D64 = DecodeCfg<64, false, 1, 4, 16, 4>;
+using DecFp8D128 = DecodeCfg<128, true, 1, 4, 32, 3>;
+using VerBf16D128_2 = DecodeCfg<128, false, 2, 1, 64, 3>;
+using VerBf16D128_4 = DecodeCfg<128, false, 4, 1, 64, 3>;
+using VerBf16D128_8 = DecodeCfg<128, false, 8, 1, 64, 3>;
+using VerBf16D64_2 = DecodeCfg<64, false, 2, 1, 64, 4>;
+using VerBf16D64_4 = DecodeCfg<64, false, 4, 1, 64, 4>;
+using VerBf16D64_8 = DecodeCfg<64, false, 8, 1, 64, 4>;
+using VerFp8D128_2 = DecodeCfg<128, true, 2, 1, 128, 3>;
+using VerFp8D128_4 = DecodeCfg<128, true, 4, 1, 128, 3>;
+using VerFp8D128_8 = DecodeCfg<128, true, 8, 1, 128, 3>;
+
+}  // namespace
+
+// Rows a decode-path unit must hold: every query row of one request's group.
+int decode_row_warps(const pkv_config& cfg) {
+  const int rows = cfg.max_qo_len * (cfg.num_q_heads / cfg.num_kv_heads);
+  if (rows <= 16) return 1;
+  if (rows <= 32) return 2;
+  if (rows <= 64) return 4;
+  if (rows <= 128) return 8;
+  return 0;
+}
+
+int decode_stage_pages(const pkv_config& cfg) {
+  const int wr = decode_row_warps(cfg);
+  const bool fp8 = cfg.kv_dtype == PKV_KV_FP8_E4M3;
+  if (wr == 1) return fp8 ? 8 : 4;
+  return fp8 ? 8 : 4;
+}
+
+int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+                  float v_scale, void* out, float* lse, cudaStream_t st) {
+  const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
+  const int D = c.cfg.head_dim;
+  const int wr = decode_row_warps(c.cfg);
+#define PKV_RUN(CFG) return run_decode<CFG>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st)
+  if (!fp8 && D == 128) {
+    if (wr == 1) PKV_RUN(DecBf16D128);
+    if (wr == 2) PKV_RUN(VerBf16D128_2);
+    if (wr == 4) PKV_RUN(VerBf16D128_4);
+    if (wr == 8) PKV_RUN(VerBf16D128_8);
+  } else if (!fp8 && D == 64) {
+    if (wr == 1) PKV_RUN(DecBf16D64);
+    if (wr == 2) PKV_RUN(VerBf16D64_2);
+    if (wr == 4) PKV_RUN(VerBf16D64_4);
+    if (wr == 8) PKV_RUN(VerBf16D64_8);
+  } else if (fp8 && D == 128) {
+    if (wr == 1) PKV_RUN(DecFp8D128);
+    if (wr == 2) PKV_RUN(VerFp8D128_2);
+    if (wr == 4) PKV_RUN(VerFp8D128_4);
+    if (wr == 8) PKV_RUN(VerFp8D128_8);
+  }
+#undef PKV_RUN
+  return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pkv

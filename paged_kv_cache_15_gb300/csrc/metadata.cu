@@ -1,0 +1,375 @@
+// Per-batch metadata build ("--attention-backend", section "What an attention
+// backend is": a backend builds per-batch metadata such as page tables and
+// index buffers; CUDA-graph replay needs them in fixed-size buffers).
+//
+// One launch, every input read on the device, so it can sit in a captured
+// graph. Outputs, for request b with KV length L_b and qo_len_b query rows:
+//   kv_indptr[b+1]      = kv_indptr[b] + ceil(L_b / page_size)
+//   kv_indices          = page_table[b, 0 : pages_b] concatenated over b
+//   kv_last_page_len[b] = L_b - (pages_b - 1) * page_size   (0 when L_b == 0)
+//   qo_indptr[b+1]      = qo_indptr[b] + qo_len_b
+// and two work lists:
+//   decode path: (request, split, page range) items; every request's pages are
+//     cut into chunks of chunk_pages, with chunk_pages chosen so the number of
+//     (item, KV head) units fills the persistent grid a few times over and the
+//     partial-output buffer cannot overflow;
+//   extend path: (request, first query row) tiles of 128 rows, where a row is
+//     (token, head-in-group), with the number of 128-key KV tiles it reaches.
+//
+// Work split: CTA j owns a contiguous range of requests. Every CTA first
+// reduces the batch totals (they fix chunk_pages and the capacity checks) and
+// the prefix of each scanned quantity before its range, then scans its range.
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxCtas = 64;
+
+struct ReqInfo {
+  int L;       // KV length used (0 if the request's lengths were invalid)
+  int qo;      // query rows
+  int np;      // pages
+  int nsplit;  // decode splits
+  int prow;    // partial-output rows (0 when the request has a single split)
+  int qtiles;  // extend query tiles
+  bool bad;
+};
+
+struct Sums {
+  long long np, qo, ns, pr, qt, npqo;
+  int maxqo;
+};
+
+struct MetaArgs {
+  int* plan;
+  int* kv_indptr;
+  int* kv_indices;
+  int* kv_last_page_len;
+  int* qo_indptr;
+  int* kv_len;
+  int* n_splits;
+  int* partial_indptr;
+  int* token_req;
+  DecodeItem* items;
+  ExtendTile* tiles;
+  const int* seq_lens;
+  const int* qo_lens;  // may be null: one row per request
+  const int* page_table;
+  int stride;
+  int bs;
+  int num_pages;
+  int group;  // num_q_heads / num_kv_heads
+  int num_kv_heads;
+  int stage_pages;  // the decode kernel's pages per pipeline stage
+  int units_target;
+  int partial_cap;
+  int max_pages_total;
+  int max_q_tokens;
+  int max_items;
+  int max_tiles;
+};
+
+__device__ __forceinline__ void raw_lengths(const MetaArgs& a, int b, int& L, int& qo, bool& bad) {
+  L = a.seq_lens[b];
+  qo = a.qo_lens ? a.qo_lens[b] : 1;
+  bad = (L < 0) || (qo < 0) || (L > 0 && qo > L);
+  if (bad) {
+    L = 0;
+    qo = qo < 0 ? 0 : qo;
+  }
+}
+
+__device__ __forceinline__ ReqInfo req_info(const MetaArgs& a, int b, int chunk) {
+  ReqInfo r;
+  raw_lengths(a, b, r.L, r.qo, r.bad);
+  r.np = (r.L + kPageSize - 1) / kPageSize;
+  r.nsplit = r.np > 0 ? (r.np + chunk - 1) / chunk : 1;
+  r.prow = r.nsplit > 1 ? r.nsplit * r.qo : 0;
+  r.qtiles = (r.qo * a.group + kExtendRows - 1) / kExtendRows;
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ int warp_max(int v) {
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum of a Sums record (result valid in every thread).
+__device__ Sums block_sum(Sums s) {
+  __shared__ long long red[6][kThreads / 32];
+  __shared__ int redm[kThreads / 32];
+  int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  s.np = warp_sum(s.np);
+  s.qo = warp_sum(s.qo);
+  s.ns = warp_sum(s.ns);
+  s.pr = warp_sum(s.pr);
+  s.qt = warp_sum(s.qt);
+  s.npqo = warp_sum(s.npqo);
+  s.maxqo = warp_max(s.maxqo);
+  __syncthreads();
+  if (l == 0) {
+    red[0][w] = s.np;
+    red[1][w] = s.qo;
+    red[2][w] = s.ns;
+    red[3][w] = s.pr;
+    red[4][w] = s.qt;
+    red[5][w] = s.npqo;
+    redm[w] = s.maxqo;
+  }
+  __syncthreads();
+  Sums t{0, 0, 0, 0, 0, 0, 0};
+  for (int i = 0; i < kThreads / 32; ++i) {
+    t.np += red[0][i];
+    t.qo += red[1][i];
+    t.ns += red[2][i];
+    t.pr += red[3][i];
+    t.qt += red[4][i];
+    t.npqo += red[5][i];
+    t.maxqo = max(t.maxqo, redm[i]);
+  }
+  return t;
+}
+
+// Exclusive block scan of five ints; returns this thread's prefix and the tile total.
+struct Scan5 {
+  int v[5];
+};
+__device__ Scan5 block_exclusive_scan(const Scan5& x, Scan5& total) {
+  __shared__ int part[5][kThreads / 32];
+  int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  Scan5 inc = x;
+  for (int k = 0; k < 5; ++k) {
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, inc.v[k], o);
+      if (l >= o) inc.v[k] += y;
+    }
+  }
+  __syncthreads();
+  if (l == 31)
+    for (int k = 0; k < 5; ++k) part[k][w] = inc.v[k];
+  __syncthreads();
+  Scan5 ex;
+  for (int k = 0; k < 5; ++k) {
+    int before = 0, all = 0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+      if (i < w) before += part[k][i];
+      all += part[k][i];
+    }
+    ex.v[k] = before + inc.v[k] - x.v[k];
+    total.v[k] = all;
+  }
+  return ex;
+}
+
+__global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
+  // ---- 1. batch totals (identical in every CTA) ----
+  Sums s{0, 0, 0, 0, 0, 0, 0};
+  for (int b = threadIdx.x; b < a.bs; b += kThreads) {
+    int L, qo;
+    bool bad;
+    raw_lengths(a, b, L, qo, bad);
+    long long np = (L + kPageSize - 1) / kPageSize;
+    s.np += np;
+    s.qo += qo;
+    s.npqo += np * qo;
+    s.maxqo = max(s.maxqo, qo);
+  }
+  Sums tot = block_sum(s);
+  bool over = tot.np > a.max_pages_total || tot.qo > a.max_q_tokens || tot.qo >= a.partial_cap;
+
+  // decode split size: fill the grid, never finer than the minimum chunk, and
+  // keep sum over split requests of nsplit*qo below the partial buffer
+  long long chunk = (tot.np * a.num_kv_heads + a.units_target - 1) / a.units_target;
+  if (chunk < kDecodeMinChunkPages) chunk = kDecodeMinChunkPages;
+  long long room = (long long)a.partial_cap - tot.qo;
+  if (room > 0) {
+    long long c2 = (tot.npqo + room - 1) / room;
+    if (c2 > chunk) chunk = c2;
+  }
+  chunk = (chunk + a.stage_pages - 1) / a.stage_pages * a.stage_pages;
+  if (chunk > (1 << 30)) chunk = 1 << 30;
+  int ichunk = (int)chunk;
+
+  if (over) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      record_error(a.plan, PKV_DEV_CAPACITY, (int)tot.np);
+      a.plan[kBatch] = 0;
+      a.plan[kTotalPages] = 0;
+      a.plan[kTotalQ] = 0;
+      a.plan[kDecodeItems] = 0;
+      a.plan[kExtendTiles] = 0;
+      a.plan[kPartialRows] = 0;
+      a.plan[kChunkPages] = ichunk;
+      a.plan[kMaxQo] = 0;
+    }
+    return;
+  }
+
+  // ---- 2. this CTA's request range and the prefix before it ----
+  int per = (a.bs + gridDim.x - 1) / gridDim.x;
+  int b0 = min(a.bs, (int)blockIdx.x * per), b1 = min(a.bs, b0 + per);
+  Sums pre{0, 0, 0, 0, 0, 0, 0};
+  for (int b = threadIdx.x; b < b0; b += kThreads) {
+    ReqInfo r = req_info(a, b, ichunk);
+    pre.np += r.np;
+    pre.qo += r.qo;
+    pre.ns += r.nsplit;
+    pre.pr += r.prow;
+    pre.qt += r.qtiles;
+  }
+  Sums base = block_sum(pre);
+  // totals of the scanned quantities over the whole batch (for the plan words)
+  Sums all{0, 0, 0, 0, 0, 0, 0};
+  if (blockIdx.x == 0) {
+    for (int b = threadIdx.x; b < a.bs; b += kThreads) {
+      ReqInfo r = req_info(a, b, ichunk);
+      all.ns += r.nsplit;
+      all.pr += r.prow;
+      all.qt += r.qtiles;
+    }
+    all = block_sum(all);
+  }
+
+  // ---- 3. scan the range tile by tile ----
+  Scan5 carry{{(int)base.np, (int)base.qo, (int)base.ns, (int)base.pr, (int)base.qt}};
+  __shared__ int s_np[kThreads], s_pbase[kThreads];
+  for (int t0 = b0; t0 < b1; t0 += kThreads) {
+    int b = t0 + threadIdx.x;
+    ReqInfo r{0, 0, 0, 0, 0, 0, false};
+    bool live = b < b1;
+    if (live) r = req_info(a, b, ichunk);
+    Scan5 x{{r.np, r.qo, r.nsplit, r.prow, r.qtiles}};
+    if (!live) x = Scan5{{0, 0, 0, 0, 0}};
+    Scan5 tile_tot;
+    Scan5 ex = block_exclusive_scan(x, tile_tot);
+    int p_np = carry.v[0] + ex.v[0], p_qo = carry.v[1] + ex.v[1], p_ns = carry.v[2] + ex.v[2];
+    int p_pr = carry.v[3] + ex.v[3], p_qt = carry.v[4] + ex.v[4];
+    s_np[threadIdx.x] = live ? r.np : 0;
+    s_pbase[threadIdx.x] = p_np;
+    if (live) {
+      if (r.bad) record_error(a.plan, PKV_DEV_BAD_LENGTH, b);
+      a.kv_indptr[b] = p_np;
+      a.qo_indptr[b] = p_qo;
+      a.partial_indptr[b] = p_pr;
+      a.kv_len[b] = r.L;
+      a.n_splits[b] = r.nsplit;
+      a.kv_last_page_len[b] = r.np > 0 ? r.L - (r.np - 1) * kPageSize : 0;
+      if (b == a.bs - 1) {
+        a.kv_indptr[a.bs] = p_np + r.np;
+        a.qo_indptr[a.bs] = p_qo + r.qo;
+        a.partial_indptr[a.bs] = p_pr + r.prow;
+      }
+      for (int sp = 0; sp < r.nsplit; ++sp) {
+        int idx = p_ns + sp;
+        if (idx < a.max_items) {
+          DecodeItem it;
+          it.b = b;
+          it.split = sp;
+          it.p0 = sp * ichunk;
+          it.p1 = min(r.np, (sp + 1) * ichunk);
+          a.items[idx] = it;
+        }
+      }
+      int rows = r.qo * a.group;
+      int prefix = r.L - r.qo;
+      for (int qt = 0; qt < r.qtiles; ++qt) {
+        int idx = p_qt + qt;
+        if (idx < a.max_tiles) {
+          int last_row = min((qt + 1) * kExtendRows, rows) - 1;
+          int last_tok = last_row / a.group;
+          ExtendTile et;
+          et.b = b;
+          et.row0 = qt * kExtendRows;
+          et.kv_tiles = r.L > 0 ? (prefix + last_tok + 1 + kExtendKeys - 1) / kExtendKeys : 0;
+          et.pad = 0;
+          a.tiles[idx] = et;
+        }
+      }
+      for (int i = 0; i < r.qo; ++i) a.token_req[p_qo + i] = b;
+    }
+    __syncthreads();
+    // copy the page-table rows of this tile's requests, one warp per request
+    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int nreq = min(kThreads, b1 - t0);
+    for (int j = warp; j < nreq; j += kThreads / 32) {
+      int bb = t0 + j;
+      int n = s_np[j], dst = s_pbase[j];
+      const int* row = a.page_table + (long long)bb * a.stride;
+      for (int p = lane; p < n; p += 32) {
+        int page = row[p];
+        if (page < 0 || page >= a.num_pages) {
+          record_error(a.plan, PKV_DEV_BAD_PAGE, bb);
+          page = 0;
+        }
+        a.kv_indices[dst + p] = page;
+      }
+    }
+    for (int k = 0; k < 5; ++k) carry.v[k] += tile_tot.v[k];
+    __syncthreads();
+  }
+
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (a.bs == 0) {
+      a.kv_indptr[0] = 0;
+      a.qo_indptr[0] = 0;
+      a.partial_indptr[0] = 0;
+    }
+    bool items_over = all.ns > a.max_items || all.qt > a.max_tiles;
+    if (items_over) record_error(a.plan, PKV_DEV_CAPACITY, -1);
+    a.plan[kBatch] = a.bs;
+    a.plan[kTotalPages] = (int)tot.np;
+    a.plan[kTotalQ] = (int)tot.qo;
+    a.plan[kDecodeItems] = items_over ? 0 : (int)all.ns;
+    a.plan[kChunkPages] = ichunk;
+    a.plan[kExtendTiles] = items_over ? 0 : (int)all.qt;
+    a.plan[kPartialRows] = (int)all.pr;
+    a.plan[kMaxQo] = tot.maxqo;
+  }
+}
+
+}  // namespace
+
+int launch_build_metadata(Ctx& c, int batch, const int32_t* seq_lens, const int32_t* qo_lens,
+                          const int32_t* page_table, int stride, cudaStream_t st) {
+  Meta m = make_meta(c);
+  MetaArgs a;
+  a.plan = m.plan;
+  a.kv_indptr = const_cast<int*>(m.kv_indptr);
+  a.kv_indices = const_cast<int*>(m.kv_indices);
+  a.kv_last_page_len = const_cast<int*>(m.kv_last_page_len);
+  a.qo_indptr = const_cast<int*>(m.qo_indptr);
+  a.kv_len = const_cast<int*>(m.kv_len);
+  a.n_splits = const_cast<int*>(m.n_splits);
+  a.partial_indptr = const_cast<int*>(m.partial_indptr);
+  a.token_req = const_cast<int*>(m.token_req);
+  a.items = const_cast<DecodeItem*>(m.decode_items);
+  a.tiles = const_cast<ExtendTile*>(m.extend_tiles);
+  a.seq_lens = seq_lens;
+  a.qo_lens = qo_lens;
+  a.page_table = page_table;
+  a.stride = stride;
+  a.bs = batch;
+  a.num_pages = c.cfg.num_pages;
+  a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
+  a.num_kv_heads = c.cfg.num_kv_heads;
+  a.stage_pages = c.cfg.kv_dtype == PKV_KV_FP8_E4M3 ? 8 : 4;
+  a.units_target = c.decode_ctas * kDecodeTargetWaves;
+  a.partial_cap = c.lay.partial_rows_cap;
+  a.max_pages_total = c.cfg.max_pages_total;
+  a.max_q_tokens = c.cfg.max_q_tokens;
+  a.max_items = c.lay.max_decode_items;
+  a.max_tiles = c.lay.max_extend_tiles;
+  int grid = batch < 1 ? 1 : (batch < kMaxCtas ? batch : kMaxCtas);
+  build_metadata_kernel<<<grid, kThreads, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

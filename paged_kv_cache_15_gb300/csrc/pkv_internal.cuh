@@ -1,0 +1,265 @@
+// Internal declarations shared by the library's translation units: workspace
+// layout, launch parameter blocks, and small inline-PTX helpers for sm_103a
+// (mbarrier with bounded waits, TMA tensor loads, ldmatrix, warp-level MMA).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Fixed tiling constants
+// ---------------------------------------------------------------------------
+constexpr int kPageSize = 16;           // the only page size this build accepts
+constexpr int kDecodeTargetWaves = 4;   // split-KV aims at this many work units per CTA slot
+constexpr int kDecodeMinChunkPages = 8; // never cut a (request, head) range finer than 128 keys
+constexpr int kExtendRows = 128;        // query rows (token x head-in-group) per extend tile
+constexpr int kExtendKeys = 128;        // keys per extend KV tile
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s bound on any mbarrier wait
+
+// Device error codes beyond the public PKV_DEV_* values
+constexpr int kDevTimeout = 16;
+
+// ---------------------------------------------------------------------------
+// Plan header (int32 words at the start of the workspace)
+// ---------------------------------------------------------------------------
+enum PlanWord : int {
+  kErr = 0,            // first device error (PKV_DEV_*), 0 when clean
+  kErrIndex = 1,       // index that raised it
+  kBatch = 2,          // batch size of the last build
+  kTotalPages = 3,     // kv_indptr[bs]
+  kTotalQ = 4,         // qo_indptr[bs]
+  kDecodeItems = 5,    // number of (request, split) items on the decode path
+  kChunkPages = 6,     // pages per split on the decode path
+  kExtendTiles = 7,    // number of (request, q-tile) items on the extend path
+  kPartialRows = 8,    // rows of the partial-output buffer in use
+  kMaxQo = 9,          // max qo_len in the batch
+  kPlanWords = 32
+};
+
+// Work item of the decode path: request, split index, page range [p0, p1).
+struct DecodeItem {
+  int b, split, p0, p1;
+};
+// Work item of the extend path: request, first query row (token * group + head-in-group).
+struct ExtendTile {
+  int b, row0, kv_tiles, pad;
+};
+
+// Byte offsets of every buffer inside the caller's workspace.
+struct Layout {
+  size_t plan, kv_indptr, kv_indices, kv_last_page_len, qo_indptr, kv_len, n_splits, partial_indptr, token_req,
+      decode_items, extend_tiles, partial_o, partial_lse, total;
+  int max_decode_items, max_extend_tiles, partial_rows_cap;
+};
+
+struct Ctx {
+  pkv_config cfg;
+  Layout lay;
+  char* ws;  // device workspace base
+  int num_sms;
+  int decode_ctas;  // persistent grid of the decode kernel
+  int extend_ctas;
+  int batch;  // batch size of the last pkv_build_metadata
+  int mode;
+  bool qo_given;  // last build had explicit qo_lens
+  int device;
+};
+
+// Device-side view of the metadata in the workspace.
+struct Meta {
+  int* plan;
+  const int* kv_indptr;
+  const int* kv_indices;
+  const int* kv_last_page_len;
+  const int* qo_indptr;
+  const int* kv_len;
+  const int* n_splits;
+  const int* partial_indptr;
+  const int* token_req;
+  const DecodeItem* decode_items;
+  const ExtendTile* extend_tiles;
+  float* partial_o;
+  float* partial_lse;
+};
+
+Meta make_meta(const Ctx& c);
+
+// Entry points of the kernels' host launchers (one per translation unit).
+int launch_build_metadata(Ctx& c, int batch, const int32_t* seq_lens, const int32_t* qo_lens,
+                          const int32_t* page_table, int stride, cudaStream_t st);
+int launch_set_kv_buffer(Ctx& c, void* k_pool, void* v_pool, const int32_t* loc, const void* k, const void* v,
+                         int n, float k_inv, float v_inv, cudaStream_t st);
+int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+                  float v_scale, void* out, float* lse, cudaStream_t st);
+int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, void* out,
+                  float* lse, cudaStream_t st);
+
+// Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
+int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                   CUtensorMapSwizzle swz);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void record_error(int* plan, int code, int index) {
+  if (atomicCAS(&plan[kErr], 0, code) == 0) plan[kErrIndex] = index;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete. Bounded: gives up
+// after kWaitTimeoutNs, records kDevTimeout and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* plan) {
+  if (mbar_try_wait(bar, parity)) return true;
+  unsigned long long t0 = global_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitTimeoutNs) {
+      record_error(plan, kDevTimeout, 0);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// TMA: 2-D tiled load into shared memory, completion counted on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (low byte first) -> two f16 in one register (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace pkv

@@ -1,0 +1,281 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Metadata and KV scatter must be bit-exact. Attention outputs (bf16) and LSE
+(fp32) must satisfy |got - ref| <= 1e-2 + 1e-2 |ref| element by element: bf16
+output rounding (2^-9 relative) and fp32 accumulation with bf16 (FP8 pools:
+f16) MMA operands stay well inside that bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_15_gb300 import binding as B
+from paged_kv_cache_15_gb300.runner import DeviceBatch, config_for
+from paged_kv_cache_15_gb300.workloads import make_workload, pool_bits, preset
+from tests._pipeline import oracle_meta, oracle_pools, oracle_reference, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built():
+    from paged_kv_cache_15_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def check_close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    both_ninf = np.isneginf(got) & np.isneginf(ref)
+    err = np.where(both_ninf, 0.0, np.abs(got - ref))
+    tol = ATOL + RTOL * np.abs(np.where(both_ninf, 0.0, ref))
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; first at {idx}: "
+                             f"got {got[idx]} ref {ref[idx]}")
+
+
+def run_path(W, spec_mode=B.PKV_SPEC_PREFILL, cfg=None):
+    d = DeviceBatch(W, cfg=cfg)
+    d.step(spec_mode)
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    return d
+
+
+def full_check(W, spec_mode=B.PKV_SPEC_PREFILL):
+    d = run_path(W, spec_mode)
+    ref_o, ref_lse = oracle_reference(W)
+    check_close(d.out.double().cpu().numpy(), ref_o, "o")
+    check_close(d.lse.double().cpu().numpy(), ref_lse, "lse")
+    return d
+
+
+def sampled_check(W, n_rows=96, spec_mode=B.PKV_SPEC_PREFILL):
+    d = run_path(W, spec_mode)
+    rows = sample_rows(W, n_rows)
+    ref_o, ref_lse = oracle_reference(W, rows=rows)
+    out = d.out.double().cpu().numpy()
+    lse = d.lse.double().cpu().numpy()
+    check_close(out[rows[:, 0], rows[:, 1]], ref_o, "o (sampled)")
+    check_close(lse[rows[:, 0], rows[:, 1]], ref_lse, "lse (sampled)")
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    return d
+
+
+def workspace_ints(d: DeviceBatch, ptr: int, n: int) -> np.ndarray:
+    """int32 view of n values at a device address inside the context's workspace."""
+    ws = d.attn.workspace
+    off = ptr - ws.data_ptr()
+    assert 0 <= off and off + 4 * n <= ws.numel()
+    return ws[off:off + 4 * n].view(torch.int32).cpu().numpy()
+
+
+# ------------------------------------------------------------------ metadata
+def _meta_case(name):
+    if name == "tiny_decode":
+        return preset("tiny_decode")
+    if name == "decode_ragged":
+        return make_workload("r", "decode", 37, 8, 2, 64, np.arange(37) * 29 % 700, np.ones(37))
+    if name == "extend":
+        return preset("prefix_extend", bs=5, len_scale=0.25)
+    if name == "verify":
+        return preset("spec_verify", bs=6, len_scale=0.1)
+    if name == "many_requests":
+        rng = np.random.default_rng(3)
+        return make_workload("m", "extend", 300, 4, 2, 64, rng.integers(0, 90, 300), rng.integers(1, 20, 300))
+    raise KeyError(name)
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "decode_ragged", "extend", "verify", "many_requests"])
+def test_metadata_bit_exact(name):
+    W = _meta_case(name)
+    d = DeviceBatch(W)
+    d.build_metadata()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    ref = oracle_meta(W)
+    p_indptr, p_indices, p_last, p_qo = B.pkv_get_metadata(d.ctx)
+    bs = W.bs
+    n_pages = int(ref["kv_indptr"][-1])
+    assert np.array_equal(workspace_ints(d, p_indptr, bs + 1), ref["kv_indptr"])
+    assert np.array_equal(workspace_ints(d, p_indices, n_pages), ref["kv_indices"])
+    assert np.array_equal(workspace_ints(d, p_last, bs), ref["kv_last_page_len"])
+    assert np.array_equal(workspace_ints(d, p_qo, bs + 1), ref["qo_indptr"])
+
+
+# ------------------------------------------------------------------ set_kv_buffer
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_set_kv_buffer_bit_exact(kv_dtype):
+    W = make_workload("s", "extend", 6, 16, 8, 128, [0, 40, 7, 100, 3, 64], [37, 16, 1, 200, 90, 5],
+                      kv_dtype=kv_dtype)
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    kp, vp = oracle_pools(W)
+    assert np.array_equal(pool_bits(d.k_pool.cpu()), kp)
+    assert np.array_equal(pool_bits(d.v_pool.cpu()), vp)
+
+
+def test_set_kv_buffer_fp8_saturates_like_oracle():
+    W = make_workload("sat", "extend", 1, 8, 8, 128, [0], [64], kv_dtype="fp8_e4m3")
+    W.k_new.mul_(300.0)  # many values beyond +-448 after scaling
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    torch.cuda.synchronize()
+    kp, _ = oracle_pools(W)
+    assert np.array_equal(pool_bits(d.k_pool.cpu()), kp)
+
+
+def test_set_kv_buffer_bad_slot_recorded_and_skipped():
+    W = make_workload("bad", "extend", 1, 8, 8, 128, [0], [4])
+    W.loc[2] = W.num_slots + 10
+    d = DeviceBatch(W)
+    before = pool_bits(d.k_pool.cpu()).copy()
+    d.set_kv_buffer()
+    assert d.device_error() == B.PKV_DEV_BAD_SLOT
+    after = pool_bits(d.k_pool.cpu())
+    assert np.array_equal(np.delete(after, W.loc[[0, 1, 3]], axis=0), np.delete(before, W.loc[[0, 1, 3]], axis=0))
+
+
+# ------------------------------------------------------------------ decode
+@pytest.mark.parametrize("case", ["tiny", "llama_small", "fp8_small", "ragged_short", "single_key"])
+def test_decode_parity(case):
+    if case == "tiny":
+        W = preset("tiny_decode")
+    elif case == "llama_small":
+        W = preset("llama3_8b_decode", bs=8, len_scale=0.25)
+    elif case == "fp8_small":
+        W = preset("long_fp8_decode", bs=4, len_scale=1 / 16)
+    elif case == "ragged_short":
+        rng = np.random.default_rng(9)
+        W = make_workload("rs", "decode", 21, 32, 8, 128, rng.integers(0, 300, 21), np.ones(21))
+    elif case == "single_key":
+        W = make_workload("one", "decode", 3, 8, 2, 64, [0, 0, 0], [1, 1, 1])
+    full_check(W)
+
+
+def test_decode_padding_requests_give_zero_and_neg_inf():
+    W = make_workload("pad", "decode", 4, 8, 2, 64, [50, 0, 17, 0], [1, 0, 1, 0])
+    W_dec = make_workload("pad", "decode", 4, 8, 2, 64, [50, 0, 17, 0], [1, 0, 1, 0])
+    # two padding requests with seq_len 0 but one query row each, as a padded graph batch has
+    W_dec.seq_lens[:] = [51, 0, 18, 0]
+    W_dec.qo_lens[:] = 1
+    q = torch.zeros((4, 8, 64), dtype=torch.bfloat16)
+    q[[0, 2]] = W.q
+    W_dec.q = q
+    d = run_path(W_dec)
+    out = d.out.float().cpu().numpy()
+    lse = d.lse.cpu().numpy()
+    assert np.all(out[[1, 3]] == 0) and np.all(np.isneginf(lse[[1, 3]]))
+    ref_o, ref_lse = oracle.attention(
+        np.ascontiguousarray(q.view(torch.int16).numpy().view(np.uint16)), *oracle_pools(W_dec),
+        oracle.build_metadata(W_dec.seq_lens, W_dec.page_table, 16), 8, 2, 16, W_dec.sm_scale)
+    check_close(out, ref_o, "o")
+    check_close(lse, ref_lse, "lse")
+
+
+def test_decode_nan_unused_slots_never_read():
+    # workloads fill every slot that holds no token with NaN; a read of one shows up as NaN
+    W = preset("llama3_8b_decode", bs=16, len_scale=0.05)
+    d = run_path(W)
+    assert torch.isfinite(d.out.float()).all() and torch.isfinite(d.lse).all()
+
+
+def test_idle_and_empty_batch_are_no_ops():
+    W = preset("tiny_decode")
+    d = DeviceBatch(W)
+    d.out.fill_(7.0)
+    B.pkv_build_metadata(d.ctx, B.PKV_MODE_IDLE, 0, None, None, None)
+    B.pkv_forward(d.ctx, B.PKV_MODE_IDLE, B.PKV_SPEC_PREFILL, d.q, d.k_pool, d.v_pool, 1.0, d.out, d.lse)
+    torch.cuda.synchronize()
+    assert torch.all(d.out.float() == 7.0)
+
+
+# ------------------------------------------------------------------ verify on the decode path
+@pytest.mark.parametrize("bs,len_scale", [(8, 0.1), (3, 0.02)])
+def test_verify_decode_path_parity(bs, len_scale):
+    W = preset("spec_verify", bs=bs, len_scale=len_scale)
+    full_check(W, spec_mode=B.PKV_SPEC_DECODE)
+
+
+def test_verify_decode_path_fp8():
+    W = make_workload("vf8", "verify", 5, 32, 8, 128, [100, 2000, 517, 33, 4096], [4, 8, 5, 7, 6],
+                      kv_dtype="fp8_e4m3")
+    full_check(W, spec_mode=B.PKV_SPEC_DECODE)
+
+
+# ------------------------------------------------------------------ full sizes, sampled rows
+@pytest.mark.parametrize("name", ["llama3_8b_decode", "long_fp8_decode"])
+def test_full_size_decode_sampled(name):
+    sampled_check(preset(name))
+
+
+def test_full_size_verify_decode_path_sampled():
+    sampled_check(preset("spec_verify"), spec_mode=B.PKV_SPEC_DECODE)
+
+
+# ------------------------------------------------------------------ device-side data errors
+def test_bad_page_id_recorded_without_fault():
+    W = preset("tiny_decode")
+    W.page_table[1, 2] = W.num_pages + 3
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    d.build_metadata()
+    d.forward()
+    assert d.device_error() == B.PKV_DEV_BAD_PAGE
+    assert d.device_error() == 0  # reading clears the word
+
+
+def test_capacity_overflow_recorded():
+    W = preset("tiny_decode")
+    cfg = config_for(W, max_pages_total=10)
+    d = DeviceBatch(W, cfg=cfg)
+    d.build_metadata()
+    assert d.device_error() == B.PKV_DEV_CAPACITY
+
+
+# ------------------------------------------------------------------ CUDA graph capture / replay
+def test_graph_replay_with_new_lengths():
+    """Capture save_kv_cache + metadata + decode once, replay with other lengths."""
+    shape = dict(bs=6, num_q_heads=32, num_kv_heads=8, head_dim=128)
+    pages = 700
+    W1 = make_workload("g1", "decode", 6, 32, 8, 128, [1500, 30, 700, 2047, 5, 999], np.ones(6), num_pages=pages)
+    W2 = make_workload("g2", "decode", 6, 32, 8, 128, [100, 2500, 16, 1, 1300, 444], np.ones(6), num_pages=pages)
+    width = max(W1.page_table.shape[1], W2.page_table.shape[1])
+    cfg = config_for(W1, max_pages_total=pages - 1)
+    d = DeviceBatch(W1, cfg=cfg)
+    d.page_table = torch.zeros((6, width), dtype=torch.int32, device="cuda")
+    d.page_table[:, :W1.page_table.shape[1]] = torch.from_numpy(W1.page_table)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d.step()  # warm-up outside the graph
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d.step()
+    for W in (W1, W2):
+        d.q.copy_(W.q)
+        d.k_pool.copy_(W.k_pool)
+        d.v_pool.copy_(W.v_pool)
+        d.k_new.copy_(W.k_new)
+        d.v_new.copy_(W.v_new)
+        d.loc.copy_(torch.from_numpy(W.loc))
+        d.seq_lens.copy_(torch.from_numpy(W.seq_lens))
+        d.page_table.zero_()
+        d.page_table[:, :W.page_table.shape[1]] = torch.from_numpy(W.page_table)
+        g.replay()
+        torch.cuda.synchronize()
+        assert d.device_error() == 0
+        ref_o, ref_lse = oracle_reference(W)
+        check_close(d.out.double().cpu().numpy(), ref_o, f"o ({W.name})")
+        check_close(d.lse.double().cpu().numpy(), ref_lse, f"lse ({W.name})")
