@@ -1,0 +1,388 @@
+"""Benchmark of the paged-KV attention hot path on GB300.
+
+One step = one batch of one layer through the whole path: save_kv_cache
+(pkv_set_kv_buffer for the step's new tokens), the metadata build, and the
+ForwardMode-dispatched forward (decode, extend or verify). Inputs are seeded
+synthetic tensors shaped like the pages' serving cases (no dataset, no
+weights); the KV pools are resident in HBM and larger than L2 for every
+named workload, so timed iterations do not run from L2.
+
+Default workload: Llama-3-8B-shaped paged decode (batch 64, 32/8 heads,
+head_dim 128, contexts uniform in [1024, 8192], page_size 16). The metric is
+KV GB/s of the step (algorithmic K+V bytes read / step time); extend workloads
+report TFLOP/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--spec-mode prefill|decode]
+
+With --gpus N > 1 (launched by torch.distributed.run), every rank runs its own
+replica of the workload on its own GPU ("replicas only": the path has no
+exchange step); value = all ranks' work / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged decode KV GB/s (% HBM peak); extend TFLOP/s (% bf16 peak); µs/call"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM traffic per launch of the dominant kernel from one ncu capture
+# (profiles/), valid only while the kernel source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def src_sha(name):
+    with open(os.path.join(ROOT, "paged_kv_cache_15_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def work_of(W):
+    """Algorithmic work of one forward over workload W.
+
+    bytes: K and V of every visible key of every (request, KV head) once, plus
+    Q in, O out, LSE out, page indices. flops: 4 * D per (query row, visible
+    key) pair (QK^T and PV multiply-adds)."""
+    esz = 1 if W.is_fp8 else 2
+    L = W.seq_lens.astype(np.int64)
+    kv_bytes = int(L.sum()) * W.num_kv_heads * W.head_dim * esz * 2
+    T = W.total_q
+    io_bytes = T * W.num_q_heads * W.head_dim * 2 * 2 + T * W.num_q_heads * 4
+    idx_bytes = int(((L + W.page_size - 1) // W.page_size).sum()) * 4
+    N = W.qo_lens.astype(np.int64)
+    P = L - N
+    pairs = int((N * P + N * (N + 1) // 2).sum())  # visible (row, key) pairs per q-head
+    flops = 4 * W.head_dim * W.num_q_heads * pairs
+    return dict(kv_bytes=kv_bytes, bytes=kv_bytes + io_bytes + idx_bytes, flops=flops, pairs=pairs)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    if n_gpus <= 1 and "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def metric_value(W, work, seconds):
+    """(value, unit) of the workload's headline metric for one step taking `seconds`."""
+    if W.mode == "extend":
+        return work["flops"] / seconds / 1e12, "TFLOP/s"
+    return work["kv_bytes"] / seconds / 1e9, "GB/s"
+
+
+def oracle_sample(W, budget_s=15.0):
+    """Time the fp64 oracle on whole requests of W until about budget_s of CPU work."""
+    sys.path.insert(0, ROOT)
+    import oracle
+    from tests._pipeline import oracle_pools
+    from paged_kv_cache_15_gb300.workloads import bf16_bits
+    kp, vp = oracle_pools(W)
+    meta = oracle.build_metadata(W.seq_lens, W.page_table, W.page_size,
+                                 qo_lens=None if W.mode == "decode" else W.qo_lens)
+    qo_indptr = meta["qo_indptr"]
+    qbits = bf16_bits(W.q)
+    nthreads = os.cpu_count() or 1
+    kv = oracle.KV_FP8_E4M3 if W.is_fp8 else oracle.KV_BF16
+    done_kv = done_pairs = 0
+    t0 = time.perf_counter()
+    n_req = 0
+    esz = 1 if W.is_fp8 else 2
+    for b in range(W.bs):
+        rows = [(t, h) for t in range(qo_indptr[b], qo_indptr[b + 1]) for h in range(W.num_q_heads)]
+        if not rows:
+            continue
+        oracle.attention(qbits, kp, vp, meta, W.num_q_heads, W.num_kv_heads, W.page_size, W.sm_scale, kv_dtype=kv,
+                         k_scale=W.k_scale, v_scale=W.v_scale, rows=np.array(rows), nthreads=nthreads)
+        L, N = int(W.seq_lens[b]), int(W.qo_lens[b])
+        done_kv += L * W.num_kv_heads * W.head_dim * esz * 2
+        done_pairs += N * (L - N) + N * (N + 1) // 2
+        n_req += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    if W.mode == "extend":
+        val, unit = 4 * W.head_dim * W.num_q_heads * done_pairs / dt / 1e12, "TFLOP/s"
+    else:
+        val, unit = done_kv / dt / 1e9, "GB/s"
+    return {"value": val, "unit": unit, "cores": nthreads, "kind": "oracle",
+            "sample": f"{n_req} of {W.bs} requests (all query heads), {dt:.1f} s, fp64 C oracle"}, dt
+
+
+def run_reference(args, W, rank, world):
+    if rank != 0:
+        return
+    per_step = []
+    cpu = None
+    for i in range(args.warmup + args.steps):
+        cpu, dt = oracle_sample(W, budget_s=args.ref_budget)
+        if i >= args.warmup:
+            per_step.append((cpu["value"], dt))
+    value = statistics.median(v for v, _ in per_step)
+    ms = statistics.median(dt for _, dt in per_step) * 1e3
+    cpu["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": cpu["unit"], "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": W.name, "batch": W.bs, "num_q_heads": W.num_q_heads,
+                       "num_kv_heads": W.num_kv_heads, "head_dim": W.head_dim, "page_size": W.page_size,
+                       "kv_dtype": W.kv_dtype},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": cpu["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, W, rank, world, local):
+    from paged_kv_cache_15_gb300 import binding as B
+    from paged_kv_cache_15_gb300.runner import DeviceBatch
+
+    hbm_peak, tf_peak, tf_sust, peak_kind = peaks()
+    spec = B.PKV_SPEC_DECODE if args.spec_mode == "decode" else B.PKV_SPEC_PREFILL
+    d = DeviceBatch(W, device=f"cuda:{local}")
+    work = work_of(W)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        d.set_kv_buffer()
+        d.build_metadata()
+        d.forward(spec)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    err = d.device_error()
+    if err:
+        raise RuntimeError(f"device error {err}")
+
+    # --- device-resident timed region: K steps, events on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        d.set_kv_buffer()
+        d.build_metadata()
+        ev[i][0].record(stream)
+        d.forward(spec)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [a.elapsed_time(b) for a, b in ev]
+    step_s = max_over_ranks(total_ms / args.steps / 1e3, world)
+    fwd_s = max_over_ranks(statistics.mean(fwd_ms) / 1e3, world)
+    launches = 4 * args.steps  # set_kv, metadata, attention kernel, merge (decode) / epilogue (extend)
+
+    # --- end to end through the C ABI with host buffers (pinned), inputs copied every step
+    pin = lambda t: t.pin_memory()
+    h_q = pin(W.q)
+    h_k = pin(W.k_new)
+    h_v = pin(W.v_new)
+    h_loc = pin(torch.from_numpy(W.loc))
+    h_seq = pin(torch.from_numpy(W.seq_lens))
+    h_qo = pin(torch.from_numpy(W.qo_lens))
+    h_pt = pin(torch.from_numpy(W.page_table))
+    h_out = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
+    h_lse = torch.empty(d.lse.shape, dtype=d.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_loc, h_seq, h_pt)) + \
+        (h_qo.numel() * 4 if d.qo_lens is not None else 0)
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
+    e2e_steps = max(1, min(args.steps, 50))
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        d.q.copy_(h_q, non_blocking=True)
+        d.k_new.copy_(h_k, non_blocking=True)
+        d.v_new.copy_(h_v, non_blocking=True)
+        d.loc.copy_(h_loc, non_blocking=True)
+        d.seq_lens.copy_(h_seq, non_blocking=True)
+        if d.qo_lens is not None:
+            d.qo_lens.copy_(h_qo, non_blocking=True)
+        d.page_table.copy_(h_pt, non_blocking=True)
+        step()
+        h_out.copy_(d.out, non_blocking=True)
+        h_lse.copy_(d.lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / e2e_steps / 1e3, world)
+
+    if rank != 0:
+        return
+    value, unit = metric_value(W, work, step_s)
+    value *= world  # every rank ran one replica
+    e2e_value = metric_value(W, work, e2e_s)[0] * world
+    if W.mode == "extend":
+        achieved = work["flops"] / fwd_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": achieved / tf_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                "traffic": None}
+    else:
+        achieved = work["bytes"] / fwd_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} HBM copy", "traffic": None}
+    key = "extend_tc" if W.mode == "extend" or (W.mode == "verify" and spec == B.PKV_SPEC_PREFILL) else \
+        "decode_splitkv"
+    tr = NCU_TRAFFIC.get((key, W.name))
+    if tr and tr["src_sha"] == src_sha("extend.cu" if key == "extend_tc" else "decode.cu"):
+        roof["traffic"] = tr["bytes_per_launch"]
+    roof["kernel"] = key
+    roof["timed"] = "forward call (attention kernel + merge), CUDA events on the launching stream"
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu, _ = oracle_sample(W, budget_s=args.ref_budget)
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8_e4m3 kv / bf16 q" if W.is_fp8 else "bf16",
+            "data": "synthetic",
+            "config": {"workload": W.name, "batch": W.bs, "num_q_heads": W.num_q_heads,
+                       "num_kv_heads": W.num_kv_heads, "head_dim": W.head_dim, "page_size": W.page_size,
+                       "kv_dtype": W.kv_dtype, "mode": W.mode, "spec_mode": args.spec_mode,
+                       "total_kv_tokens": int(W.seq_lens.sum()), "total_q_rows": W.total_q,
+                       "l2": "inputs larger than L2 (K+V pools "
+                             f"{2 * W.k_pool.numel() * W.k_pool.element_size() / 1e9:.2f} GB)",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_call": fwd_s * 1e6,
+            "step_us": step_s * 1e6,
+            "work": work,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps, "api": "pkv_set_kv_buffer + pkv_build_metadata + pkv_forward"},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "describe": B.pkv_describe(d.ctx)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama3_8b_decode")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--spec-mode", default="prefill", choices=["prefill", "decode"])
+    ap.add_argument("--ref-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    from paged_kv_cache_15_gb300.workloads import preset
+    W = preset(args.workload)
+    if args.impl == "reference":
+        run_reference(args, W, rank, world)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA device")
+        from paged_kv_cache_15_gb300 import build
+        build.build()
+        run_ours(args, W, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

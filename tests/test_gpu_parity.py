@@ -279,3 +279,90 @@ def test_graph_replay_with_new_lengths():
         ref_o, ref_lse = oracle_reference(W)
         check_close(d.out.double().cpu().numpy(), ref_o, f"o ({W.name})")
         check_close(d.lse.double().cpu().numpy(), ref_lse, f"lse ({W.name})")
+
+
+# ------------------------------------------------------------------ extend (tcgen05) and verify on the prefill path
+@pytest.mark.parametrize("case", ["small", "ragged", "d64", "mha", "prefix_zero", "long_new"])
+def test_extend_parity(case):
+    if case == "small":
+        W = make_workload("e", "extend", 3, 8, 2, 128, [0, 37, 200], [130, 9, 61])
+    elif case == "ragged":
+        rng = np.random.default_rng(21)
+        W = make_workload("er", "extend", 9, 32, 8, 128, rng.integers(0, 700, 9), rng.integers(1, 300, 9))
+    elif case == "d64":
+        W = make_workload("e64", "extend", 4, 8, 2, 64, [5, 0, 300, 129], [200, 33, 7, 128])
+    elif case == "mha":
+        W = make_workload("emha", "extend", 2, 4, 4, 128, [100, 17], [150, 260])
+    elif case == "prefix_zero":
+        W = make_workload("ez", "extend", 2, 16, 4, 128, [0, 0], [1, 383])
+    elif case == "long_new":
+        W = preset("prefix_extend", bs=2, len_scale=0.3)
+    full_check(W)
+
+
+def test_extend_rows_exceeding_group_tiles():
+    # group 16: a 128-row tile holds 8 tokens
+    W = make_workload("g16", "extend", 3, 64, 4, 128, [10, 500, 0], [20, 9, 130])
+    full_check(W)
+
+
+@pytest.mark.parametrize("bs,len_scale", [(8, 0.1), (3, 0.02)])
+def test_verify_prefill_path_parity(bs, len_scale):
+    W = preset("spec_verify", bs=bs, len_scale=len_scale)
+    full_check(W, spec_mode=B.PKV_SPEC_PREFILL)
+
+
+def test_verify_paths_agree():
+    """target_verify through the decode path and through the prefill path."""
+    W = preset("spec_verify", bs=6, len_scale=0.05)
+    d1 = run_path(W, spec_mode=B.PKV_SPEC_DECODE)
+    o1, l1 = d1.out.double().cpu().numpy(), d1.lse.double().cpu().numpy()
+    d2 = run_path(W, spec_mode=B.PKV_SPEC_PREFILL)
+    o2, l2 = d2.out.double().cpu().numpy(), d2.lse.double().cpu().numpy()
+    check_close(o1, o2, "decode-path vs prefill-path output")
+    check_close(l1, l2, "decode-path vs prefill-path lse")
+
+
+def test_extend_nan_unused_slots_never_read():
+    W = preset("prefix_extend", bs=4, len_scale=0.05)
+    d = run_path(W)
+    assert torch.isfinite(d.out.float()).all() and torch.isfinite(d.lse).all()
+
+
+def test_extend_fp8_pool_unsupported():
+    W = make_workload("e8", "extend", 1, 8, 2, 128, [10], [20], kv_dtype="fp8_e4m3")
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    d.build_metadata()
+    with pytest.raises(B.PkvError) as ei:
+        d.forward()
+    assert ei.value.status == B.PKV_ERR_UNSUPPORTED
+
+
+def test_full_size_extend_sampled():
+    sampled_check(preset("prefix_extend"), n_rows=48)
+
+
+def test_full_size_verify_prefill_path_sampled():
+    sampled_check(preset("spec_verify"), spec_mode=B.PKV_SPEC_PREFILL)
+
+
+def test_extend_graph_replay():
+    W = make_workload("eg", "extend", 3, 32, 8, 128, [64, 1000, 3], [200, 50, 317])
+    d = DeviceBatch(W)
+    d.step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d.step()
+    torch.cuda.current_stream().wait_stream(s)
+    with torch.cuda.graph(g):
+        d.step()
+    d.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    ref_o, ref_lse = oracle_reference(W)
+    check_close(d.out.double().cpu().numpy(), ref_o, "o (graph)")
+    check_close(d.lse.double().cpu().numpy(), ref_lse, "lse (graph)")
