@@ -18,8 +18,10 @@
  *   anything is launched; a failed check launches nothing.
  * - Pointers named d_* are DEVICE pointers into memory the caller owns (for
  *   example PyTorch tensors). The library never allocates or frees device
- *   memory: its only device state lives in the workspace the caller passes to
- *   pkv_create. Host-side, pkv_create allocates one small context object.
+ *   memory: its device state lives in the workspace the caller passes to
+ *   pkv_create, plus the one fixed scratch array that loading the library
+ *   reserves for pkv_forward_decode_static. Host-side, pkv_create allocates
+ *   one small context object.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream). Work is enqueued asynchronously on it; no call below synchronises
  *   except pkv_get_device_error. pkv_build_metadata, pkv_set_kv_buffer and the
@@ -205,6 +207,42 @@ int pkv_get_device_error(pkv_ctx* ctx, int32_t* code, void* stream);
 /* Write a one-line description of the context (paths, tile shapes, split
  * policy, SM count) into buf (always NUL-terminated when n > 0). */
 int pkv_describe(pkv_ctx* ctx, char* buf, size_t n);
+
+/* ---- decode without any device allocation -------------------------------
+ * The source pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory. pkv_create needs a workspace that
+ * somebody has to cudaMalloc; code running under another framework's caching
+ * allocator (which owns the device memory, so a raw cudaMalloc can fail or
+ * fragment its pool) and latency-critical loops (cudaMalloc / cudaFree can
+ * synchronise the whole device) cannot. This call allocates nothing: its
+ * metadata and split-KV scratch live in one fixed array of
+ * PKV_STATIC_SCRATCH_BYTES in the library's device memory, which every GPU that
+ * loads the library keeps until the process exits.
+ *
+ * It computes exactly what pkv_build_metadata (decode mode, d_qo_lens NULL)
+ * followed by pkv_forward_decode computes, with the same kernels: one query
+ * row per request, d_q / d_out bf16 [batch][num_q_heads][head_dim], d_lse
+ * fp32 [batch][num_q_heads] or NULL, pools as in pkv_forward_decode. The K/V
+ * of this step's tokens must already be in the pools (pkv_set_kv_buffer, or
+ * the caller's own scatter).
+ *   - cfg is checked as by pkv_workspace_bytes; a configuration whose scratch
+ *     needs more than PKV_STATIC_SCRATCH_BYTES on this device (the split-KV
+ *     partial buffer grows with max_q_tokens * num_q_heads * head_dim) returns
+ *     PKV_ERR_CAPACITY and launches nothing.
+ *   - d_error (device int32, nullable) receives the device error word of this
+ *     call (PKV_DEV_*), written on `stream` after the kernels.
+ *   - The first call on each device looks up the array's device address; make
+ *     that first call before any stream capture on that device.
+ *   - Every call on a device shares the one array, and it keeps the previous
+ *     call's contents (the call clears the words that must start at zero).
+ *     Calls whose work overlaps on the GPU (other streams, other host threads)
+ *     race on it: serialise them. */
+#define PKV_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int pkv_forward_decode_static(const pkv_config* cfg, int32_t batch, const int32_t* d_seq_lens,
+                              const int32_t* d_page_table, int32_t page_table_stride, const void* d_q,
+                              const void* d_k_pool, const void* d_v_pool, float sm_scale, float k_scale,
+                              float v_scale, void* d_out, float* d_lse, int32_t* d_error, void* stream);
 
 #ifdef __cplusplus
 }

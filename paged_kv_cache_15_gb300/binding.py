@@ -28,7 +28,8 @@ PKV_KV_BF16, PKV_KV_FP8_E4M3 = 0, 1
 # every function the header declares (checked against include/pkv.h by the tests)
 EXPORTS = ("pkv_status_string", "pkv_workspace_bytes", "pkv_pool_bytes", "pkv_create", "pkv_destroy",
            "pkv_select_backend", "pkv_build_metadata", "pkv_get_metadata", "pkv_set_kv_buffer",
-           "pkv_forward_decode", "pkv_forward_extend", "pkv_forward", "pkv_get_device_error", "pkv_describe")
+           "pkv_forward_decode", "pkv_forward_extend", "pkv_forward", "pkv_get_device_error", "pkv_describe",
+           "pkv_forward_decode_static")
 
 
 class PkvError(RuntimeError):
@@ -78,6 +79,8 @@ def lib():
                                            ctypes.c_float, ctypes.c_float, vp, vp, vp]),
             "pkv_get_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), vp]),
             "pkv_describe": (ctypes.c_int, [vp, ctypes.c_char_p, sz]),
+            "pkv_forward_decode_static": (ctypes.c_int, [cfgp, i32, vp, vp, i32, vp, vp, vp, ctypes.c_float,
+                                                         ctypes.c_float, ctypes.c_float, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -196,6 +199,17 @@ def pkv_describe(ctx) -> str:
     buf = ctypes.create_string_buffer(512)
     _check(lib().pkv_describe(ctx, buf, 512), "pkv_describe")
     return buf.value.decode()
+
+
+def pkv_forward_decode_static(cfg: pkv_config, batch, seq_lens, page_table, q, k_pool, v_pool, sm_scale, out,
+                              lse=None, error=None, k_scale=1.0, v_scale=1.0, stream=None) -> None:
+    """Decode without a context or workspace (scratch lives in the library's
+    fixed device array); see include/pkv.h for who needs this and its limits."""
+    stride = page_table.shape[1] if page_table is not None and page_table.dim() == 2 else 0
+    _check(lib().pkv_forward_decode_static(ctypes.byref(cfg), int(batch), _ptr(seq_lens), _ptr(page_table),
+                                           int(stride), _ptr(q), _ptr(k_pool), _ptr(v_pool), float(sm_scale),
+                                           float(k_scale), float(v_scale), _ptr(out), _ptr(lse), _ptr(error),
+                                           _stream(stream)), "pkv_forward_decode_static")
 
 
 class PagedAttention:

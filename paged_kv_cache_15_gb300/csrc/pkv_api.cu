@@ -161,6 +161,18 @@ int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// Accessors for the allocation-free decode entry point (its own translation unit).
+int static_config_ok(const pkv_config* cfg) { return check_config(cfg); }
+
+size_t static_layout_bytes(const pkv_config& cfg, int num_sms, Layout* lay) {
+  *lay = make_layout(cfg, num_sms);
+  return lay->total;
+}
+
+void static_grid_sizes(int num_sms, int* decode_ctas, int* extend_ctas) {
+  grid_sizes(num_sms, decode_ctas, extend_ctas);
+}
+
 }  // namespace pkv
 
 using namespace pkv;
