@@ -271,7 +271,31 @@ def run_ours(args, W, rank, world, local):
     fwd_ms = [a.elapsed_time(b) for a, b in ev]
     step_s = max_over_ranks(total_ms / args.steps / 1e3, world)
     fwd_s = max_over_ranks(statistics.mean(fwd_ms) / 1e3, world)
-    launches = 4 * args.steps  # set_kv, metadata, attention kernel, merge (decode) / epilogue (extend)
+    launches = (4 if d.mode != B.PKV_MODE_EXTEND and not (d.mode == B.PKV_MODE_TARGET_VERIFY and spec == B.PKV_SPEC_PREFILL) else 3) * args.steps  # set_kv, metadata, attention (+ split merge on the decode path)
+
+    # --- the same step captured once in a CUDA graph and replayed (serving runs decode this way)
+    graph_us = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_us = max_over_ranks(g0.elapsed_time(g1) / args.steps * 1e3, world)
+        del g
 
     # --- end to end through the C ABI with host buffers (pinned), inputs copied every step
     pin = lambda t: t.pin_memory()
@@ -329,7 +353,7 @@ def run_ours(args, W, rank, world, local):
     if tr and tr["src_sha"] == src_sha("extend.cu" if key == "extend_tc" else "decode.cu"):
         roof["traffic"] = tr["bytes_per_launch"]
     roof["kernel"] = key
-    roof["timed"] = "forward call (attention kernel + merge), CUDA events on the launching stream"
+    roof["timed"] = "forward call (attention kernel, plus the split merge kernel on the decode path), CUDA events on the launching stream"
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu, _ = oracle_sample(W, budget_s=args.ref_budget)
@@ -346,6 +370,7 @@ def run_ours(args, W, rank, world, local):
                        "parallelism": f"replicas x{world}"},
             "us_per_call": fwd_s * 1e6,
             "step_us": step_s * 1e6,
+            "graph_step_us": graph_us,
             "work": work,
             "roofline": roof,
             "cpu_baseline": cpu,
@@ -367,6 +392,7 @@ def main():
     ap.add_argument("--spec-mode", default="prefill", choices=["prefill", "decode"])
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     from paged_kv_cache_15_gb300.workloads import preset

@@ -17,7 +17,8 @@
 //     (running max m, running sum l) in registers, in the log2 domain.
 //   * Each unit ends with its normalised output and LSE. A request with one split
 //     writes the final bf16 output directly; otherwise the unit writes an fp32
-//     partial row that the merge kernel combines:
+//     partial row, and a small merge kernel (one CTA per split (request, KV
+//     head) group) combines them:
 //        lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s.
 //   * FP8 E4M3 pools: codes are widened to f16 in registers (cvt e4m3x2 -> f16x2,
 //     exact), the MMAs run in f16 (Q and P rounded to f16), and the per-pool
@@ -91,6 +92,69 @@ __device__ __forceinline__ int ocol(int nt, int q, int e) {
   }
 }
 
+// Combine the nsplit partial rows of one (request, KV head) group:
+//   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s.
+// One warp per row, lanes across head_dim. Lane s holds split s's weight, so
+// the loads of the partial rows do not depend on each other and are issued
+// in batches. Partials were written by other CTAs, so they are read through
+// L2 (ld.global.cg), never from a stale L1 line.
+template <int D>
+__device__ __forceinline__ void merge_group(const DecodeArgs& a, int b, int g, int q0, int qo, int nsplit, int cw,
+                                            int lane, int ncw) {
+  const int G = a.group;
+  const long long pbase = a.m.partial_indptr[b];
+  constexpr int PER = D / 32;
+  for (int r = cw; r < qo * G; r += ncw) {
+    const int i = r / G, h = g * G + r % G;
+    auto lse_of = [&](int sp) {
+      return __ldcg(a.m.partial_lse + (pbase + (long long)sp * qo + i) * a.num_q_heads + h);
+    };
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < nsplit; s0 += 32)
+      if (s0 + lane < nsplit) M = fmaxf(M, lse_of(s0 + lane));
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Z = 0.f;
+    if (M != -INFINITY)
+      for (int s0 = 0; s0 < nsplit; s0 += 32)
+        if (s0 + lane < nsplit) Z += fast_exp2((lse_of(s0 + lane) - M) * kLog2e);
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    const float invZ = Z > 0.f ? 1.f / Z : 0.f;
+    float acc[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+      float my_w = 0.f;
+      if (M != -INFINITY && s0 + lane < nsplit) my_w = fast_exp2((lse_of(s0 + lane) - M) * kLog2e) * invZ;
+      const int n = min(32, nsplit - s0);
+#pragma unroll 8
+      for (int j = 0; j < n; ++j) {
+        const float wgt = __shfl_sync(0xffffffffu, my_w, j);
+        const long long pr = pbase + (long long)(s0 + j) * qo + i;
+        const float* src = a.m.partial_o + (pr * a.num_q_heads + h) * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+          acc[0] += wgt * x.x;
+          acc[1] += wgt * x.y;
+          acc[2] += wgt * x.z;
+          acc[3] += wgt * x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+          acc[0] += wgt * x.x;
+          acc[1] += wgt * x.y;
+        }
+      }
+    }
+    const long long orow = (long long)(q0 + i) * a.num_q_heads + h;
+    uint16_t* dst = a.out + orow * D + lane * PER;
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
+    }
+    if (a.lse && lane == 0) a.lse[orow] = Z > 0.f ? M + __logf(Z) : -INFINITY;
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                      const __grid_constant__ CUtensorMap tmap_v,
@@ -124,14 +188,14 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
   const int n_units = plan[kDecodeItems] * a.num_kv_heads;
 
   if (warp == C::kConsumerWarps) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (one lane)
     if (lane == 0) {
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_v);
       const uint64_t pol = policy_evict_first();
       int slot = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_phase = 0;  // per-slot: issued at least once / parity of last fill
+      uint32_t armed = 0, armed_phase = 0;
       for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
         const DecodeItem it = a.m.decode_items[w / a.num_kv_heads];
         const int g = w % a.num_kv_heads;
@@ -139,7 +203,7 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
         const int npages = it.p1 - it.p0;
         const int nst = (npages + C::kStagePages - 1) / C::kStagePages;
         for (int st = 0; st < nst; ++st) {
-          if (!mbar_wait(&empty[slot], phase ^ 1, plan)) {
+          if (!mbar_wait_ab(&empty[slot], phase ^ 1, plan, s_abort)) {
             *s_abort = 1;
             break;
           }
@@ -165,7 +229,6 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
           }
         }
       }
-      // never leave the CTA with a TMA still writing into shared memory
       for (int s = 0; s < C::STAGES; ++s)
         if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1, plan);
     }
@@ -180,9 +243,10 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
   const int G = a.group;
   int slot = 0;
   uint32_t phase = 0;
+  bool aborted = false;
 
   for (int w = blockIdx.x; w < n_units; w += gridDim.x) {
-    if (*s_abort) break;
+    if (named_bar_or(1, C::kConsumerWarps * 32, *s_abort)) break;
     const DecodeItem it = a.m.decode_items[w / a.num_kv_heads];
     const int g = w % a.num_kv_heads;
     const int b = it.b;
@@ -244,12 +308,12 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
     for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
 
-    bool aborted = false;
     for (int st = 0; st < nst; ++st) {
-      if (!mbar_wait(&full[slot], phase, plan)) {
+      // a failed wait keeps this warp on the common control flow (so every
+      // named barrier still sees all consumer warps); the loop-top vote ends it
+      if (!aborted && !mbar_wait_ab(&full[slot], phase, plan, s_abort)) {
         *s_abort = 1;
         aborted = true;
-        break;
       }
       const uint32_t kbase = smem_u32(smem + slot * C::kStageBytes);
       const uint32_t vbase = kbase + C::kTileBytes;
@@ -413,8 +477,6 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
         }
       }
     }
-    if (aborted) break;
-
     // ---------------------------------------------------------- epilogue
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
@@ -565,65 +627,22 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
         }
       }
     }
+
   }
+
 }
 
-// LSE merge of split partials: one warp per (token, q-head) of requests with
-// more than one split.
+
+// Separate merge: one CTA of 4 warps per (request, KV head) group with splits.
 template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(Meta m, uint16_t* out, float* lse, int num_q_heads,
-                                                           int max_rows) {
-  const int total_q = m.plan[kTotalQ];
-  const int n_rows = min(total_q, max_rows) * num_q_heads;
-  const int lane = threadIdx.x & 31;
-  for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < n_rows; row += gridDim.x * 8) {
-    const int t = row / num_q_heads, h = row % num_q_heads;
-    const int b = m.token_req[t];
-    const int ns = m.n_splits[b];
-    if (ns <= 1) continue;
-    const int q0 = m.qo_indptr[b];
-    const int qo = m.qo_indptr[b + 1] - q0;
-    const long long base = (long long)m.partial_indptr[b] + (t - q0);
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, m.partial_lse[(base + (long long)s * qo) * num_q_heads + h]);
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Z = 0.f;
-    for (int s = lane; s < ns; s += 32) {
-      const float ls = m.partial_lse[(base + (long long)s * qo) * num_q_heads + h];
-      Z += (M == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
-    }
-    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-    constexpr int PER = D / 32;
-    float acc[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-    const float invZ = Z > 0.f ? 1.f / Z : 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const long long pr = base + (long long)s * qo;
-      const float ls = m.partial_lse[pr * num_q_heads + h];
-      if (ls == -INFINITY) continue;
-      const float wgt = fast_exp2((ls - M) * kLog2e) * invZ;
-      const float* src = m.partial_o + (pr * num_q_heads + h) * D + lane * PER;
-      if constexpr (PER == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] += wgt * x.x;
-        acc[1] += wgt * x.y;
-        acc[2] += wgt * x.z;
-        acc[3] += wgt * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] += wgt * x.x;
-        acc[1] += wgt * x.y;
-      }
-    }
-    uint16_t* dst = out + ((long long)t * num_q_heads + h) * D + lane * PER;
-    if constexpr (PER == 4) {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
-    }
-    if (lse && lane == 0) lse[(long long)t * num_q_heads + h] = Z > 0.f ? M + __logf(Z) : -INFINITY;
-  }
+__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a) {
+  const int grp = blockIdx.x;
+  const int b = grp / a.num_kv_heads, g = grp % a.num_kv_heads;
+  if (b >= a.m.plan[kBatch]) return;
+  const int nsplit = a.m.n_splits[b];
+  if (nsplit <= 1) return;
+  const int q0 = a.m.qo_indptr[b];
+  merge_group<D>(a, b, g, q0, a.m.qo_indptr[b + 1] - q0, nsplit, threadIdx.x >> 5, threadIdx.x & 31, 4);
 }
 
 template <class C>
@@ -651,18 +670,12 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
   a.scale_log2 = sm_scale * (fp8 ? k_scale : 1.f) * kLog2e;
   a.v_scale = fp8 ? v_scale : 1.f;
-  static bool attr_set[8] = {false};  // per device is enough: the attribute is per function
-  (void)attr_set;
   cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   decode_splitkv_kernel<C><<<c.decode_ctas, C::kThreads, C::kSmemBytes, st>>>(tk, tv, a);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-  const int rows = c.cfg.max_q_tokens * c.cfg.num_q_heads;
-  int grid = (rows + 7) / 8;
-  if (grid > c.num_sms * 8) grid = c.num_sms * 8;
-  if (grid < 1) grid = 1;
-  decode_merge_kernel<C::D><<<grid, 256, 0, st>>>(a.m, a.out, lse, c.cfg.num_q_heads, c.cfg.max_q_tokens);
+  decode_merge_kernel<C::D><<<c.cfg.max_batch * c.cfg.num_kv_heads, 128, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -238,22 +238,21 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
     all = block_sum(all);
   }
 
-  // ---- 3. scan the range tile by tile ----
+  // ---- 3. scan the range tile by tile; per-element writes spread over the CTA ----
   Scan5 carry{{(int)base.np, (int)base.qo, (int)base.ns, (int)base.pr, (int)base.qt}};
-  __shared__ int s_np[kThreads], s_pbase[kThreads];
+  enum { kNp, kPBase, kQo, kQBase, kNs, kSBase, kQt, kTBase, kL, kInfo };
+  __shared__ int s_info[kThreads][kInfo];
   for (int t0 = b0; t0 < b1; t0 += kThreads) {
-    int b = t0 + threadIdx.x;
+    const int b = t0 + threadIdx.x;
     ReqInfo r{0, 0, 0, 0, 0, 0, false};
-    bool live = b < b1;
+    const bool live = b < b1;
     if (live) r = req_info(a, b, ichunk);
     Scan5 x{{r.np, r.qo, r.nsplit, r.prow, r.qtiles}};
     if (!live) x = Scan5{{0, 0, 0, 0, 0}};
     Scan5 tile_tot;
     Scan5 ex = block_exclusive_scan(x, tile_tot);
-    int p_np = carry.v[0] + ex.v[0], p_qo = carry.v[1] + ex.v[1], p_ns = carry.v[2] + ex.v[2];
-    int p_pr = carry.v[3] + ex.v[3], p_qt = carry.v[4] + ex.v[4];
-    s_np[threadIdx.x] = live ? r.np : 0;
-    s_pbase[threadIdx.x] = p_np;
+    const int p_np = carry.v[0] + ex.v[0], p_qo = carry.v[1] + ex.v[1], p_ns = carry.v[2] + ex.v[2];
+    const int p_pr = carry.v[3] + ex.v[3], p_qt = carry.v[4] + ex.v[4];
     if (live) {
       if (r.bad) record_error(a.plan, PKV_DEV_BAD_LENGTH, b);
       a.kv_indptr[b] = p_np;
@@ -267,50 +266,56 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
         a.qo_indptr[a.bs] = p_qo + r.qo;
         a.partial_indptr[a.bs] = p_pr + r.prow;
       }
-      for (int sp = 0; sp < r.nsplit; ++sp) {
-        int idx = p_ns + sp;
-        if (idx < a.max_items) {
-          DecodeItem it;
-          it.b = b;
-          it.split = sp;
-          it.p0 = sp * ichunk;
-          it.p1 = min(r.np, (sp + 1) * ichunk);
-          a.items[idx] = it;
-        }
-      }
-      int rows = r.qo * a.group;
-      int prefix = r.L - r.qo;
-      for (int qt = 0; qt < r.qtiles; ++qt) {
-        int idx = p_qt + qt;
-        if (idx < a.max_tiles) {
-          int last_row = min((qt + 1) * kExtendRows, rows) - 1;
-          int last_tok = last_row / a.group;
-          ExtendTile et;
-          et.b = b;
-          et.row0 = qt * kExtendRows;
-          et.kv_tiles = r.L > 0 ? (prefix + last_tok + 1 + kExtendKeys - 1) / kExtendKeys : 0;
-          et.pad = 0;
-          a.tiles[idx] = et;
-        }
-      }
-      for (int i = 0; i < r.qo; ++i) a.token_req[p_qo + i] = b;
+      int* inf = s_info[threadIdx.x];
+      inf[kNp] = r.np;
+      inf[kPBase] = p_np;
+      inf[kQo] = r.qo;
+      inf[kQBase] = p_qo;
+      inf[kNs] = r.nsplit;
+      inf[kSBase] = p_ns;
+      inf[kQt] = r.qtiles;
+      inf[kTBase] = p_qt;
+      inf[kL] = r.L;
     }
     __syncthreads();
-    // copy the page-table rows of this tile's requests, one warp per request
-    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int nreq = min(kThreads, b1 - t0);
-    for (int j = warp; j < nreq; j += kThreads / 32) {
-      int bb = t0 + j;
-      int n = s_np[j], dst = s_pbase[j];
-      const int* row = a.page_table + (long long)bb * a.stride;
-      for (int p = lane; p < n; p += 32) {
+    const int nreq = min(kThreads, b1 - t0);
+    for (int j = 0; j < nreq; ++j) {
+      const int bb = t0 + j;
+      const int* inf = s_info[j];
+      const int np = inf[kNp], pbase = inf[kPBase], qo = inf[kQo], qbase = inf[kQBase];
+      const int ns = inf[kNs], sbase = inf[kSBase], qt = inf[kQt], tbase = inf[kTBase], L = inf[kL];
+      const int* __restrict__ row = a.page_table + (long long)bb * a.stride;
+      for (int p = threadIdx.x; p < np; p += kThreads) {
         int page = row[p];
         if (page < 0 || page >= a.num_pages) {
           record_error(a.plan, PKV_DEV_BAD_PAGE, bb);
           page = 0;
         }
-        a.kv_indices[dst + p] = page;
+        a.kv_indices[pbase + p] = page;
       }
+      for (int sp = threadIdx.x; sp < ns; sp += kThreads) {
+        if (sbase + sp < a.max_items) {
+          DecodeItem it;
+          it.b = bb;
+          it.split = sp;
+          it.p0 = sp * ichunk;
+          it.p1 = min(np, (sp + 1) * ichunk);
+          a.items[sbase + sp] = it;
+        }
+      }
+      const int rows = qo * a.group;
+      for (int t = threadIdx.x; t < qt; t += kThreads) {
+        if (tbase + t < a.max_tiles) {
+          const int last_tok = (min((t + 1) * kExtendRows, rows) - 1) / a.group;
+          ExtendTile et;
+          et.b = bb;
+          et.row0 = t * kExtendRows;
+          et.kv_tiles = L > 0 ? (L - qo + last_tok + 1 + kExtendKeys - 1) / kExtendKeys : 0;
+          et.pad = 0;
+          a.tiles[tbase + t] = et;
+        }
+      }
+      for (int i = threadIdx.x; i < qo; i += kThreads) a.token_req[qbase + i] = bb;
     }
     for (int k = 0; k < 5; ++k) carry.v[k] += tile_tot.v[k];
     __syncthreads();

@@ -165,6 +165,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* p
   }
 }
 
+// Same wait, but it also gives up as soon as the CTA's abort flag is set
+// (another role timed out), so one failure stops every waiter quickly.
+__device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t parity, int* plan, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  unsigned long long t0 = global_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitTimeoutNs) {
+      record_error(plan, kDevTimeout, 0);
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -260,6 +276,18 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads, so
+// every one of them takes the same branch afterwards.
+__device__ __forceinline__ int named_bar_or(int id, int threads, int pred) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.s32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(threads)
+      : "memory");
+  return r;
 }
 
 }  // namespace pkv
