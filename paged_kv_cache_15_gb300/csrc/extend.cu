@@ -4,27 +4,29 @@
 // compute). The same kernel runs target-verify on the prefill path ("[SGLang]
 // Hybrid Attention", section "_select_backend: ForwardMode 기반 동적 전환").
 //
-// One work unit = (request, 128-row query tile, KV head). A row is a
-// (query token, head-in-group) pair, so the GQA group shares every K/V tile.
-// The query block attends to the cached prefix plus the new tokens with the
-// causal rule "row of token i sees keys 0 .. P + i" (P = cached prefix).
+// A work unit is (request, 256 query rows, KV head): two 128-row tiles A and
+// B that share every K/V tile. A row is a (query token, head-in-group) pair,
+// so the GQA group shares K/V as well. Row of token i sees keys 0 .. P + i
+// (P = cached prefix of the request).
 //
-// Warp roles (192 threads, one CTA per SM, persistent over units):
-//   warps 0-3  softmax: thread r owns row r (TMEM lane r). Reads S from TMEM,
-//              masks, keeps the running max / sum in the log2 domain, writes
-//              P (bf16) to shared memory, rescales O in TMEM when the max grows
-//              by more than 2^8 (otherwise the stale max is kept: the result is
-//              the same, the factor cancels in O / l), and writes the output.
-//   warp 4     producer: copies the unit's Q rows into shared memory, then
-//              gathers K/V pages with TMA (16-token boxes, 128-byte swizzle)
-//              into a 2-stage ring.
-//   warp 5     MMA: allocates 512 TMEM columns and issues tcgen05.mma
+// Warp roles (320 threads, one CTA per SM, persistent over units):
+//   warps 0-3  softmax A, warps 4-7 softmax B: thread r of a warpgroup owns
+//              row r of its tile (TMEM lane r). It copies its Q row into shared
+//              memory at the start of a unit, reads S from TMEM, masks, keeps
+//              the running max / sum in the log2 domain, writes P (bf16) back
+//              into the first half of its S columns, rescales O in TMEM only
+//              when the max grows by more than 2^8 (the factor cancels in
+//              O / l), and writes the output rows.
+//   warp 8     producer: gathers K and V pages with TMA (one 16-token box per
+//              page and 128-byte column block, 128-byte swizzle) into a 3-deep
+//              K ring and a 2-deep V ring.
+//   warp 9     MMA: owns 512 TMEM columns and issues tcgen05.mma
 //              (kind::f16, bf16 in, fp32 accumulate):
-//                S[slot] = Q K^T   (M=128 rows, N=128 keys, K=head_dim)
-//                O      += P V     (M=128 rows, N=head_dim, K=128 keys)
-//              QK of tile j is issued before PV of tile j-1, so the tensor
-//              core computes the next scores while the softmax warps work.
-// TMEM: S double buffer (columns 0-127, 128-255), O (columns 256-).
+//                S_X = Q_X K^T      (M=128, N=128 keys, K=head_dim; A, B from smem)
+//                O_X += P_X V       (M=128, N=head_dim, K=128 keys; P from TMEM)
+//              in the order PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1), so one
+//              tile's softmax runs while the tensor core works on the other.
+// TMEM columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
 #include <math.h>
 
 #include "pkv_internal.cuh"
@@ -36,26 +38,28 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
 
-template <int D_>
+template <int D_, int NK_, int NV_>
 struct ExtCfg {
   static constexpr int D = D_;
-  static constexpr int kThreads = 192;
-  static constexpr int kColBlocks = D / 64;                 // 128-byte swizzle spans per row
-  static constexpr int kQBytes = kExtendRows * D * 2;       // [cb][128 rows][128 B]
-  static constexpr int kTileBytes = kExtendKeys * D * 2;    // K or V tile
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kPBytes = kExtendRows * kExtendKeys * 2;  // [2][128 rows][128 B]
+  static constexpr int NK = NK_;  // K ring depth
+  static constexpr int NV = NV_;  // V ring depth
+  static constexpr int kThreads = 320;
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;
+  static constexpr int kColBlocks = D / 64;               // 128-byte swizzle spans per row
+  static constexpr int kQBytes = kExtendRows * D * 2;     // one Q tile: [cb][128 rows][128 B]
+  static constexpr int kTileBytes = kExtendKeys * D * 2;  // one K or V tile
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQOff + kQBytes;
-  static constexpr int kPOff = kKVOff + 2 * kStageBytes;
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
-  static constexpr int kNumBars = 15;
+  static constexpr int kKOff = 2 * kQBytes;
+  static constexpr int kVOff = kKOff + NK * kTileBytes;
+  static constexpr int kBarOff = kVOff + NV * kTileBytes;
+  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAbortOff = kTmemSlotOff + 8;
   static constexpr int kSmemBytes = kAbortOff + 8 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kOCol = 256;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(D <= 128, "O needs at most 128 TMEM columns per tile");
 };
 
 struct ExtendArgs {
@@ -72,18 +76,19 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
                                                                    const __grid_constant__ CUtensorMap tmap_v,
                                                                    ExtendArgs a) {
   constexpr int D = C::D;
+  constexpr int NK = C::NK, NV = C::NV;
+  constexpr int kPagesPerTile = kExtendKeys / kPageSize;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;   // [2]
-  uint64_t* kv_empty = bars + 4;  // [2]
-  uint64_t* s_full = bars + 6;    // [2]
-  uint64_t* s_free = bars + 8;    // [2]
-  uint64_t* p_full = bars + 10;   // [2]
-  uint64_t* p_free = bars + 12;   // [2]
-  uint64_t* o_free = bars + 14;
+  uint64_t* q_full = bars;              // [2] tile A, B: Q rows written
+  uint64_t* k_full = bars + 2;          // [NK]
+  uint64_t* k_empty = k_full + NK;      // [NK]
+  uint64_t* v_full = k_empty + NK;      // [NV]
+  uint64_t* v_empty = v_full + NV;      // [NV]
+  uint64_t* s_full = v_empty + NV;      // [2] S_X computed
+  uint64_t* p_full = s_full + 2;        // [2] P_X written
+  uint64_t* pv_done = p_full + 2;       // [2] PV_X finished
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
@@ -91,239 +96,267 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   int* plan = a.m.plan;
 
   if (tid == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 128);
-      mbar_init(&p_full[s], 128);
-      mbar_init(&p_free[s], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&q_full[x], 128);
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&pv_done[x], 1);
     }
-    mbar_init(o_free, 128);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
   }
   // K/V stages start as zeros so rows of a partly loaded tile are finite
-  for (int i = tid; i < 2 * C::kStageBytes / 16; i += C::kThreads)
-    reinterpret_cast<uint4*>(smem + C::kKVOff)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < (NK + NV) * C::kTileBytes / 16; i += C::kThreads)
+    reinterpret_cast<uint4*>(smem + C::kKOff)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  const int n_units = a.m.plan[kExtendTiles] * a.num_kv_heads;
+  const int n_units = plan[kExtendTiles] * a.num_kv_heads;
   const int G = a.group;
   const uint32_t smem_base = smem_u32(smem);
 
-  if (warp == 4) {
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol = policy_evict_first();
     if (lane == 0) {
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_v);
-    }
-    uint32_t jt = 0, uq = 0;
-    uint32_t armed = 0, armed_ph = 0;
-    for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
-      const ExtendTile tile = a.m.extend_tiles[w / a.num_kv_heads];
-      const int g = w % a.num_kv_heads;
-      const int nkv = tile.kv_tiles;
-      if (nkv == 0) continue;
-      const int b = tile.b;
-      const int q0 = a.m.qo_indptr[b];
-      const int rows_valid = (a.m.qo_indptr[b + 1] - q0) * G;
-      const int np = a.m.kv_indptr[b + 1] - a.m.kv_indptr[b];
-      const int page_base = a.m.kv_indptr[b];
-      if (!mbar_wait(q_empty, (uq & 1) ^ 1, plan)) {
-        *s_abort = 1;
-        break;
-      }
-      // Q rows -> shared memory (swizzled K-major), 16-byte chunks, two rows per warp pass
-      constexpr int kChunksPerRow = D / 8;
-      for (int it = 0; it < kExtendRows * kChunksPerRow / 32; it += 4) {
-        uint4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int ci = (it + u) * 32 + lane;
-          const int row = ci / kChunksPerRow, c = ci % kChunksPerRow;
-          const int R = tile.row0 + row;
-          v[u] = make_uint4(0, 0, 0, 0);
-          if (R < rows_valid) {
-            const long long src = ((long long)(q0 + R / G) * a.num_q_heads + g * G + R % G) * D + c * 8;
-            v[u] = __ldg(reinterpret_cast<const uint4*>(a.q + src));
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int ci = (it + u) * 32 + lane;
-          const int row = ci / kChunksPerRow, c = ci % kChunksPerRow;
-          *reinterpret_cast<uint4*>(smem + C::kQOff + (c >> 3) * (kExtendRows * 128) + row * 128 +
-                                    (((c & 7) ^ (row & 7)) << 4)) = v[u];
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(q_full);
-        for (int j = 0; j < nkv; ++j, ++jt) {
-          const int slot = jt & 1;
-          if (!mbar_wait(&kv_empty[slot], ((jt >> 1) & 1) ^ 1, plan)) {
-            *s_abort = 1;
+      const uint64_t pol = policy_evict_first();
+      uint32_t jt = 0;
+      uint32_t k_armed = 0, k_ph = 0, v_armed = 0, v_ph = 0;
+      bool stop = false;
+      for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
+        const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
+        const int g = w % a.num_kv_heads;
+        const int nT = max(u.kv_a, u.kv_b);
+        const int np = a.m.kv_indptr[u.b + 1] - a.m.kv_indptr[u.b];
+        const int page_base = a.m.kv_indptr[u.b];
+        for (int j = 0; j < nT; ++j, ++jt) {
+          const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
+          const uint32_t bytes = (uint32_t)(npg * kPageSize * D * 2);
+          // K tile j
+          const int ks = jt % NK;
+          if (!mbar_wait_ab(&k_empty[ks], ((jt / NK) & 1) ^ 1, plan, s_abort)) {
+            stop = true;
             break;
           }
-          const int npg = min(kExtendKeys / kPageSize, np - j * (kExtendKeys / kPageSize));
-          mbar_arrive_expect_tx(&kv_full[slot], (uint32_t)(npg * kPageSize * D * 2 * 2));
-          uint8_t* kd = smem + C::kKVOff + slot * C::kStageBytes;
-          uint8_t* vd = kd + C::kTileBytes;
+          mbar_arrive_expect_tx(&k_full[ks], bytes);
+          uint8_t* kd = smem + C::kKOff + ks * C::kTileBytes;
           for (int p = 0; p < npg; ++p) {
-            const int page = a.m.kv_indices[page_base + j * (kExtendKeys / kPageSize) + p];
+            const int page = a.m.kv_indices[page_base + j * kPagesPerTile + p];
 #pragma unroll
-            for (int cb = 0; cb < C::kColBlocks; ++cb) {
-              const int off = cb * (kExtendKeys * 128) + p * (kPageSize * 128);
-              tma_load_2d_hint(kd + off, &tmap_k, g * D + cb * 64, page * kPageSize, &kv_full[slot], pol);
-              tma_load_2d_hint(vd + off, &tmap_v, g * D + cb * 64, page * kPageSize, &kv_full[slot], pol);
-            }
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_2d_hint(kd + cb * (kExtendKeys * 128) + p * (kPageSize * 128), &tmap_k, g * D + cb * 64,
+                               page * kPageSize, &k_full[ks], pol);
           }
-          armed |= 1u << slot;
-          armed_ph = (armed_ph & ~(1u << slot)) | (((jt >> 1) & 1) << slot);
+          k_armed |= 1u << ks;
+          k_ph = (k_ph & ~(1u << ks)) | (((jt / NK) & 1) << ks);
+          // V tile j
+          const int vs = jt % NV;
+          if (!mbar_wait_ab(&v_empty[vs], ((jt / NV) & 1) ^ 1, plan, s_abort)) {
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[vs], bytes);
+          uint8_t* vd = smem + C::kVOff + vs * C::kTileBytes;
+          for (int p = 0; p < npg; ++p) {
+            const int page = a.m.kv_indices[page_base + j * kPagesPerTile + p];
+#pragma unroll
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_2d_hint(vd + cb * (kExtendKeys * 128) + p * (kPageSize * 128), &tmap_v, g * D + cb * 64,
+                               page * kPageSize, &v_full[vs], pol);
+          }
+          v_armed |= 1u << vs;
+          v_ph = (v_ph & ~(1u << vs)) | (((jt / NV) & 1) << vs);
         }
-      } else {
-        jt += nkv;
       }
-      jt = __shfl_sync(0xffffffffu, jt, 0);
-      ++uq;
+      if (stop) *s_abort = 1;
+      // never leave the CTA with a TMA still writing into shared memory
+      for (int s = 0; s < NK; ++s)
+        if (k_armed & (1u << s)) mbar_wait(&k_full[s], (k_ph >> s) & 1, plan);
+      for (int s = 0; s < NV; ++s)
+        if (v_armed & (1u << s)) mbar_wait(&v_full[s], (v_ph >> s) & 1, plan);
     }
-    if (lane == 0)
-      for (int s = 0; s < 2; ++s)
-        if (armed & (1u << s)) mbar_wait(&kv_full[s], (armed_ph >> s) & 1, plan);
-  } else if (warp == 5) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(kExtendRows, kExtendKeys, false, false);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(kExtendRows, D, false, true);
-      const uint32_t q_addr = smem_base + C::kQOff;
-      uint32_t jt = 0, uq = 0;
+      uint32_t jt = 0;
+      uint32_t tcount[2] = {0, 0};  // tiles processed per X (phase of s_full / p_full / pv_done)
+      uint32_t ucount[2] = {0, 0};  // units processed per X (phase of q_full)
       bool ok = true;
-      auto issue_pv = [&](uint32_t jtp, bool first) -> bool {
-        const int slot = jtp & 1;
-        if (!mbar_wait(&p_full[slot], (jtp >> 1) & 1, plan)) return false;
-        if (first && !mbar_wait(o_free, (uq & 1) ^ 1, plan)) return false;
-        tc_fence_after();
-        const uint32_t p_addr = smem_base + C::kPOff + slot * C::kPBytes;
-        const uint32_t v_addr = smem_base + C::kKVOff + slot * C::kStageBytes + C::kTileBytes;
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (ok && !mbar_wait_ab(bar, parity, plan, s_abort)) ok = false;
+        return ok;
+      };
+      auto issue_qk = [&](int x, int ks) {
+        const uint32_t q_addr = smem_base + C::kQOff + x * C::kQBytes;
+        const uint32_t k_addr = smem_base + C::kKOff + ks * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kExtendRows * 128) + (kk & 3) * 32;
+          const uint64_t qd = umma_desc_sw128(q_addr + off, 16, 1024);
+          const uint64_t kd = umma_desc_sw128(k_addr + (kk >> 2) * (kExtendKeys * 128) + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tmem + x * 128, qd, kd, idesc_qk, kk > 0);
+        }
+        umma_commit(&s_full[x]);
+      };
+      auto issue_pv = [&](int x, int vs, bool first) {
+        const uint32_t v_addr = smem_base + C::kVOff + vs * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kExtendKeys / 16; ++kk) {
-          const uint64_t pd = umma_desc_sw128(p_addr + (kk >> 2) * (kExtendRows * 128) + (kk & 3) * 32, 16, 1024);
           const uint64_t vd = umma_desc_sw128(v_addr + kk * 16 * 128, kExtendKeys * 128, 1024);
-          umma_bf16(tmem + C::kOCol, pd, vd, idesc_pv, !(first && kk == 0));
+          umma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, vd, idesc_pv, !(first && kk == 0));
         }
-        umma_commit(&p_free[slot]);
-        umma_commit(&kv_empty[slot]);
-        return true;
+        umma_commit(&pv_done[x]);
       };
-      for (int w = blockIdx.x; w < n_units && ok && !*s_abort; w += gridDim.x) {
-        const ExtendTile tile = a.m.extend_tiles[w / a.num_kv_heads];
-        const int nkv = tile.kv_tiles;
-        if (nkv == 0) continue;
-        if (!mbar_wait(q_full, uq & 1, plan)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int j = 0; j < nkv; ++j, ++jt) {
-          const int slot = jt & 1;
-          const uint32_t ph = (jt >> 1) & 1;
-          if (!mbar_wait(&kv_full[slot], ph, plan) || !mbar_wait(&s_free[slot], ph ^ 1, plan)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t k_addr = smem_base + C::kKVOff + slot * C::kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (kExtendRows * 128) + (kk & 3) * 32;
-            const uint64_t qd = umma_desc_sw128(q_addr + off, 16, 1024);
-            const uint64_t kd = umma_desc_sw128(k_addr + (kk >> 2) * (kExtendKeys * 128) + (kk & 3) * 32, 16, 1024);
-            umma_bf16(tmem + slot * kExtendKeys, qd, kd, idesc_qk, kk > 0);
-          }
-          umma_commit(&s_full[slot]);
-          if (j == nkv - 1) umma_commit(q_empty);
-          if (j >= 1 && !issue_pv(jt - 1, j - 1 == 0)) {
-            ok = false;
-            break;
-          }
-        }
+      for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+        const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
+        const int n[2] = {u.kv_a, u.kv_b};
+        const int nT = max(n[0], n[1]);
+        if (nT == 0) continue;
+        for (int x = 0; x < 2; ++x)
+          if (n[x] > 0 && !wait(&q_full[x], ucount[x] & 1)) break;
         if (!ok) break;
-        if (!issue_pv(jt - 1, nkv == 1)) {
-          ok = false;
-          break;
+        tc_fence_after();
+        // prologue: S_X(0) for both tiles
+        if (!wait(&k_full[jt % NK], (jt / NK) & 1)) break;
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x)
+          if (n[x] > 0) issue_qk(x, jt % NK);
+        umma_commit(&k_empty[jt % NK]);
+        for (int j = 0; j < nT && ok; ++j) {
+          const uint32_t jj = jt + j;
+          const int vs = jj % NV;
+          bool v_ready = false, k_ready = false;
+          for (int x = 0; x < 2; ++x) {
+            if (j >= n[x]) continue;
+            if (!wait(&p_full[x], tcount[x] & 1)) break;
+            if (!v_ready) {
+              if (!wait(&v_full[vs], (jj / NV) & 1)) break;
+              v_ready = true;
+            }
+            tc_fence_after();
+            issue_pv(x, vs, j == 0);
+            ++tcount[x];
+            if (j + 1 < n[x]) {
+              if (!k_ready) {
+                if (!wait(&k_full[(jj + 1) % NK], ((jj + 1) / NK) & 1)) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_qk(x, (jj + 1) % NK);
+            }
+          }
+          if (!ok) break;
+          umma_commit(&v_empty[vs]);
+          if (k_ready) umma_commit(&k_empty[(jj + 1) % NK]);
         }
-        ++uq;
+        jt += nT;
+        for (int x = 0; x < 2; ++x)
+          if (n[x] > 0) ++ucount[x];
       }
       if (!ok) *s_abort = 1;
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int r = tid;  // row of the tile == TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    uint32_t jt = 0, uq = 0;
+    const int x = warp >> 2;          // tile of this warpgroup
+    const int r = tid & 127;          // row within the tile == TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = x * 128, o_col = 256 + x * 128;
+    uint8_t* qtile = smem + C::kQOff + x * C::kQBytes;
+    uint32_t jt = 0, tcount = 0;
     for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
-      const ExtendTile tile = a.m.extend_tiles[w / a.num_kv_heads];
+      const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
       const int g = w % a.num_kv_heads;
-      const int nkv = tile.kv_tiles;
-      const int b = tile.b;
+      const int nA = u.kv_a;
+      const int nX = x == 0 ? u.kv_a : u.kv_b;
+      const int nT = max(u.kv_a, u.kv_b);
+      const int b = u.b;
       const int q0 = a.m.qo_indptr[b];
       const int qo = a.m.qo_indptr[b + 1] - q0;
       const int L = a.m.kv_len[b];
       const int np = a.m.kv_indptr[b + 1] - a.m.kv_indptr[b];
-      const int R = tile.row0 + r;
+      const int R = u.row0 + x * kExtendRows + r;
       const bool valid = R < qo * G;
       const int tok = min(R / G, qo - 1);
       const int limit = L - qo + tok;
-      const long long orow = ((long long)(q0 + R / G) * a.num_q_heads + g * G + R % G);
-      if (nkv == 0) {
+      const long long orow = (long long)(q0 + R / G) * a.num_q_heads + g * G + R % G;
+      if (nX == 0) {
         if (valid) {
           for (int c = 0; c < D; c += 8)
             *reinterpret_cast<uint4*>(a.out + orow * D + c) = make_uint4(0, 0, 0, 0);
           if (a.lse) a.lse[orow] = -INFINITY;
         }
+        jt += nT;
         continue;
+      }
+      // this row of Q -> shared memory (swizzled, K-major); the tile's previous
+      // QKs finished before the previous epilogue saw its last PV complete
+      {
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {  // 128 bytes of the row at a time
+          uint4 v[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            v[c] = valid ? __ldg(reinterpret_cast<const uint4*>(a.q + orow * D) + h * 8 + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(qtile + h * (kExtendRows * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v[c];
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&q_full[x]);
       }
       float m_ref = -INFINITY, l = 0.f;
       bool aborted = false;
-      for (int j = 0; j < nkv; ++j, ++jt) {
-        const int slot = jt & 1;
-        const uint32_t ph = (jt >> 1) & 1;
-        if (!mbar_wait(&s_full[slot], ph, plan)) {
+      for (int j = 0; j < nX; ++j) {
+        const uint32_t jj = jt + j;
+        if (!mbar_wait_ab(&s_full[x], tcount & 1, plan, s_abort)) {
           aborted = true;
           break;
         }
         tc_fence_after();
-        float s[kExtendKeys];
-        {
-          uint32_t sr[kExtendKeys];
+        const int key0 = j * kExtendKeys;
+        const bool diag = key0 + kExtendKeys - 1 > limit;  // some keys of this tile are masked for this row
+        // pass 1: row max of the visible raw scores, 32 columns at a time
+        float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < kExtendKeys / 32; ++c) tmem_ld32(lane_base + slot * kExtendKeys + c * 32, sr + c * 32);
+        for (int cc = 0; cc < kExtendKeys / 32; ++cc) {
+          uint32_t sr[32];
+          tmem_ld32(lane_base + s_col + cc * 32, sr);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < kExtendKeys; ++c) s[c] = __uint_as_float(sr[c]);
+          for (int c = 0; c < 32; ++c) {
+            const float v = __uint_as_float(sr[c]);
+            mx = (diag && key0 + cc * 32 + c > limit) ? mx : fmaxf(mx, v);
+          }
         }
-        tc_fence_before();
-        mbar_arrive(&s_free[slot]);
-
-        // the request's last page inside this tile: zero the V rows past L
-        if (j == nkv - 1 && np <= (j + 1) * (kExtendKeys / kPageSize) && (L % kPageSize) != 0) {
+        // the request's last page inside this KV tile: zero the V rows past L
+        // (done by the first tile that reads this V tile, before its PV)
+        if ((x == 0 || j >= nA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
+          const int vs = jj % NV;
+          if (!mbar_wait_ab(&v_full[vs], (jj / NV) & 1, plan, s_abort)) {
+            aborted = true;
+            break;
+          }
           const int r0 = L - j * kExtendKeys;
-          const int r1 = (np - j * (kExtendKeys / kPageSize)) * kPageSize;
-          uint8_t* vt = smem + C::kKVOff + slot * C::kStageBytes + C::kTileBytes;
+          const int r1 = (np - j * kPagesPerTile) * kPageSize;
+          uint8_t* vt = smem + C::kVOff + vs * C::kTileBytes;
           const int n16 = (r1 - r0) * C::kColBlocks * 8;
           for (int i = r; i < n16; i += 128) {
             const int row = r0 + i / (C::kColBlocks * 8);
@@ -331,29 +364,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             *reinterpret_cast<uint4*>(vt + (rest >> 3) * (kExtendKeys * 128) + row * 128 + (rest & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
         }
-
-        const int key0 = j * kExtendKeys;
-        float mt = -INFINITY;
-        if (key0 + kExtendKeys - 1 <= limit) {
-#pragma unroll
-          for (int c = 0; c < kExtendKeys; ++c) {
-            s[c] *= a.scale_log2;
-            mt = fmaxf(mt, s[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kExtendKeys; ++c) {
-            s[c] = (key0 + c <= limit) ? s[c] * a.scale_log2 : -INFINITY;
-            mt = fmaxf(mt, s[c]);
-          }
-        }
+        const float mt = mx * a.scale_log2;
         if (j == 0) {
           m_ref = mt;
         } else if (mt > m_ref + kRescaleThreshold) {
-          // O must hold every earlier PV before it is rescaled
-          const uint32_t jp = jt - 1;
-          if (!mbar_wait(&p_free[jp & 1], (jp >> 1) & 1, plan)) {
+          // O_X must hold every earlier PV before it is rescaled
+          if (!mbar_wait_ab(&pv_done[x], (tcount - 1) & 1, plan, s_abort)) {
             aborted = true;
             break;
           }
@@ -362,50 +380,53 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            tmem_ld32(lane_base + C::kOCol + c * 32, o);
+            tmem_ld32(lane_base + o_col + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(lane_base + C::kOCol + c * 32, o);
+            tmem_st32(lane_base + o_col + c * 32, o);
           }
           tmem_wait_st();
           l *= alpha;
           m_ref = mt;
         }
         const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+        // pass 2: P = exp2(s * scale - m), bf16 pairs written over the first
+        // half of this tile's S columns; chunk cc writes columns 16cc..16cc+15,
+        // which pass 2 has already read
         float rs = 0.f;
 #pragma unroll
-        for (int c = 0; c < kExtendKeys; ++c) {
-          s[c] = fast_exp2(s[c] - ref);
-          rs += s[c];
+        for (int cc = 0; cc < kExtendKeys / 32; ++cc) {
+          uint32_t sr[32];
+          tmem_ld32(lane_base + s_col + cc * 32, sr);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int k0 = key0 + cc * 32 + c;
+            float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), a.scale_log2, -ref));
+            float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), a.scale_log2, -ref));
+            if (diag) {
+              p0 = k0 > limit ? 0.f : p0;
+              p1 = k0 + 1 > limit ? 0.f : p1;
+            }
+            rs += p0 + p1;
+            pk[c >> 1] = pack_bf16(p0, p1);
+          }
+          tmem_st16(lane_base + s_col + cc * 16, pk);
         }
         l += rs;
-        // P slot is free once the PV of two tiles ago has completed
-        if (!mbar_wait(&p_free[slot], ph ^ 1, plan)) {
-          aborted = true;
-          break;
-        }
-        uint8_t* pt = smem + C::kPOff + slot * C::kPBytes;
-#pragma unroll
-        for (int c = 0; c < kExtendKeys / 8; ++c) {
-          uint4 v;
-          v.x = pack_bf16(s[8 * c + 0], s[8 * c + 1]);
-          v.y = pack_bf16(s[8 * c + 2], s[8 * c + 3]);
-          v.z = pack_bf16(s[8 * c + 4], s[8 * c + 5]);
-          v.w = pack_bf16(s[8 * c + 6], s[8 * c + 7]);
-          *reinterpret_cast<uint4*>(pt + (c >> 3) * (kExtendRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[slot]);
+        mbar_arrive(&p_full[x]);
+        ++tcount;
       }
       if (aborted) {
         *s_abort = 1;
         break;
       }
-      // epilogue: O / l
-      const uint32_t jl = jt - 1;
-      if (!mbar_wait(&p_free[jl & 1], (jl >> 1) & 1, plan)) {
+      // epilogue: O / l once the last PV of this tile has finished
+      if (!mbar_wait_ab(&pv_done[x], (tcount - 1) & 1, plan, s_abort)) {
         *s_abort = 1;
         break;
       }
@@ -414,7 +435,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(lane_base + C::kOCol + c * 32, o);
+        tmem_ld32(lane_base + o_col + c * 32, o);
         tmem_wait_ld();
         if (valid) {
 #pragma unroll
@@ -429,15 +450,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         }
       }
       tc_fence_before();
-      mbar_arrive(o_free);
       if (valid && a.lse) a.lse[orow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-      ++uq;
+      jt += nT;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -475,8 +495,8 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
 
 int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, void* out,
                   float* lse, cudaStream_t st) {
-  if (c.cfg.head_dim == 128) return run_extend<ExtCfg<128>>(c, q, k_pool, v_pool, sm_scale, out, lse, st);
-  if (c.cfg.head_dim == 64) return run_extend<ExtCfg<64>>(c, q, k_pool, v_pool, sm_scale, out, lse, st);
+  if (c.cfg.head_dim == 128) return run_extend<ExtCfg<128, 3, 2>>(c, q, k_pool, v_pool, sm_scale, out, lse, st);
+  if (c.cfg.head_dim == 64) return run_extend<ExtCfg<64, 4, 4>>(c, q, k_pool, v_pool, sm_scale, out, lse, st);
   return PKV_ERR_UNSUPPORTED;
 }
 

@@ -13,8 +13,9 @@
 //     cut into chunks of chunk_pages, with chunk_pages chosen so the number of
 //     (item, KV head) units fills the persistent grid a few times over and the
 //     partial-output buffer cannot overflow;
-//   extend path: (request, first query row) tiles of 128 rows, where a row is
-//     (token, head-in-group), with the number of 128-key KV tiles it reaches.
+//   extend path: (request, first query row) units of 256 rows (two 128-row
+//     tiles), where a row is (token, head-in-group), with the number of
+//     128-key KV tiles each tile reaches.
 //
 // Work split: CTA j owns a contiguous range of requests. Every CTA first
 // reduces the batch totals (they fix chunk_pages and the capacity checks) and
@@ -87,7 +88,7 @@ __device__ __forceinline__ ReqInfo req_info(const MetaArgs& a, int b, int chunk)
   r.np = (r.L + kPageSize - 1) / kPageSize;
   r.nsplit = r.np > 0 ? (r.np + chunk - 1) / chunk : 1;
   r.prow = r.nsplit > 1 ? r.nsplit * r.qo : 0;
-  r.qtiles = (r.qo * a.group + kExtendRows - 1) / kExtendRows;
+  r.qtiles = (r.qo * a.group + kExtendUnitRows - 1) / kExtendUnitRows;
   return r;
 }
 
@@ -304,14 +305,18 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
         }
       }
       const int rows = qo * a.group;
+      auto kv_tiles_to = [&](int row_end) {  // KV tiles reached by rows [.., row_end)
+        const int last_tok = (row_end - 1) / a.group;
+        return L > 0 ? (L - qo + last_tok + 1 + kExtendKeys - 1) / kExtendKeys : 0;
+      };
       for (int t = threadIdx.x; t < qt; t += kThreads) {
         if (tbase + t < a.max_tiles) {
-          const int last_tok = (min((t + 1) * kExtendRows, rows) - 1) / a.group;
+          const int row0 = t * kExtendUnitRows;
           ExtendTile et;
           et.b = bb;
-          et.row0 = t * kExtendRows;
-          et.kv_tiles = L > 0 ? (L - qo + last_tok + 1 + kExtendKeys - 1) / kExtendKeys : 0;
-          et.pad = 0;
+          et.row0 = row0;
+          et.kv_a = kv_tiles_to(min(row0 + kExtendRows, rows));
+          et.kv_b = row0 + kExtendRows < rows ? kv_tiles_to(min(row0 + kExtendUnitRows, rows)) : 0;
           a.tiles[tbase + t] = et;
         }
       }

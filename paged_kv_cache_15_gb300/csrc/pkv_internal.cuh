@@ -18,6 +18,7 @@ constexpr int kPageSize = 16;           // the only page size this build accepts
 constexpr int kDecodeTargetWaves = 4;   // split-KV aims at this many work units per CTA slot
 constexpr int kDecodeMinChunkPages = 8; // never cut a (request, head) range finer than 128 keys
 constexpr int kExtendRows = 128;        // query rows (token x head-in-group) per extend tile
+constexpr int kExtendUnitRows = 256;    // an extend work unit holds two tiles (A, B) sharing K/V
 constexpr int kExtendKeys = 128;        // keys per extend KV tile
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s bound on any mbarrier wait
 
@@ -45,9 +46,11 @@ enum PlanWord : int {
 struct DecodeItem {
   int b, split, p0, p1;
 };
-// Work item of the extend path: request, first query row (token * group + head-in-group).
+// Work item of the extend path: request, first query row (token * group +
+// head-in-group) of a 256-row unit, and the number of 128-key KV tiles its
+// first and second 128-row tile reach (0 when the tile has no rows).
 struct ExtendTile {
-  int b, row0, kv_tiles, pad;
+  int b, row0, kv_a, kv_b;
 };
 
 // Byte offsets of every buffer inside the caller's workspace.
@@ -352,6 +355,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A (M rows x 16 K) sits in TMEM, row m in
+// lane m, two bf16 per 32-bit column, lower K index in the low half.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 operation issued so far by
 // this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -379,6 +393,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
       "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
       "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
