@@ -38,6 +38,62 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+constexpr uint32_t kNegInfBits = 0xff800000u;
+
+// Masks raw scores of keys past the row's limit (sets them to -inf).
+__device__ __forceinline__ void mask32(uint32_t* sr, int key_base, int limit) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) sr[c] = key_base + c > limit ? kNegInfBits : sr[c];
+}
+
+// Max of 32 raw scores with four independent 3-input chains.
+__device__ __forceinline__ float max32(const uint32_t* sr, float m) {
+  float a0 = m, a1 = m, a2 = m, a3 = m;
+#pragma unroll
+  for (int c = 0; c < 32; c += 8) {
+    a0 = max3f(a0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+    a1 = max3f(a1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+    a2 = max3f(a2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+    a3 = max3f(a3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+  }
+  return max3f(fmaxf(a0, a1), a2, a3);
+}
+
+// p = exp2(s * scale - ref) for 32 raw scores: packed bf16 pairs into pk,
+// running sums in four packed accumulators.
+__device__ __forceinline__ void exp32(const uint32_t* sr, uint64_t sc2, uint64_t nref2, uint32_t* pk, uint64_t* acc) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nref2);
+    const float p0 = fast_exp2(f2_lo(x)), p1 = fast_exp2(f2_hi(x));
+    acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+    pk[c >> 1] = pack_bf16(p0, p1);
+  }
+}
+
 template <int D_, int NK_, int NV_>
 struct ExtCfg {
   static constexpr int D = D_;
@@ -333,18 +389,19 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         tc_fence_after();
         const int key0 = j * kExtendKeys;
         const bool diag = key0 + kExtendKeys - 1 > limit;  // some keys of this tile are masked for this row
-        // pass 1: row max of the visible raw scores, 32 columns at a time
+        // pass 1: row max of the visible raw scores, two 32-column loads per wait
         float mx = -INFINITY;
 #pragma unroll
-        for (int cc = 0; cc < kExtendKeys / 32; ++cc) {
-          uint32_t sr[32];
+        for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
+          uint32_t sr[64];
           tmem_ld32(lane_base + s_col + cc * 32, sr);
+          tmem_ld32(lane_base + s_col + cc * 32 + 32, sr + 32);
           tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float v = __uint_as_float(sr[c]);
-            mx = (diag && key0 + cc * 32 + c > limit) ? mx : fmaxf(mx, v);
+          if (diag) {
+            mask32(sr, key0 + cc * 32, limit);
+            mask32(sr + 32, key0 + cc * 32 + 32, limit);
           }
+          mx = max32(sr + 32, max32(sr, mx));
         }
         // the request's last page inside this KV tile: zero the V rows past L
         // (done by the first tile that reads this V tile, before its PV)
@@ -392,29 +449,28 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         }
         const float ref = m_ref == -INFINITY ? 0.f : m_ref;
         // pass 2: P = exp2(s * scale - m), bf16 pairs written over the first
-        // half of this tile's S columns; chunk cc writes columns 16cc..16cc+15,
-        // which pass 2 has already read
-        float rs = 0.f;
+        // half of this tile's S columns; the chunk pair (cc, cc+1) writes
+        // columns 16cc..16cc+31, which this pass has already read
+        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nref2 = f2_pack(-ref, -ref);
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int cc = 0; cc < kExtendKeys / 32; ++cc) {
-          uint32_t sr[32];
+        for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
+          uint32_t sr[64];
           tmem_ld32(lane_base + s_col + cc * 32, sr);
+          tmem_ld32(lane_base + s_col + cc * 32 + 32, sr + 32);
           tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const int k0 = key0 + cc * 32 + c;
-            float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), a.scale_log2, -ref));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), a.scale_log2, -ref));
-            if (diag) {
-              p0 = k0 > limit ? 0.f : p0;
-              p1 = k0 + 1 > limit ? 0.f : p1;
-            }
-            rs += p0 + p1;
-            pk[c >> 1] = pack_bf16(p0, p1);
+          if (diag) {
+            mask32(sr, key0 + cc * 32, limit);
+            mask32(sr + 32, key0 + cc * 32 + 32, limit);
           }
-          tmem_st16(lane_base + s_col + cc * 16, pk);
+          uint32_t pk[32];
+          exp32(sr, sc2, nref2, pk, acc);
+          exp32(sr + 32, sc2, nref2, pk + 16, acc);
+          tmem_st32(lane_base + s_col + cc * 16, pk);
         }
+        const uint64_t acc01 = f2_add(acc[0], acc[1]), acc23 = f2_add(acc[2], acc[3]);
+        const uint64_t accs = f2_add(acc01, acc23);
+        const float rs = f2_lo(accs) + f2_hi(accs);
         l += rs;
         tmem_wait_st();
         tc_fence_before();
