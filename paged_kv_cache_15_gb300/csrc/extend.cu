@@ -9,7 +9,7 @@
 // so the GQA group shares K/V as well. Row of token i sees keys 0 .. P + i
 // (P = cached prefix of the request).
 //
-// Warp roles (320 threads, one CTA per SM, persistent over units):
+// Warp roles (352 threads, one CTA per SM, persistent over units):
 //   warps 0-3  softmax A, warps 4-7 softmax B: thread r of a warpgroup owns
 //              row r of its tile (TMEM lane r). It copies its Q row into shared
 //              memory at the start of a unit, reads S from TMEM, masks, keeps
@@ -17,9 +17,9 @@
 //              into the first half of its S columns, rescales O in TMEM only
 //              when the max grows by more than 2^8 (the factor cancels in
 //              O / l), and writes the output rows.
-//   warp 8     producer: gathers K and V pages with TMA (one 16-token box per
-//              page and 128-byte column block, 128-byte swizzle) into a 3-deep
-//              K ring and a 2-deep V ring.
+//   warps 8, 10 producers: gather K (warp 8) and V (warp 10) pages with TMA
+//              (one 16-token box per page and 128-byte column block, 128-byte
+//              swizzle) into separate K and V rings.
 //   warp 9     MMA: owns 512 TMEM columns and issues tcgen05.mma
 //              (kind::f16, bf16 in, fp32 accumulate):
 //                S_X = Q_X K^T      (M=128, N=128 keys, K=head_dim; A, B from smem)
@@ -99,9 +99,10 @@ struct ExtCfg {
   static constexpr int D = D_;
   static constexpr int NK = NK_;  // K ring depth
   static constexpr int NV = NV_;  // V ring depth
-  static constexpr int kThreads = 320;
-  static constexpr int kProducerWarp = 8;
+  static constexpr int kThreads = 352;
+  static constexpr int kProducerWarp = 8;   // K tiles
   static constexpr int kMmaWarp = 9;
+  static constexpr int kVProducerWarp = 10;  // V tiles
   static constexpr int kColBlocks = D / 64;               // 128-byte swizzle spans per row
   static constexpr int kQBytes = kExtendRows * D * 2;     // one Q tile: [cb][128 rows][128 B]
   static constexpr int kTileBytes = kExtendKeys * D * 2;  // one K or V tile
@@ -186,14 +187,21 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   const int G = a.group;
   const uint32_t smem_base = smem_u32(smem);
 
-  if (warp == C::kProducerWarp) {
-    // ------------------------------------------------------------ producer
+  if (warp == C::kProducerWarp || warp == C::kVProducerWarp) {
+    // ------------------------------------------------------------ producers
+    // one warp streams K tiles, the other V tiles, each through its own ring,
+    // so a full V ring never holds back the next K tile
+    const bool is_v = warp == C::kVProducerWarp;
+    const int depth = is_v ? NV : NK;
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* empty = is_v ? v_empty : k_empty;
+    const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
+    const int ring_off = is_v ? C::kVOff : C::kKOff;
     if (lane == 0) {
-      prefetch_tmap(&tmap_k);
-      prefetch_tmap(&tmap_v);
+      prefetch_tmap(tmap);
       const uint64_t pol = policy_evict_first();
       uint32_t jt = 0;
-      uint32_t k_armed = 0, k_ph = 0, v_armed = 0, v_ph = 0;
+      uint32_t armed = 0, armed_ph = 0;
       bool stop = false;
       for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
         const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
@@ -203,49 +211,36 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         const int page_base = a.m.kv_indptr[u.b];
         for (int j = 0; j < nT; ++j, ++jt) {
           const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
-          const uint32_t bytes = (uint32_t)(npg * kPageSize * D * 2);
-          // K tile j
-          const int ks = jt % NK;
-          if (!mbar_wait_ab(&k_empty[ks], ((jt / NK) & 1) ^ 1, plan, s_abort)) {
+          // the tile's page indices: independent loads issued before the ring wait
+          int pg[kPagesPerTile];
+#pragma unroll
+          for (int p = 0; p < kPagesPerTile; ++p)
+            pg[p] = p < npg ? __ldg(a.m.kv_indices + page_base + j * kPagesPerTile + p) : 0;
+          const int st = jt % depth;
+          const uint32_t ph = (jt / depth) & 1;
+          if (!mbar_wait_ab(&empty[st], ph ^ 1, plan, s_abort)) {
             stop = true;
             break;
           }
-          mbar_arrive_expect_tx(&k_full[ks], bytes);
-          uint8_t* kd = smem + C::kKOff + ks * C::kTileBytes;
-          for (int p = 0; p < npg; ++p) {
-            const int page = a.m.kv_indices[page_base + j * kPagesPerTile + p];
+          mbar_arrive_expect_tx(&full[st], (uint32_t)(npg * kPageSize * D * 2));
+          uint8_t* dst = smem + ring_off + st * C::kTileBytes;
 #pragma unroll
-            for (int cb = 0; cb < C::kColBlocks; ++cb)
-              tma_load_2d_hint(kd + cb * (kExtendKeys * 128) + p * (kPageSize * 128), &tmap_k, g * D + cb * 64,
-                               page * kPageSize, &k_full[ks], pol);
-          }
-          k_armed |= 1u << ks;
-          k_ph = (k_ph & ~(1u << ks)) | (((jt / NK) & 1) << ks);
-          // V tile j
-          const int vs = jt % NV;
-          if (!mbar_wait_ab(&v_empty[vs], ((jt / NV) & 1) ^ 1, plan, s_abort)) {
-            stop = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&v_full[vs], bytes);
-          uint8_t* vd = smem + C::kVOff + vs * C::kTileBytes;
-          for (int p = 0; p < npg; ++p) {
-            const int page = a.m.kv_indices[page_base + j * kPagesPerTile + p];
+          for (int p = 0; p < kPagesPerTile; ++p) {
+            if (p < npg) {
 #pragma unroll
-            for (int cb = 0; cb < C::kColBlocks; ++cb)
-              tma_load_2d_hint(vd + cb * (kExtendKeys * 128) + p * (kPageSize * 128), &tmap_v, g * D + cb * 64,
-                               page * kPageSize, &v_full[vs], pol);
+              for (int cb = 0; cb < C::kColBlocks; ++cb)
+                tma_load_2d_hint(dst + cb * (kExtendKeys * 128) + p * (kPageSize * 128), tmap, g * D + cb * 64,
+                                 pg[p] * kPageSize, &full[st], pol);
+            }
           }
-          v_armed |= 1u << vs;
-          v_ph = (v_ph & ~(1u << vs)) | (((jt / NV) & 1) << vs);
+          armed |= 1u << st;
+          armed_ph = (armed_ph & ~(1u << st)) | (ph << st);
         }
       }
       if (stop) *s_abort = 1;
       // never leave the CTA with a TMA still writing into shared memory
-      for (int s = 0; s < NK; ++s)
-        if (k_armed & (1u << s)) mbar_wait(&k_full[s], (k_ph >> s) & 1, plan);
-      for (int s = 0; s < NV; ++s)
-        if (v_armed & (1u << s)) mbar_wait(&v_full[s], (v_ph >> s) & 1, plan);
+      for (int s2 = 0; s2 < depth; ++s2)
+        if (armed & (1u << s2)) mbar_wait(&full[s2], (armed_ph >> s2) & 1, plan);
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -389,20 +384,6 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         tc_fence_after();
         const int key0 = j * kExtendKeys;
         const bool diag = key0 + kExtendKeys - 1 > limit;  // some keys of this tile are masked for this row
-        // pass 1: row max of the visible raw scores, two 32-column loads per wait
-        float mx = -INFINITY;
-#pragma unroll
-        for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
-          uint32_t sr[64];
-          tmem_ld32(lane_base + s_col + cc * 32, sr);
-          tmem_ld32(lane_base + s_col + cc * 32 + 32, sr + 32);
-          tmem_wait_ld();
-          if (diag) {
-            mask32(sr, key0 + cc * 32, limit);
-            mask32(sr + 32, key0 + cc * 32 + 32, limit);
-          }
-          mx = max32(sr + 32, max32(sr, mx));
-        }
         // the request's last page inside this KV tile: zero the V rows past L
         // (done by the first tile that reads this V tile, before its PV)
         if ((x == 0 || j >= nA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
@@ -423,39 +404,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           }
           fence_proxy_async_smem();
         }
-        const float mt = mx * a.scale_log2;
-        if (j == 0) {
-          m_ref = mt;
-        } else if (mt > m_ref + kRescaleThreshold) {
-          // O_X must hold every earlier PV before it is rescaled
-          if (!mbar_wait_ab(&pv_done[x], (tcount - 1) & 1, plan, s_abort)) {
-            aborted = true;
-            break;
-          }
-          tc_fence_after();
-          const float alpha = fast_exp2(m_ref - mt);
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + o_col + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(lane_base + o_col + c * 32, o);
-          }
-          tmem_wait_st();
-          l *= alpha;
-          m_ref = mt;
-        }
-        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-        // pass 2: P = exp2(s * scale - m), bf16 pairs written over the first
-        // half of this tile's S columns; the chunk pair (cc, cc+1) writes
-        // columns 16cc..16cc+31, which this pass has already read
-        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nref2 = f2_pack(-ref, -ref);
+        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+        uint32_t pk[kExtendKeys / 2];  // P as bf16 pairs, written to TMEM once final
         uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
-          uint32_t sr[64];
+        // S read 64 columns per TMEM wait; masked keys become -inf
+        auto load_s = [&](int cc, uint32_t* sr) {
           tmem_ld32(lane_base + s_col + cc * 32, sr);
           tmem_ld32(lane_base + s_col + cc * 32 + 32, sr + 32);
           tmem_wait_ld();
@@ -463,15 +416,75 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             mask32(sr, key0 + cc * 32, limit);
             mask32(sr + 32, key0 + cc * 32 + 32, limit);
           }
-          uint32_t pk[32];
-          exp32(sr, sc2, nref2, pk, acc);
-          exp32(sr + 32, sc2, nref2, pk + 16, acc);
-          tmem_st32(lane_base + s_col + cc * 16, pk);
+        };
+        bool rebase = j == 0;
+        float mt = -INFINITY;
+        if (j > 0) {
+          // one pass: P against the running reference, row max alongside
+          const uint64_t nref2 = f2_pack(-m_ref, -m_ref);
+          float mx = -INFINITY;
+#pragma unroll
+          for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
+            uint32_t sr[64];
+            load_s(cc, sr);
+            mx = max32(sr + 32, max32(sr, mx));
+            exp32(sr, sc2, nref2, pk + cc * 16, acc);
+            exp32(sr + 32, sc2, nref2, pk + cc * 16 + 16, acc);
+          }
+          mt = mx * a.scale_log2;
+          rebase = mt > m_ref + kRescaleThreshold;
         }
+        if (rebase) {
+          // first tile, or the row max grew past the reference by more than
+          // 2^8: move the reference, rescale O, recompute P from S (still intact)
+          if (j == 0) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
+              uint32_t sr[64];
+              load_s(cc, sr);
+              mx = max32(sr + 32, max32(sr, mx));
+            }
+            m_ref = mx * a.scale_log2;
+          } else {
+            // O_X must hold every earlier PV before it is rescaled
+            if (!mbar_wait_ab(&pv_done[x], (tcount - 1) & 1, plan, s_abort)) {
+              aborted = true;
+              break;
+            }
+            tc_fence_after();
+            const float alpha = fast_exp2(m_ref - mt);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(lane_base + o_col + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(lane_base + o_col + c * 32, o);
+            }
+            tmem_wait_st();
+            l *= alpha;
+            m_ref = mt;
+          }
+          const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+          const uint64_t nref2 = f2_pack(-ref, -ref);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = 0;
+#pragma unroll
+          for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
+            uint32_t sr[64];
+            load_s(cc, sr);
+            exp32(sr, sc2, nref2, pk + cc * 16, acc);
+            exp32(sr + 32, sc2, nref2, pk + cc * 16 + 16, acc);
+          }
+        }
+        // P overwrites the first half of this tile's S columns
+        tmem_st32(lane_base + s_col, pk);
+        tmem_st32(lane_base + s_col + 32, pk + 32);
         const uint64_t acc01 = f2_add(acc[0], acc[1]), acc23 = f2_add(acc[2], acc[3]);
         const uint64_t accs = f2_add(acc01, acc23);
-        const float rs = f2_lo(accs) + f2_hi(accs);
-        l += rs;
+        l += f2_lo(accs) + f2_hi(accs);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[x]);
