@@ -224,11 +224,113 @@ def run_reference(args, W, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def graph_step_us(d, step, steps, stream):
+    """Per-step time of the same step captured once in a CUDA graph and replayed
+    (serving replays decode graphs); None if capture is unavailable."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return g0.elapsed_time(g1) / steps * 1e3
+
+
+def roofline_of(W, work, fwd_s, spec, B):
+    hbm_peak, tf_peak, _, peak_kind = peaks()
+    on_extend = W.mode == "extend" or (W.mode == "verify" and spec == B.PKV_SPEC_PREFILL)
+    if W.mode == "extend":
+        achieved = work["flops"] / fwd_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": achieved / tf_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)"}
+    else:
+        achieved = work["bytes"] / fwd_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} HBM copy"}
+    key = "extend_tc" if on_extend else "decode_splitkv"
+    tr = NCU_TRAFFIC.get((key, W.name))
+    roof["traffic"] = None
+    if tr and tr["src_sha"] == src_sha("extend.cu" if on_extend else "decode.cu"):
+        roof["traffic"] = tr["bytes_per_launch"]
+    roof["kernel"] = key
+    roof["timed"] = ("forward call (attention kernel, plus the split merge kernel on the decode path), "
+                     "CUDA events on the launching stream")
+    return roof
+
+
+def timed_steps(d, spec, steps, world):
+    """K steps on the launching stream: whole-step time and forward-call time."""
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        d.set_kv_buffer()
+        d.build_metadata()
+        ev[i][0].record(stream)
+        d.forward(spec)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_s = max_over_ranks(start.elapsed_time(end) / steps / 1e3, world)
+    fwd_s = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3, world)
+    return step_s, fwd_s
+
+
+def secondary(name, spec_name, local, steps, world):
+    """Short measurement of another workload (no e2e / CPU baseline)."""
+    from paged_kv_cache_15_gb300 import binding as B
+    from paged_kv_cache_15_gb300.runner import DeviceBatch
+    from paged_kv_cache_15_gb300.workloads import preset
+    W = preset(name)
+    spec = B.PKV_SPEC_DECODE if spec_name == "decode" else B.PKV_SPEC_PREFILL
+    d = DeviceBatch(W, device=f"cuda:{local}")
+
+    def step():
+        d.set_kv_buffer()
+        d.build_metadata()
+        d.forward(spec)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if d.device_error():
+        raise RuntimeError(f"device error on {name}")
+    step_s, fwd_s = timed_steps(d, spec, steps, world)
+    work = work_of(W)
+    value, unit = metric_value(W, work, step_s)
+    roof = roofline_of(W, work, fwd_s, spec, B)
+    out = {"metric_value": value * world, "unit": unit, "us_per_call": fwd_s * 1e6, "step_us": step_s * 1e6,
+           "graph_step_us": graph_step_us(d, step, steps, torch.cuda.current_stream()),
+           "roofline_frac": roof["frac"], "achieved": roof["achieved"], "achieved_unit": roof["unit"],
+           "kernel": roof["kernel"], "path": "decode" if roof["kernel"] == "decode_splitkv" else "extend",
+           "steps": steps}
+    del d
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, W, rank, world, local):
     from paged_kv_cache_15_gb300 import binding as B
     from paged_kv_cache_15_gb300.runner import DeviceBatch
 
-    hbm_peak, tf_peak, tf_sust, peak_kind = peaks()
     spec = B.PKV_SPEC_DECODE if args.spec_mode == "decode" else B.PKV_SPEC_PREFILL
     d = DeviceBatch(W, device=f"cuda:{local}")
     work = work_of(W)
@@ -247,55 +349,16 @@ def run_ours(args, W, rank, world, local):
         raise RuntimeError(f"device error {err}")
 
     # --- device-resident timed region: K steps, events on the launching stream
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        d.set_kv_buffer()
-        d.build_metadata()
-        ev[i][0].record(stream)
-        d.forward(spec)
-        ev[i][1].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    step_s, fwd_s = timed_steps(d, spec, args.steps, world)
     clocks = sampler.stop() if sampler else None
-    total_ms = start.elapsed_time(end)
-    fwd_ms = [a.elapsed_time(b) for a, b in ev]
-    step_s = max_over_ranks(total_ms / args.steps / 1e3, world)
-    fwd_s = max_over_ranks(statistics.mean(fwd_ms) / 1e3, world)
-    launches = (4 if d.mode != B.PKV_MODE_EXTEND and not (d.mode == B.PKV_MODE_TARGET_VERIFY and spec == B.PKV_SPEC_PREFILL) else 3) * args.steps  # set_kv, metadata, attention (+ split merge on the decode path)
+    on_decode_path = W.mode == "decode" or (W.mode == "verify" and spec == B.PKV_SPEC_DECODE)
+    launches = (4 if on_decode_path else 3) * args.steps  # set_kv, metadata, attention (+ split merge)
 
-    # --- the same step captured once in a CUDA graph and replayed (serving runs decode this way)
-    graph_us = None
-    if not args.no_graph:
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            step()
-        stream.wait_stream(side)
-        with torch.cuda.graph(g):
-            step()
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        g0 = torch.cuda.Event(enable_timing=True)
-        g1 = torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(args.steps):
-            g.replay()
-        g1.record(stream)
-        torch.cuda.synchronize()
-        graph_us = max_over_ranks(g0.elapsed_time(g1) / args.steps * 1e3, world)
-        del g
+    graph_us = None if args.no_graph else max_over_ranks(graph_step_us(d, step, args.steps, stream), world)
 
     # --- end to end through the C ABI with host buffers (pinned), inputs copied every step
     pin = lambda t: t.pin_memory()
@@ -332,28 +395,26 @@ def run_ours(args, W, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / e2e_steps / 1e3, world)
+    describe = B.pkv_describe(d.ctx)
+    del d
+    torch.cuda.empty_cache()
+
+    # --- the other named workloads of the metric, short runs
+    others = {}
+    if not args.no_secondary:
+        for name, sp in (("tiny_decode", "prefill"), ("prefix_extend", "prefill"), ("spec_verify", "decode"),
+                         ("spec_verify", "prefill"), ("long_fp8_decode", "prefill")):
+            if name == W.name and sp == args.spec_mode:
+                continue
+            key = name if name != "spec_verify" else f"spec_verify/{sp}_path"
+            others[key] = secondary(name, sp, local, args.secondary_steps, world)
 
     if rank != 0:
         return
     value, unit = metric_value(W, work, step_s)
     value *= world  # every rank ran one replica
     e2e_value = metric_value(W, work, e2e_s)[0] * world
-    if W.mode == "extend":
-        achieved = work["flops"] / fwd_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": achieved / tf_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)",
-                "traffic": None}
-    else:
-        achieved = work["bytes"] / fwd_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} HBM copy", "traffic": None}
-    key = "extend_tc" if W.mode == "extend" or (W.mode == "verify" and spec == B.PKV_SPEC_PREFILL) else \
-        "decode_splitkv"
-    tr = NCU_TRAFFIC.get((key, W.name))
-    if tr and tr["src_sha"] == src_sha("extend.cu" if key == "extend_tc" else "decode.cu"):
-        roof["traffic"] = tr["bytes_per_launch"]
-    roof["kernel"] = key
-    roof["timed"] = "forward call (attention kernel, plus the split merge kernel on the decode path), CUDA events on the launching stream"
+    roof = roofline_of(W, work, fwd_s, spec, B)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu, _ = oracle_sample(W, budget_s=args.ref_budget)
@@ -378,7 +439,8 @@ def run_ours(args, W, rank, world, local):
                     "steps": e2e_steps, "api": "pkv_set_kv_buffer + pkv_build_metadata + pkv_forward"},
             "gpu_launches": launches,
             "clocks": clocks,
-            "describe": B.pkv_describe(d.ctx)}
+            "workloads": others,
+            "describe": describe}
     print(json.dumps(line), flush=True)
 
 
@@ -393,6 +455,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the short runs of the other workloads")
+    ap.add_argument("--secondary-steps", type=int, default=30)
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     from paged_kv_cache_15_gb300.workloads import preset

@@ -99,12 +99,12 @@ __device__ __forceinline__ int ocol(int nt, int q, int e) {
 // in batches. Partials were written by other CTAs, so they are read through
 // L2 (ld.global.cg), never from a stale L1 line.
 template <int D>
-__device__ __forceinline__ void merge_group(const DecodeArgs& a, int b, int g, int q0, int qo, int nsplit, int cw,
-                                            int lane, int ncw) {
+__device__ __forceinline__ void merge_rows(const DecodeArgs& a, int b, int g, int q0, int qo, int nsplit, int r0,
+                                           int lane, int rstep = 1 << 30) {
   const int G = a.group;
   const long long pbase = a.m.partial_indptr[b];
   constexpr int PER = D / 32;
-  for (int r = cw; r < qo * G; r += ncw) {
+  for (int r = r0; r < qo * G; r += rstep) {
     const int i = r / G, h = g * G + r % G;
     auto lse_of = [&](int sp) {
       return __ldcg(a.m.partial_lse + (pbase + (long long)sp * qo + i) * a.num_q_heads + h);
@@ -633,16 +633,21 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
 }
 
 
-// Separate merge: one CTA of 4 warps per (request, KV head) group with splits.
+// Split merge: a (request, KV head) group's rows (query tokens x heads of the
+// group) are spread over CTAs of 4 warps, one row per warp.
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a) {
-  const int grp = blockIdx.x;
+__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a, int row_blocks) {
+  const int grp = blockIdx.x / row_blocks, rb = blockIdx.x % row_blocks;
   const int b = grp / a.num_kv_heads, g = grp % a.num_kv_heads;
   if (b >= a.m.plan[kBatch]) return;
   const int nsplit = a.m.n_splits[b];
   if (nsplit <= 1) return;
   const int q0 = a.m.qo_indptr[b];
-  merge_group<D>(a, b, g, q0, a.m.qo_indptr[b + 1] - q0, nsplit, threadIdx.x >> 5, threadIdx.x & 31, 4);
+  const int qo = a.m.qo_indptr[b + 1] - q0;
+  const int rows = qo * a.group;
+  const int r = rb * 4 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  merge_rows<D>(a, b, g, q0, qo, nsplit, r, threadIdx.x & 31);
 }
 
 template <class C>
@@ -675,7 +680,8 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   decode_splitkv_kernel<C><<<c.decode_ctas, C::kThreads, C::kSmemBytes, st>>>(tk, tv, a);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-  decode_merge_kernel<C::D><<<c.cfg.max_batch * c.cfg.num_kv_heads, 128, 0, st>>>(a);
+  const int row_blocks = (c.cfg.max_qo_len * a.group + 3) / 4;
+  decode_merge_kernel<C::D><<<c.cfg.max_batch * c.cfg.num_kv_heads * row_blocks, 128, 0, st>>>(a, row_blocks);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -47,7 +47,7 @@ int scratch_address(int dev, void** out) {
 
 int static_config_ok(const pkv_config* cfg);
 size_t static_layout_bytes(const pkv_config& cfg, int num_sms, Layout* lay);
-void static_grid_sizes(int num_sms, int* decode_ctas, int* extend_ctas);
+void static_grid_sizes(const pkv_config& cfg, int num_sms, int* decode_ctas, int* extend_ctas);
 
 }  // namespace pkv
 
@@ -79,7 +79,7 @@ extern "C" int pkv_forward_decode_static(const pkv_config* cfg, int32_t batch, c
   if (st != PKV_OK) return st;
   c.ws = static_cast<char*>(scratch);
   c.num_sms = sms;
-  static_grid_sizes(sms, &c.decode_ctas, &c.extend_ctas);
+  static_grid_sizes(*cfg, sms, &c.decode_ctas, &c.extend_ctas);
   c.batch = batch;
   c.mode = PKV_MODE_DECODE;
   c.qo_given = false;

@@ -40,16 +40,28 @@ int check_config(const pkv_config* cfg) {
   return PKV_OK;
 }
 
-// Persistent-grid sizes; both need the SM count of the device.
-void grid_sizes(int num_sms, int* decode_ctas, int* extend_ctas) {
-  *decode_ctas = num_sms * 2;
-  *extend_ctas = num_sms;
+// Persistent-grid sizes: two decode CTAs and one extend CTA per SM, never
+// more than the configuration can ever give them work. Decode items per batch
+// are at most max_pages_total / (minimum chunk) + max_batch (every request
+// adds at most one partial chunk); extend units at most
+// ceil(max_q_tokens * group / 256) + max_batch.
+void grid_sizes(const pkv_config& cfg, int num_sms, int* decode_ctas, int* extend_ctas) {
+  const long long group = cfg.num_q_heads / cfg.num_kv_heads;
+  const long long dec_units =
+      (long long)cfg.num_kv_heads * ((long long)cfg.max_pages_total / kDecodeMinChunkPages + cfg.max_batch + 1);
+  const long long ext_units =
+      (long long)cfg.num_kv_heads * (((long long)cfg.max_q_tokens * group + kExtendUnitRows - 1) / kExtendUnitRows +
+                                     cfg.max_batch);
+  *decode_ctas = (int)(dec_units < num_sms * 2ll ? dec_units : num_sms * 2ll);
+  *extend_ctas = (int)(ext_units < num_sms ? ext_units : num_sms);
+  if (*decode_ctas < 1) *decode_ctas = 1;
+  if (*extend_ctas < 1) *extend_ctas = 1;
 }
 
 Layout make_layout(const pkv_config& cfg, int num_sms) {
   Layout L;
   int dctas, ectas;
-  grid_sizes(num_sms, &dctas, &ectas);
+  grid_sizes(cfg, num_sms, &dctas, &ectas);
   const int group = cfg.num_q_heads / cfg.num_kv_heads;
   const long long target = (long long)dctas * kDecodeTargetWaves;
   L.max_decode_items = (int)(target + cfg.max_batch + 1);
@@ -169,8 +181,8 @@ size_t static_layout_bytes(const pkv_config& cfg, int num_sms, Layout* lay) {
   return lay->total;
 }
 
-void static_grid_sizes(int num_sms, int* decode_ctas, int* extend_ctas) {
-  grid_sizes(num_sms, decode_ctas, extend_ctas);
+void static_grid_sizes(const pkv_config& cfg, int num_sms, int* decode_ctas, int* extend_ctas) {
+  grid_sizes(cfg, num_sms, decode_ctas, extend_ctas);
 }
 
 }  // namespace pkv
@@ -236,7 +248,7 @@ int pkv_create(const pkv_config* cfg, void* d_workspace, size_t workspace_bytes,
   c->lay = lay;
   c->ws = static_cast<char*>(d_workspace);
   c->num_sms = sms;
-  grid_sizes(sms, &c->decode_ctas, &c->extend_ctas);
+  grid_sizes(*cfg, sms, &c->decode_ctas, &c->extend_ctas);
   c->batch = 0;
   c->mode = PKV_MODE_IDLE;
   c->qo_given = false;
