@@ -42,7 +42,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (profiles/), valid only while the kernel source is unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("extend_tc", "prefix_extend"): {"src_sha": "e5a4373850e98b26", "bytes_per_launch": 919979520,
+                                     "source": "profiles/extend_tc_prefix_extend.md"},
+}
 
 
 def peaks():
