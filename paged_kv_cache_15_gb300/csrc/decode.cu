@@ -28,6 +28,8 @@
 // to -inf, so unused pool slots never reach the result.
 #include <math.h>
 
+#include <algorithm>
+
 #include "pkv_internal.cuh"
 
 namespace pkv {
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* plan = a.m.plan;
+  pdl_launch_dependents();
 
   if (tid == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -184,6 +187,9 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   __syncthreads();
+  // launched with programmatic serialization: the metadata (and the K/V this
+  // step stored) are only read after the preceding grid has finished
+  pdl_wait();
 
   const int n_units = plan[kDecodeItems] * a.num_kv_heads;
 
@@ -633,21 +639,32 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
 }
 
 
-// Split merge: a (request, KV head) group's rows (query tokens x heads of the
-// group) are spread over CTAs of 4 warps, one row per warp.
+// Split merge: every (request, KV head) group's rows (query tokens x heads of
+// the group) get one warp each; blocks of 4 warps walk (group, row block)
+// items with a grid stride. Groups of requests with one split, or with more
+// rows per head than max_rows_per_head (those were not split on the calling
+// path), are skipped. The extend path merges its own (tile-aligned) split
+// counts, the decode path the decode plan's.
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a, int row_blocks) {
-  const int grp = blockIdx.x / row_blocks, rb = blockIdx.x % row_blocks;
-  const int b = grp / a.num_kv_heads, g = grp % a.num_kv_heads;
-  if (b >= a.m.plan[kBatch]) return;
-  const int nsplit = a.m.n_splits[b];
-  if (nsplit <= 1) return;
-  const int q0 = a.m.qo_indptr[b];
-  const int qo = a.m.qo_indptr[b + 1] - q0;
-  const int rows = qo * a.group;
-  const int r = rb * 4 + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  merge_rows<D>(a, b, g, q0, qo, nsplit, r, threadIdx.x & 31);
+__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a, int row_blocks, int max_rows_per_head,
+                                                           int n_items, int count_word, int extend_path) {
+  pdl_wait();  // the partial rows come from the preceding attention grid
+  if (a.m.plan[count_word] == 0) return;  // nothing was split on this path
+  const int bs = a.m.plan[kBatch];
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int grp = item / row_blocks, rb = item % row_blocks;
+    const int b = grp / a.num_kv_heads, g = grp % a.num_kv_heads;
+    if (b >= bs) continue;
+    const int nsplit = extend_path ? a.m.ext_splits[b] : a.m.n_splits[b];
+    if (nsplit <= 1) continue;
+    const int q0 = a.m.qo_indptr[b];
+    const int qo = a.m.qo_indptr[b + 1] - q0;
+    const int rows = qo * a.group;
+    if (rows > max_rows_per_head) continue;
+    const int r = rb * 4 + (threadIdx.x >> 5);
+    if (r >= rows) continue;
+    merge_rows<D>(a, b, g, q0, qo, nsplit, r, threadIdx.x & 31);
+  }
 }
 
 template <class C>
@@ -678,10 +695,10 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
-  decode_splitkv_kernel<C><<<c.decode_ctas, C::kThreads, C::kSmemBytes, st>>>(tk, tv, a);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-  const int row_blocks = (c.cfg.max_qo_len * a.group + 3) / 4;
-  decode_merge_kernel<C::D><<<c.cfg.max_batch * c.cfg.num_kv_heads * row_blocks, 128, 0, st>>>(a, row_blocks);
+  if (launch_pdl(decode_splitkv_kernel<C>, dim3(c.decode_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, a) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  return launch_split_merge(c, out, lse, c.cfg.max_qo_len * a.group, false, st);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -744,6 +761,33 @@ int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool,
   }
 #undef PKV_RUN
   return PKV_ERR_UNSUPPORTED;
+}
+
+int launch_split_merge(Ctx& c, void* out, float* lse, int max_rows_per_head, bool extend_path, cudaStream_t st) {
+  DecodeArgs a;
+  a.m = make_meta(c);
+  a.q = nullptr;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.num_q_heads = c.cfg.num_q_heads;
+  a.num_kv_heads = c.cfg.num_kv_heads;
+  a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
+  a.scale_log2 = 0.f;
+  a.v_scale = 1.f;
+  const long long rows_cap = std::min<long long>(max_rows_per_head, (long long)c.cfg.max_q_tokens * a.group);
+  const int row_blocks = (int)((rows_cap + 3) / 4);
+  const long long items = (long long)c.cfg.max_batch * c.cfg.num_kv_heads * row_blocks;
+  const long long grid = std::min<long long>(items, (long long)c.num_sms * 8);
+  if (items <= 0) return PKV_OK;
+  const int word = extend_path ? kSplitExtend : kSplitDecode;
+  cudaError_t e;
+  if (c.cfg.head_dim == 128)
+    e = launch_pdl(decode_merge_kernel<128>, dim3((unsigned)grid), dim3(128), 0, st, a, row_blocks, max_rows_per_head,
+                   (int)items, word, extend_path ? 1 : 0);
+  else
+    e = launch_pdl(decode_merge_kernel<64>, dim3((unsigned)grid), dim3(128), 0, st, a, row_blocks, max_rows_per_head,
+                   (int)items, word, extend_path ? 1 : 0);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* plan = a.m.plan;
+  pdl_launch_dependents();
 
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {
@@ -182,6 +183,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  // launched with programmatic serialization: metadata, Q and the K/V this
+  // step stored are only read after the preceding grid has finished
+  pdl_wait();
 
   const int n_units = plan[kExtendTiles] * a.num_kv_heads;
   const int G = a.group;
@@ -206,10 +210,10 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
         const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
         const int g = w % a.num_kv_heads;
-        const int nT = max(u.kv_a, u.kv_b);
+        const int kend = min(u.kv1, max(u.kv_a, u.kv_b));
         const int np = a.m.kv_indptr[u.b + 1] - a.m.kv_indptr[u.b];
         const int page_base = a.m.kv_indptr[u.b];
-        for (int j = 0; j < nT; ++j, ++jt) {
+        for (int j = u.kv0; j < kend; ++j, ++jt) {
           const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
           // the tile's page indices: independent loads issued before the ring wait
           int pg[kPagesPerTile];
@@ -278,14 +282,16 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       };
       for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
         const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
-        const int n[2] = {u.kv_a, u.kv_b};
+        // tiles [kb, kb + n[x]) of this unit's KV range for tile X
+        const int kb = u.kv0;
+        const int n[2] = {max(0, min(u.kv1, u.kv_a) - kb), max(0, min(u.kv1, u.kv_b) - kb)};
         const int nT = max(n[0], n[1]);
         if (nT == 0) continue;
         for (int x = 0; x < 2; ++x)
           if (n[x] > 0 && !wait(&q_full[x], ucount[x] & 1)) break;
         if (!ok) break;
         tc_fence_after();
-        // prologue: S_X(0) for both tiles
+        // prologue: S_X of the first tile for both tiles
         if (!wait(&k_full[jt % NK], (jt / NK) & 1)) break;
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
@@ -335,9 +341,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
       const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
       const int g = w % a.num_kv_heads;
-      const int nA = u.kv_a;
-      const int nX = x == 0 ? u.kv_a : u.kv_b;
-      const int nT = max(u.kv_a, u.kv_b);
+      const int kb = u.kv0;
+      const int endA = min(u.kv1, u.kv_a);                        // tile A: KV tiles [kb, endA)
+      const int endX = min(u.kv1, x == 0 ? u.kv_a : u.kv_b);      // this warpgroup's tile
+      const int nX = max(0, endX - kb);
+      const int nT = max(0, min(u.kv1, max(u.kv_a, u.kv_b)) - kb);
+      const bool split = u.split >= 0;
       const int b = u.b;
       const int q0 = a.m.qo_indptr[b];
       const int qo = a.m.qo_indptr[b + 1] - q0;
@@ -348,11 +357,22 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       const int tok = min(R / G, qo - 1);
       const int limit = L - qo + tok;
       const long long orow = (long long)(q0 + R / G) * a.num_q_heads + g * G + R % G;
+      // split units write fp32 partial rows (normalised output and LSE) that
+      // the merge kernel combines across the request's splits
+      const long long prow =
+          split ? ((long long)a.m.partial_indptr[b] + (long long)u.split * qo + R / G) * a.num_q_heads + g * G + R % G
+                : 0;
       if (nX == 0) {
         if (valid) {
-          for (int c = 0; c < D; c += 8)
-            *reinterpret_cast<uint4*>(a.out + orow * D + c) = make_uint4(0, 0, 0, 0);
-          if (a.lse) a.lse[orow] = -INFINITY;
+          if (split) {
+            for (int c = 0; c < D; c += 4)
+              *reinterpret_cast<float4*>(a.m.partial_o + prow * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            a.m.partial_lse[prow] = -INFINITY;
+          } else {
+            for (int c = 0; c < D; c += 8)
+              *reinterpret_cast<uint4*>(a.out + orow * D + c) = make_uint4(0, 0, 0, 0);
+            if (a.lse) a.lse[orow] = -INFINITY;
+          }
         }
         jt += nT;
         continue;
@@ -375,8 +395,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       }
       float m_ref = -INFINITY, l = 0.f;
       bool aborted = false;
-      for (int j = 0; j < nX; ++j) {
-        const uint32_t jj = jt + j;
+      for (int j = kb; j < endX; ++j) {
+        const uint32_t jj = jt + (j - kb);
         if (!mbar_wait_ab(&s_full[x], tcount & 1, plan, s_abort)) {
           aborted = true;
           break;
@@ -386,7 +406,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         const bool diag = key0 + kExtendKeys - 1 > limit;  // some keys of this tile are masked for this row
         // the request's last page inside this KV tile: zero the V rows past L
         // (done by the first tile that reads this V tile, before its PV)
-        if ((x == 0 || j >= nA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
+        if ((x == 0 || j >= endA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
           const int vs = jj % NV;
           if (!mbar_wait_ab(&v_full[vs], (jj / NV) & 1, plan, s_abort)) {
             aborted = true;
@@ -417,11 +437,26 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             mask32(sr + 32, key0 + cc * 32 + 32, limit);
           }
         };
-        bool rebase = j == 0;
-        float mt = -INFINITY;
-        if (j > 0) {
-          // one pass: P against the running reference, row max alongside
-          const uint64_t nref2 = f2_pack(-m_ref, -m_ref);
+        if (j == kb) {
+          // first tile of the unit: the reference is this tile's row max
+          float mx = -INFINITY;
+#pragma unroll
+          for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
+            uint32_t sr[64];
+            load_s(cc, sr);
+            mx = max32(sr + 32, max32(sr, mx));
+          }
+          m_ref = mx * a.scale_log2;
+        }
+        // P against the running reference, row max alongside. If the max grew
+        // past the reference by more than 2^8 (rare), move the reference,
+        // rescale O and run the pass again: S is still intact in TMEM.
+#pragma unroll 1
+        for (int attempt = 0; attempt < 2; ++attempt) {
+          const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+          const uint64_t nref2 = f2_pack(-ref, -ref);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = 0;
           float mx = -INFINITY;
 #pragma unroll
           for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
@@ -431,54 +466,29 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             exp32(sr, sc2, nref2, pk + cc * 16, acc);
             exp32(sr + 32, sc2, nref2, pk + cc * 16 + 16, acc);
           }
-          mt = mx * a.scale_log2;
-          rebase = mt > m_ref + kRescaleThreshold;
-        }
-        if (rebase) {
-          // first tile, or the row max grew past the reference by more than
-          // 2^8: move the reference, rescale O, recompute P from S (still intact)
-          if (j == 0) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
-              uint32_t sr[64];
-              load_s(cc, sr);
-              mx = max32(sr + 32, max32(sr, mx));
-            }
-            m_ref = mx * a.scale_log2;
-          } else {
-            // O_X must hold every earlier PV before it is rescaled
-            if (!mbar_wait_ab(&pv_done[x], (tcount - 1) & 1, plan, s_abort)) {
-              aborted = true;
-              break;
-            }
-            tc_fence_after();
-            const float alpha = fast_exp2(m_ref - mt);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(lane_base + o_col + c * 32, o);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(lane_base + o_col + c * 32, o);
-            }
-            tmem_wait_st();
-            l *= alpha;
-            m_ref = mt;
+          const float mt = mx * a.scale_log2;
+          if (!(mt > m_ref + kRescaleThreshold)) break;
+          // O_X must hold every earlier PV before it is rescaled
+          if (!mbar_wait_ab(&pv_done[x], (tcount - 1) & 1, plan, s_abort)) {
+            aborted = true;
+            break;
           }
-          const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-          const uint64_t nref2 = f2_pack(-ref, -ref);
+          tc_fence_after();
+          const float alpha = fast_exp2(m_ref - mt);
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + o_col + c * 32, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = 0;
-#pragma unroll
-          for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
-            uint32_t sr[64];
-            load_s(cc, sr);
-            exp32(sr, sc2, nref2, pk + cc * 16, acc);
-            exp32(sr + 32, sc2, nref2, pk + cc * 16 + 16, acc);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(lane_base + o_col + c * 32, o);
           }
+          tmem_wait_st();
+          l *= alpha;
+          m_ref = mt;
         }
+        if (aborted) break;
         // P overwrites the first half of this tile's S columns
         tmem_st32(lane_base + s_col, pk);
         tmem_st32(lane_base + s_col + 32, pk + 32);
@@ -507,19 +517,33 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         tmem_ld32(lane_base + o_col + c * 32, o);
         tmem_wait_ld();
         if (valid) {
+          if (split) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(o[i + 0]) * inv, __uint_as_float(o[i + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
-            *reinterpret_cast<uint4*>(a.out + orow * D + c * 32 + i) = v;
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(a.m.partial_o + prow * D + c * 32 + i) =
+                  make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                              __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(o[i + 0]) * inv, __uint_as_float(o[i + 1]) * inv);
+              v.y = pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+              v.z = pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
+              v.w = pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
+              *reinterpret_cast<uint4*>(a.out + orow * D + c * 32 + i) = v;
+            }
           }
         }
       }
       tc_fence_before();
-      if (valid && a.lse) a.lse[orow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      if (valid) {
+        const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        if (split)
+          a.m.partial_lse[prow] = lse_v;
+        else if (a.lse)
+          a.lse[orow] = lse_v;
+      }
       jt += nT;
     }
   }
@@ -556,8 +580,11 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   if (cudaFuncSetAttribute(extend_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return PKV_ERR_CUDA;
-  extend_tc_kernel<C><<<c.extend_ctas, C::kThreads, C::kSmemBytes, st>>>(tk, tv, a);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  if (launch_pdl(extend_tc_kernel<C>, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, a) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  // requests whose rows fit one unit were split along their KV range
+  return launch_split_merge(c, out, lse, kExtendUnitRows, true, st);
 }
 
 }  // namespace

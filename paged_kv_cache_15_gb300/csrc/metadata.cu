@@ -27,12 +27,14 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxCtas = 64;
+constexpr int kPagesPerKvTile = kExtendKeys / kPageSize;
 
 struct ReqInfo {
   int L;       // KV length used (0 if the request's lengths were invalid)
   int qo;      // query rows
   int np;      // pages
   int nsplit;  // decode splits
+  int esplit;  // extend KV splits (1 unless the rows fit one unit and the range is cut)
   int prow;    // partial-output rows (0 when the request has a single split)
   int qtiles;  // extend query tiles
   bool bad;
@@ -40,7 +42,7 @@ struct ReqInfo {
 
 struct Sums {
   long long np, qo, ns, pr, qt, npqo;
-  int maxqo;
+  int maxqo, splitd, splite;
 };
 
 struct MetaArgs {
@@ -51,6 +53,7 @@ struct MetaArgs {
   int* qo_indptr;
   int* kv_len;
   int* n_splits;
+  int* ext_splits;
   int* partial_indptr;
   int* token_req;
   DecodeItem* items;
@@ -89,6 +92,13 @@ __device__ __forceinline__ ReqInfo req_info(const MetaArgs& a, int b, int chunk)
   r.nsplit = r.np > 0 ? (r.np + chunk - 1) / chunk : 1;
   r.prow = r.nsplit > 1 ? r.nsplit * r.qo : 0;
   r.qtiles = (r.qo * a.group + kExtendUnitRows - 1) / kExtendUnitRows;
+  // rows that fit one extend unit: cut the KV range into chunks of whole
+  // 128-key tiles, at least as long as the decode chunks (so the split count
+  // never exceeds the decode plan's and its partial rows fit)
+  const int ct = (chunk + kPagesPerKvTile - 1) / kPagesPerKvTile;  // KV tiles per extend split
+  const int ntiles = (r.np + kPagesPerKvTile - 1) / kPagesPerKvTile;
+  r.esplit = (r.qtiles == 1 && r.nsplit > 1) ? (ntiles + ct - 1) / ct : 1;
+  if (r.esplit > 1) r.qtiles = r.esplit;
   return r;
 }
 
@@ -106,7 +116,7 @@ __device__ __forceinline__ int warp_max(int v) {
 // Block-wide sum of a Sums record (result valid in every thread).
 __device__ Sums block_sum(Sums s) {
   __shared__ long long red[6][kThreads / 32];
-  __shared__ int redm[kThreads / 32];
+  __shared__ int redm[kThreads / 32], redd[kThreads / 32], rede[kThreads / 32];
   int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   s.np = warp_sum(s.np);
   s.qo = warp_sum(s.qo);
@@ -115,6 +125,8 @@ __device__ Sums block_sum(Sums s) {
   s.qt = warp_sum(s.qt);
   s.npqo = warp_sum(s.npqo);
   s.maxqo = warp_max(s.maxqo);
+  s.splitd = warp_sum(s.splitd);
+  s.splite = warp_sum(s.splite);
   __syncthreads();
   if (l == 0) {
     red[0][w] = s.np;
@@ -124,10 +136,14 @@ __device__ Sums block_sum(Sums s) {
     red[4][w] = s.qt;
     red[5][w] = s.npqo;
     redm[w] = s.maxqo;
+    redd[w] = s.splitd;
+    rede[w] = s.splite;
   }
   __syncthreads();
-  Sums t{0, 0, 0, 0, 0, 0, 0};
+  Sums t{0, 0, 0, 0, 0, 0, 0, 0, 0};
   for (int i = 0; i < kThreads / 32; ++i) {
+    t.splitd += redd[i];
+    t.splite += rede[i];
     t.np += red[0][i];
     t.qo += red[1][i];
     t.ns += red[2][i];
@@ -171,8 +187,11 @@ __device__ Scan5 block_exclusive_scan(const Scan5& x, Scan5& total) {
 }
 
 __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
+  // the attention kernel launched next may start its prologue now; it waits
+  // for this grid before reading any metadata
+  pdl_launch_dependents();
   // ---- 1. batch totals (identical in every CTA) ----
-  Sums s{0, 0, 0, 0, 0, 0, 0};
+  Sums s{0, 0, 0, 0, 0, 0, 0, 0, 0};
   for (int b = threadIdx.x; b < a.bs; b += kThreads) {
     int L, qo;
     bool bad;
@@ -210,6 +229,8 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
       a.plan[kPartialRows] = 0;
       a.plan[kChunkPages] = ichunk;
       a.plan[kMaxQo] = 0;
+      a.plan[kSplitDecode] = 0;
+      a.plan[kSplitExtend] = 0;
     }
     return;
   }
@@ -217,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   // ---- 2. this CTA's request range and the prefix before it ----
   int per = (a.bs + gridDim.x - 1) / gridDim.x;
   int b0 = min(a.bs, (int)blockIdx.x * per), b1 = min(a.bs, b0 + per);
-  Sums pre{0, 0, 0, 0, 0, 0, 0};
+  Sums pre{0, 0, 0, 0, 0, 0, 0, 0, 0};
   for (int b = threadIdx.x; b < b0; b += kThreads) {
     ReqInfo r = req_info(a, b, ichunk);
     pre.np += r.np;
@@ -228,13 +249,15 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   }
   Sums base = block_sum(pre);
   // totals of the scanned quantities over the whole batch (for the plan words)
-  Sums all{0, 0, 0, 0, 0, 0, 0};
+  Sums all{0, 0, 0, 0, 0, 0, 0, 0, 0};
   if (blockIdx.x == 0) {
     for (int b = threadIdx.x; b < a.bs; b += kThreads) {
       ReqInfo r = req_info(a, b, ichunk);
       all.ns += r.nsplit;
       all.pr += r.prow;
       all.qt += r.qtiles;
+      all.splitd += r.nsplit > 1 ? 1 : 0;
+      all.splite += r.esplit > 1 ? 1 : 0;
     }
     all = block_sum(all);
   }
@@ -245,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   __shared__ int s_info[kThreads][kInfo];
   for (int t0 = b0; t0 < b1; t0 += kThreads) {
     const int b = t0 + threadIdx.x;
-    ReqInfo r{0, 0, 0, 0, 0, 0, false};
+    ReqInfo r{0, 0, 0, 0, 1, 0, 0, false};
     const bool live = b < b1;
     if (live) r = req_info(a, b, ichunk);
     Scan5 x{{r.np, r.qo, r.nsplit, r.prow, r.qtiles}};
@@ -261,6 +284,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
       a.partial_indptr[b] = p_pr;
       a.kv_len[b] = r.L;
       a.n_splits[b] = r.nsplit;
+      a.ext_splits[b] = r.esplit;
       a.kv_last_page_len[b] = r.np > 0 ? r.L - (r.np - 1) * kPageSize : 0;
       if (b == a.bs - 1) {
         a.kv_indptr[a.bs] = p_np + r.np;
@@ -309,14 +333,21 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
         const int last_tok = (row_end - 1) / a.group;
         return L > 0 ? (L - qo + last_tok + 1 + kExtendKeys - 1) / kExtendKeys : 0;
       };
+      const int qunits = (rows + kExtendUnitRows - 1) / kExtendUnitRows;
+      const bool split = qunits == 1 && ns > 1 && qt > 1;
+      const int chunk_tiles = (ichunk + kPagesPerKvTile - 1) / kPagesPerKvTile;
       for (int t = threadIdx.x; t < qt; t += kThreads) {
         if (tbase + t < a.max_tiles) {
-          const int row0 = t * kExtendUnitRows;
+          const int row0 = split ? 0 : t * kExtendUnitRows;
           ExtendTile et;
           et.b = bb;
           et.row0 = row0;
           et.kv_a = kv_tiles_to(min(row0 + kExtendRows, rows));
           et.kv_b = row0 + kExtendRows < rows ? kv_tiles_to(min(row0 + kExtendUnitRows, rows)) : 0;
+          et.split = split ? t : -1;
+          et.kv0 = split ? t * chunk_tiles : 0;
+          et.kv1 = split ? (t + 1) * chunk_tiles : 0x7fffffff;
+          et.pad = 0;
           a.tiles[tbase + t] = et;
         }
       }
@@ -342,6 +373,8 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
     a.plan[kExtendTiles] = items_over ? 0 : (int)all.qt;
     a.plan[kPartialRows] = (int)all.pr;
     a.plan[kMaxQo] = tot.maxqo;
+    a.plan[kSplitDecode] = items_over ? 0 : all.splitd;
+    a.plan[kSplitExtend] = items_over ? 0 : all.splite;
   }
 }
 
@@ -358,6 +391,7 @@ int launch_build_metadata(Ctx& c, int batch, const int32_t* seq_lens, const int3
   a.qo_indptr = const_cast<int*>(m.qo_indptr);
   a.kv_len = const_cast<int*>(m.kv_len);
   a.n_splits = const_cast<int*>(m.n_splits);
+  a.ext_splits = const_cast<int*>(m.ext_splits);
   a.partial_indptr = const_cast<int*>(m.partial_indptr);
   a.token_req = const_cast<int*>(m.token_req);
   a.items = const_cast<DecodeItem*>(m.decode_items);

@@ -44,14 +44,16 @@ int check_config(const pkv_config* cfg) {
 // more than the configuration can ever give them work. Decode items per batch
 // are at most max_pages_total / (minimum chunk) + max_batch (every request
 // adds at most one partial chunk); extend units at most
-// ceil(max_q_tokens * group / 256) + max_batch.
+// ceil(max_q_tokens * group / 256) + max_batch, plus as many KV splits as
+// decode items.
 void grid_sizes(const pkv_config& cfg, int num_sms, int* decode_ctas, int* extend_ctas) {
   const long long group = cfg.num_q_heads / cfg.num_kv_heads;
   const long long dec_units =
       (long long)cfg.num_kv_heads * ((long long)cfg.max_pages_total / kDecodeMinChunkPages + cfg.max_batch + 1);
   const long long ext_units =
       (long long)cfg.num_kv_heads * (((long long)cfg.max_q_tokens * group + kExtendUnitRows - 1) / kExtendUnitRows +
-                                     cfg.max_batch);
+                                     cfg.max_batch) +
+      dec_units;  // KV splits of requests whose rows fit one unit
   *decode_ctas = (int)(dec_units < num_sms * 2ll ? dec_units : num_sms * 2ll);
   *extend_ctas = (int)(ext_units < num_sms ? ext_units : num_sms);
   if (*decode_ctas < 1) *decode_ctas = 1;
@@ -65,7 +67,9 @@ Layout make_layout(const pkv_config& cfg, int num_sms) {
   const int group = cfg.num_q_heads / cfg.num_kv_heads;
   const long long target = (long long)dctas * kDecodeTargetWaves;
   L.max_decode_items = (int)(target + cfg.max_batch + 1);
-  L.max_extend_tiles = (int)(((long long)cfg.max_q_tokens * group + kExtendRows - 1) / kExtendRows + cfg.max_batch);
+  // unsplit units, plus the splits of requests whose rows fit one unit
+  L.max_extend_tiles = (int)(((long long)cfg.max_q_tokens * group + kExtendUnitRows - 1) / kExtendUnitRows +
+                             cfg.max_batch + L.max_decode_items);
   long long cap = 2ll * cfg.max_q_tokens;
   if (cap < cfg.max_q_tokens + target) cap = cfg.max_q_tokens + target;
   L.partial_rows_cap = (int)cap;
@@ -82,6 +86,7 @@ Layout make_layout(const pkv_config& cfg, int num_sms) {
   L.qo_indptr = take(sizeof(int) * (cfg.max_batch + 1));
   L.kv_len = take(sizeof(int) * cfg.max_batch);
   L.n_splits = take(sizeof(int) * cfg.max_batch);
+  L.ext_splits = take(sizeof(int) * cfg.max_batch);
   L.partial_indptr = take(sizeof(int) * (cfg.max_batch + 1));
   L.token_req = take(sizeof(int) * (size_t)cfg.max_q_tokens);
   L.decode_items = take(sizeof(DecodeItem) * (size_t)L.max_decode_items);
@@ -139,6 +144,7 @@ Meta make_meta(const Ctx& c) {
   m.qo_indptr = reinterpret_cast<const int*>(w + c.lay.qo_indptr);
   m.kv_len = reinterpret_cast<const int*>(w + c.lay.kv_len);
   m.n_splits = reinterpret_cast<const int*>(w + c.lay.n_splits);
+  m.ext_splits = reinterpret_cast<const int*>(w + c.lay.ext_splits);
   m.partial_indptr = reinterpret_cast<const int*>(w + c.lay.partial_indptr);
   m.token_req = reinterpret_cast<const int*>(w + c.lay.token_req);
   m.decode_items = reinterpret_cast<const DecodeItem*>(w + c.lay.decode_items);

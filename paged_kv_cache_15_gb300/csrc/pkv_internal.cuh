@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pkv.h"
 
 namespace pkv {
@@ -39,6 +41,8 @@ enum PlanWord : int {
   kExtendTiles = 7,    // number of (request, q-tile) items on the extend path
   kPartialRows = 8,    // rows of the partial-output buffer in use
   kMaxQo = 9,          // max qo_len in the batch
+  kSplitDecode = 10,   // requests with more than one split on the decode path
+  kSplitExtend = 11,   // requests split along their KV range on the extend path
   kPlanWords = 32
 };
 
@@ -47,16 +51,19 @@ struct DecodeItem {
   int b, split, p0, p1;
 };
 // Work item of the extend path: request, first query row (token * group +
-// head-in-group) of a 256-row unit, and the number of 128-key KV tiles its
-// first and second 128-row tile reach (0 when the tile has no rows).
+// head-in-group) of a 256-row unit, the number of 128-key KV tiles its first
+// and second 128-row tile reach (0 when the tile has no rows), and the KV tile
+// range [kv0, kv1) it covers. A request whose rows fit one unit is split along
+// its KV range like the decode path (split >= 0: the unit writes fp32
+// partials merged afterwards); otherwise split = -1 and the range is whole.
 struct ExtendTile {
-  int b, row0, kv_a, kv_b;
+  int b, row0, kv_a, kv_b, split, kv0, kv1, pad;
 };
 
 // Byte offsets of every buffer inside the caller's workspace.
 struct Layout {
-  size_t plan, kv_indptr, kv_indices, kv_last_page_len, qo_indptr, kv_len, n_splits, partial_indptr, token_req,
-      decode_items, extend_tiles, partial_o, partial_lse, total;
+  size_t plan, kv_indptr, kv_indices, kv_last_page_len, qo_indptr, kv_len, n_splits, ext_splits, partial_indptr,
+      token_req, decode_items, extend_tiles, partial_o, partial_lse, total;
   int max_decode_items, max_extend_tiles, partial_rows_cap;
 };
 
@@ -81,7 +88,8 @@ struct Meta {
   const int* kv_last_page_len;
   const int* qo_indptr;
   const int* kv_len;
-  const int* n_splits;
+  const int* n_splits;    // decode-path splits per request
+  const int* ext_splits;  // extend-path KV splits per request (1 when not split); never above n_splits
   const int* partial_indptr;
   const int* token_req;
   const DecodeItem* decode_items;
@@ -101,6 +109,10 @@ int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool,
                   float v_scale, void* out, float* lse, cudaStream_t st);
 int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, void* out,
                   float* lse, cudaStream_t st);
+// LSE merge of split partials for requests whose rows per KV head are at most
+// max_rows_per_head (the decode path: its largest tile; the extend path: 256,
+// the requests it split).
+int launch_split_merge(Ctx& c, void* out, float* lse, int max_rows_per_head, bool extend_path, cudaStream_t st);
 
 // Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
 int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t outer,
@@ -109,9 +121,35 @@ int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint
                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
                    CUtensorMapSwizzle swz);
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes, so it must execute pdl_wait()
+// before touching any global memory that earlier work writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // Device helpers
 // ---------------------------------------------------------------------------
+// Wait until the preceding grid in the stream has finished and its memory
+// operations are visible (no-op when launched without programmatic serialization).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream start launching its CTAs.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void record_error(int* plan, int code, int index) {
   if (atomicCAS(&plan[kErr], 0, code) == 0) plan[kErrIndex] = index;
 }

@@ -366,3 +366,16 @@ def test_extend_graph_replay():
     ref_o, ref_lse = oracle_reference(W)
     check_close(d.out.double().cpu().numpy(), ref_o, "o (graph)")
     check_close(d.lse.double().cpu().numpy(), ref_lse, "lse (graph)")
+
+
+def test_extend_mixed_split_and_unsplit_requests():
+    """Requests whose rows fit one 256-row unit are split along their KV range
+    (partials + merge); long query blocks are not. Both in one batch."""
+    W = make_workload("mix", "extend", 5, 32, 8, 128, [6000, 0, 3000, 9000, 17],
+                      [3, 700, 64, 1, 40])
+    full_check(W)
+
+
+def test_verify_prefill_path_long_context_split():
+    W = make_workload("vlong", "verify", 4, 64, 4, 128, [20000, 300, 12000, 5000], [8, 4, 6, 7])
+    full_check(W, spec_mode=B.PKV_SPEC_PREFILL)
