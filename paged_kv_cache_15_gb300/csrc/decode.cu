@@ -48,6 +48,7 @@ struct DecodeCfg {
   static constexpr int STAGES = STAGES_;
   static constexpr int kConsumerWarps = WR * WK;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static constexpr int kMinBlocks = kThreads <= 160 ? 2 : 1;  // two CTAs per SM hide latency for the decode shapes
   static constexpr int kRows = 16 * WR;
   static constexpr int kStageKeys = WK * KPW;
   static constexpr int kStagePages = kStageKeys / kPageSize;
@@ -158,7 +159,7 @@ __device__ __forceinline__ void merge_rows(const DecodeArgs& a, int b, int g, in
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
+__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                      const __grid_constant__ CUtensorMap tmap_v,
                                                                      DecodeArgs a) {
   constexpr int D = C::D;
@@ -341,7 +342,9 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
         named_bar_sync(1, C::kConsumerWarps * 32);
       }
 
-      if (!skip) {
+      // a row-warp whose 16 rows are all padding (fewer drafts than the tile
+      // holds) still takes part in the stage protocol but computes nothing
+      if (!skip && (C::WR == 1 || wr * 16 < rows_valid)) {
 #pragma unroll
         for (int kb = 0; kb < C::KPW / 16; ++kb) {
           const int kr0 = wk * C::KPW + kb * 16;  // first stage row of this 16-key block
@@ -568,8 +571,9 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int c = ocol<C::FP8>(nt, qd, e);
-            my[rq * D + c] = o[nt][e];
-            my[(rq + 8) * D + c] = o[nt][2 + e];
+            // columns XOR-swizzled by row so the 8 rows of a store hit 8 bank groups
+            my[rq * D + (c ^ ((rq & 7) << 2))] = o[nt][e];
+            my[(rq + 8) * D + (c ^ ((rq & 7) << 2))] = o[nt][2 + e];
           }
         }
         if (qd == 0) {
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__(C::kThreads) decode_splitkv_kernel(const __gri
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < C::WK; ++k) {
-            const float4 x = *reinterpret_cast<const float4*>(scr + (k * 16 + r) * D + c4 * 4);
+            const float4 x = *reinterpret_cast<const float4*>(scr + (k * 16 + r) * D + ((c4 * 4) ^ ((r & 7) << 2)));
             acc.x += x.x * wgt[k];
             acc.y += x.y * wgt[k];
             acc.z += x.z * wgt[k];

@@ -54,6 +54,8 @@ void grid_sizes(const pkv_config& cfg, int num_sms, int* decode_ctas, int* exten
       (long long)cfg.num_kv_heads * (((long long)cfg.max_q_tokens * group + kExtendUnitRows - 1) / kExtendUnitRows +
                                      cfg.max_batch) +
       dec_units;  // KV splits of requests whose rows fit one unit
+  // two per SM: the decode shapes fit twice; the verify shapes fit once, and
+  // the second wave then picks up units as CTAs of the first one finish
   *decode_ctas = (int)(dec_units < num_sms * 2ll ? dec_units : num_sms * 2ll);
   *extend_ctas = (int)(ext_units < num_sms ? ext_units : num_sms);
   if (*decode_ctas < 1) *decode_ctas = 1;
