@@ -43,8 +43,16 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (profiles/), valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("extend_tc", "prefix_extend"): {"src_sha": "e5a4373850e98b26", "bytes_per_launch": 919979520,
+    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "6f5043deb3beb7af", "bytes_per_launch": 1386761472,
+                                             "source": "profiles/decode_splitkv_llama3_8b_decode.md"},
+    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "6f5043deb3beb7af", "bytes_per_launch": 1471666176,
+                                            "source": "profiles/dram_traffic_fp8_and_verify.md"},
+    ("decode_splitkv", "spec_verify"): {"src_sha": "6f5043deb3beb7af", "bytes_per_launch": 601986304,
+                                        "source": "profiles/dram_traffic_fp8_and_verify.md"},
+    ("extend_tc", "prefix_extend"): {"src_sha": "b873d5a3bcc2d58c", "bytes_per_launch": 855017984,
                                      "source": "profiles/extend_tc_prefix_extend.md"},
+    ("extend_tc", "spec_verify"): {"src_sha": "b873d5a3bcc2d58c", "bytes_per_launch": 602822912,
+                                   "source": "profiles/dram_traffic_fp8_and_verify.md"},
 }
 
 
