@@ -19,9 +19,11 @@
 //              O / l), and writes the output rows.
 //   warps 8, 10 producers: gather K (warp 8) and V (warp 10) pages with TMA
 //              (one 16-token box per page and 128-byte column block, 128-byte
-//              swizzle) into separate K and V rings.
+//              swizzle) into separate K and V rings; lane p reads the tile's
+//              p-th page index and an elected lane issues the copies.
 //   warp 9     MMA: owns 512 TMEM columns and issues tcgen05.mma
-//              (kind::f16, bf16 in, fp32 accumulate):
+//              (kind::f16, bf16 in, fp32 accumulate) from an elected lane of
+//              the converged warp:
 //                S_X = Q_X K^T      (M=128, N=128 keys, K=head_dim; A, B from smem)
 //                O_X += P_X V       (M=128, N=head_dim, K=128 keys; P from TMEM)
 //              in the order PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1), so one
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   uint64_t* v_empty = v_full + NV;      // [NV]
   uint64_t* s_full = v_empty + NV;      // [2] S_X computed
   uint64_t* p_full = s_full + 2;        // [2] P_X written
-  uint64_t* pv_done = p_full + 2;       // [2] PV_X finished
+  uint64_t* pv_done = p_full + 2;       // [2] last PV_X of a unit finished
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
@@ -155,9 +157,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&q_full[x], 128);
+      mbar_init(&q_full[x], 4);  // one arrival per softmax warp
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 128);
+      mbar_init(&p_full[x], 4);
       mbar_init(&pv_done[x], 1);
     }
     for (int s = 0; s < NK; ++s) {
@@ -201,135 +203,140 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     uint64_t* empty = is_v ? v_empty : k_empty;
     const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
     const int ring_off = is_v ? C::kVOff : C::kKOff;
-    if (lane == 0) {
-      prefetch_tmap(tmap);
-      const uint64_t pol = policy_evict_first();
-      uint32_t jt = 0;
-      uint32_t armed = 0, armed_ph = 0;
-      bool stop = false;
-      for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
-        const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
-        const int g = w % a.num_kv_heads;
-        const int kend = min(u.kv1, max(u.kv_a, u.kv_b));
-        const int np = a.m.kv_indptr[u.b + 1] - a.m.kv_indptr[u.b];
-        const int page_base = a.m.kv_indptr[u.b];
-        for (int j = u.kv0; j < kend; ++j, ++jt) {
-          const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
-          // the tile's page indices: independent loads issued before the ring wait
-          int pg[kPagesPerTile];
-#pragma unroll
-          for (int p = 0; p < kPagesPerTile; ++p)
-            pg[p] = p < npg ? __ldg(a.m.kv_indices + page_base + j * kPagesPerTile + p) : 0;
-          const int st = jt % depth;
-          const uint32_t ph = (jt / depth) & 1;
-          if (!mbar_wait_ab(&empty[st], ph ^ 1, plan, s_abort)) {
-            stop = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[st], (uint32_t)(npg * kPageSize * D * 2));
-          uint8_t* dst = smem + ring_off + st * C::kTileBytes;
-#pragma unroll
-          for (int p = 0; p < kPagesPerTile; ++p) {
-            if (p < npg) {
-#pragma unroll
-              for (int cb = 0; cb < C::kColBlocks; ++cb)
-                tma_load_2d_hint(dst + cb * (kExtendKeys * 128) + p * (kPageSize * 128), tmap, g * D + cb * 64,
-                                 pg[p] * kPageSize, &full[st], pol);
-            }
-          }
-          armed |= 1u << st;
-          armed_ph = (armed_ph & ~(1u << st)) | (ph << st);
+    // the whole warp runs the loop; lane p loads the tile's p-th page index and
+    // one elected lane issues the copies
+    if (elect_one()) prefetch_tmap(tmap);
+    const uint64_t pol = policy_evict_first();
+    uint32_t jt = 0;
+    uint32_t armed = 0, armed_ph = 0;
+    bool stop = false;
+    for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
+      const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
+      const int g = w % a.num_kv_heads;
+      const int kend = min(u.kv1, max(u.kv_a, u.kv_b));
+      const int np = a.m.kv_indptr[u.b + 1] - a.m.kv_indptr[u.b];
+      const int page_base = a.m.kv_indptr[u.b];
+      for (int j = u.kv0; j < kend; ++j, ++jt) {
+        const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
+        const int my_pg = lane < npg ? __ldg(a.m.kv_indices + page_base + j * kPagesPerTile + lane) : 0;
+        const int st = jt % depth;
+        const uint32_t ph = (jt / depth) & 1;
+        if (!mbar_wait_warp(&empty[st], ph ^ 1, plan, s_abort)) {
+          stop = true;
+          break;
         }
+        const bool leader = elect_one();
+        if (leader) mbar_arrive_expect_tx(&full[st], (uint32_t)(npg * kPageSize * D * 2));
+        uint8_t* dst = smem + ring_off + st * C::kTileBytes;
+#pragma unroll
+        for (int p = 0; p < kPagesPerTile; ++p) {
+          const int pg = __shfl_sync(0xffffffffu, my_pg, p);
+          if (p < npg && leader) {
+#pragma unroll
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_2d_hint(dst + cb * (kExtendKeys * 128) + p * (kPageSize * 128), tmap, g * D + cb * 64,
+                               pg * kPageSize, &full[st], pol);
+          }
+        }
+        armed |= 1u << st;
+        armed_ph = (armed_ph & ~(1u << st)) | (ph << st);
       }
-      if (stop) *s_abort = 1;
-      // never leave the CTA with a TMA still writing into shared memory
-      for (int s2 = 0; s2 < depth; ++s2)
-        if (armed & (1u << s2)) mbar_wait(&full[s2], (armed_ph >> s2) & 1, plan);
     }
+    if (stop && lane == 0) *s_abort = 1;
+    // never leave the CTA with a TMA still writing into shared memory (this
+    // wait ignores the abort flag on purpose)
+    for (int s2 = 0; s2 < depth; ++s2)
+      if (armed & (1u << s2)) mbar_wait(&full[s2], (armed_ph >> s2) & 1, plan);
+    __syncwarp();
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_bf16(kExtendRows, kExtendKeys, false, false);
-      constexpr uint32_t idesc_pv = umma_idesc_bf16(kExtendRows, D, false, true);
-      uint32_t jt = 0;
-      uint32_t tcount[2] = {0, 0};  // tiles processed per X (phase of s_full / p_full / pv_done)
-      uint32_t ucount[2] = {0, 0};  // units processed per X (phase of q_full)
-      bool ok = true;
-      auto wait = [&](uint64_t* bar, uint32_t parity) {
-        if (ok && !mbar_wait_ab(bar, parity, plan, s_abort)) ok = false;
-        return ok;
-      };
-      auto issue_qk = [&](int x, int ks) {
-        const uint32_t q_addr = smem_base + C::kQOff + x * C::kQBytes;
-        const uint32_t k_addr = smem_base + C::kKOff + ks * C::kTileBytes;
+    // The whole warp runs the loop and one elected lane issues each tcgen05
+    // instruction. Descriptors: the start-address field is the low bits, so a
+    // byte offset b inside the tile adds b >> 4.
+    constexpr uint32_t idesc_qk = umma_idesc_bf16(kExtendRows, kExtendKeys, false, false);
+    constexpr uint32_t idesc_pv = umma_idesc_bf16(kExtendRows, D, false, true);
+    const uint64_t q_desc0 = umma_desc_sw128(smem_base + C::kQOff, 16, 1024);
+    const uint64_t k_desc0 = umma_desc_sw128(smem_base + C::kKOff, 16, 1024);
+    const uint64_t v_desc0 = umma_desc_sw128(smem_base + C::kVOff, kExtendKeys * 128, 1024);
+    uint32_t jt = 0;
+    uint32_t tcount[2] = {0, 0};  // tiles processed per X (phase of s_full / p_full)
+    uint32_t ucount[2] = {0, 0};  // units processed per X (phase of q_full / pv_done)
+    bool ok = true;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      if (ok && !mbar_wait_warp(bar, parity, plan, s_abort)) ok = false;
+      return ok;
+    };
+    auto issue_qk = [&](int x, int ks) {
+      const uint64_t qd = q_desc0 + (uint32_t)((x * C::kQBytes) >> 4);
+      const uint64_t kd = k_desc0 + (uint32_t)((ks * C::kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kExtendRows * 128) + (kk & 3) * 32;
-          const uint64_t qd = umma_desc_sw128(q_addr + off, 16, 1024);
-          const uint64_t kd = umma_desc_sw128(k_addr + (kk >> 2) * (kExtendKeys * 128) + (kk & 3) * 32, 16, 1024);
-          umma_bf16(tmem + x * 128, qd, kd, idesc_qk, kk > 0);
-        }
-        umma_commit(&s_full[x]);
-      };
-      auto issue_pv = [&](int x, int vs, bool first) {
-        const uint32_t v_addr = smem_base + C::kVOff + vs * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kExtendKeys / 16; ++kk) {
-          const uint64_t vd = umma_desc_sw128(v_addr + kk * 16 * 128, kExtendKeys * 128, 1024);
-          umma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, vd, idesc_pv, !(first && kk == 0));
-        }
-        umma_commit(&pv_done[x]);
-      };
-      for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
-        const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
-        // tiles [kb, kb + n[x]) of this unit's KV range for tile X
-        const int kb = u.kv0;
-        const int n[2] = {max(0, min(u.kv1, u.kv_a) - kb), max(0, min(u.kv1, u.kv_b) - kb)};
-        const int nT = max(n[0], n[1]);
-        if (nT == 0) continue;
-        for (int x = 0; x < 2; ++x)
-          if (n[x] > 0 && !wait(&q_full[x], ucount[x] & 1)) break;
-        if (!ok) break;
-        tc_fence_after();
-        // prologue: S_X of the first tile for both tiles
-        if (!wait(&k_full[jt % NK], (jt / NK) & 1)) break;
-        tc_fence_after();
-        for (int x = 0; x < 2; ++x)
-          if (n[x] > 0) issue_qk(x, jt % NK);
-        umma_commit(&k_empty[jt % NK]);
-        for (int j = 0; j < nT && ok; ++j) {
-          const uint32_t jj = jt + j;
-          const int vs = jj % NV;
-          bool v_ready = false, k_ready = false;
-          for (int x = 0; x < 2; ++x) {
-            if (j >= n[x]) continue;
-            if (!wait(&p_full[x], tcount[x] & 1)) break;
-            if (!v_ready) {
-              if (!wait(&v_full[vs], (jj / NV) & 1)) break;
-              v_ready = true;
-            }
-            tc_fence_after();
-            issue_pv(x, vs, j == 0);
-            ++tcount[x];
-            if (j + 1 < n[x]) {
-              if (!k_ready) {
-                if (!wait(&k_full[(jj + 1) % NK], ((jj + 1) / NK) & 1)) break;
-                tc_fence_after();
-                k_ready = true;
-              }
-              issue_qk(x, (jj + 1) % NK);
-            }
-          }
-          if (!ok) break;
-          umma_commit(&v_empty[vs]);
-          if (k_ready) umma_commit(&k_empty[(jj + 1) % NK]);
-        }
-        jt += nT;
-        for (int x = 0; x < 2; ++x)
-          if (n[x] > 0) ++ucount[x];
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = ((kk >> 2) * (kExtendRows * 128) + (kk & 3) * 32) >> 4;
+        const uint32_t ko = ((kk >> 2) * (kExtendKeys * 128) + (kk & 3) * 32) >> 4;
+        umma_bf16_warp(tmem + x * 128, qd + qo, kd + ko, idesc_qk, kk > 0);
       }
-      if (!ok) *s_abort = 1;
+      umma_commit_warp(&s_full[x]);
+    };
+    // pv_done is committed only after the last PV of the unit for tile X (the
+    // epilogue waits for it); an earlier PV_X is known complete once the
+    // s_full commit that follows it has fired
+    auto issue_pv = [&](int x, int vs, bool first, bool last) {
+      const uint64_t vd = v_desc0 + (uint32_t)((vs * C::kTileBytes) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < kExtendKeys / 16; ++kk)
+        umma_bf16_ts_warp(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+                          !(first && kk == 0));
+      if (last) umma_commit_warp(&pv_done[x]);
+    };
+    for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+      const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
+      // tiles [kb, kb + n[x]) of this unit's KV range for tile X
+      const int kb = u.kv0;
+      const int n[2] = {max(0, min(u.kv1, u.kv_a) - kb), max(0, min(u.kv1, u.kv_b) - kb)};
+      const int nT = max(n[0], n[1]);
+      if (nT == 0) continue;
+      for (int x = 0; x < 2; ++x)
+        if (n[x] > 0 && !wait(&q_full[x], ucount[x] & 1)) break;
+      if (!ok) break;
+      tc_fence_after();
+      // prologue: S_X of the first tile for both tiles
+      if (!wait(&k_full[jt % NK], (jt / NK) & 1)) break;
+      tc_fence_after();
+      for (int x = 0; x < 2; ++x)
+        if (n[x] > 0) issue_qk(x, jt % NK);
+      umma_commit_warp(&k_empty[jt % NK]);
+      for (int j = 0; j < nT && ok; ++j) {
+        const uint32_t jj = jt + j;
+        const int vs = jj % NV;
+        bool v_ready = false, k_ready = false;
+        for (int x = 0; x < 2; ++x) {
+          if (j >= n[x]) continue;
+          if (!wait(&p_full[x], tcount[x] & 1)) break;
+          if (!v_ready) {
+            if (!wait(&v_full[vs], (jj / NV) & 1)) break;
+            v_ready = true;
+          }
+          tc_fence_after();
+          issue_pv(x, vs, j == 0, j + 1 == n[x]);
+          ++tcount[x];
+          if (j + 1 < n[x]) {
+            if (!k_ready) {
+              if (!wait(&k_full[(jj + 1) % NK], ((jj + 1) / NK) & 1)) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_qk(x, (jj + 1) % NK);
+          }
+        }
+        if (!ok) break;
+        umma_commit_warp(&v_empty[vs]);
+        if (k_ready) umma_commit_warp(&k_empty[(jj + 1) % NK]);
+      }
+      jt += nT;
+      for (int x = 0; x < 2; ++x)
+        if (n[x] > 0) ++ucount[x];
     }
+    if (!ok && lane == 0) *s_abort = 1;
   } else {
     // ------------------------------------------------------------ softmax / epilogue
     const int x = warp >> 2;          // tile of this warpgroup
@@ -338,6 +345,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     const uint32_t s_col = x * 128, o_col = 256 + x * 128;
     uint8_t* qtile = smem + C::kQOff + x * C::kQBytes;
     uint32_t jt = 0, tcount = 0;
+    uint32_t ucount = 0;  // units with work for this tile (phase of pv_done)
     for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
       const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
       const int g = w % a.num_kv_heads;
@@ -391,13 +399,15 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             *reinterpret_cast<uint4*>(qtile + h * (kExtendRows * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v[c];
         }
         fence_proxy_async_smem();
-        mbar_arrive(&q_full[x]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[x]);
       }
       float m_ref = -INFINITY, l = 0.f;
       bool aborted = false;
       for (int j = kb; j < endX; ++j) {
         const uint32_t jj = jt + (j - kb);
-        if (!mbar_wait_ab(&s_full[x], tcount & 1, plan, s_abort)) {
+        // warp-uniform waits: every lane of the warp leaves the loop together
+        if (!mbar_wait_warp(&s_full[x], tcount & 1, plan, s_abort)) {
           aborted = true;
           break;
         }
@@ -408,7 +418,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         // (done by the first tile that reads this V tile, before its PV)
         if ((x == 0 || j >= endA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
           const int vs = jj % NV;
-          if (!mbar_wait_ab(&v_full[vs], (jj / NV) & 1, plan, s_abort)) {
+          if (!mbar_wait_warp(&v_full[vs], (jj / NV) & 1, plan, s_abort)) {
             aborted = true;
             break;
           }
@@ -468,12 +478,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           }
           const float mt = mx * a.scale_log2;
           if (!(mt > m_ref + kRescaleThreshold)) break;
-          // O_X must hold every earlier PV before it is rescaled
-          if (!mbar_wait_ab(&pv_done[x], (tcount - 1) & 1, plan, s_abort)) {
-            aborted = true;
-            break;
-          }
-          tc_fence_after();
+          // O_X holds every earlier PV: the s_full commit waited on above was
+          // issued after PV_X of the previous tile
           const float alpha = fast_exp2(m_ref - mt);
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -497,7 +503,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         l += f2_lo(accs) + f2_hi(accs);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[x]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[x]);
         ++tcount;
       }
       if (aborted) {
@@ -505,10 +512,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         break;
       }
       // epilogue: O / l once the last PV of this tile has finished
-      if (!mbar_wait_ab(&pv_done[x], (tcount - 1) & 1, plan, s_abort)) {
+      if (!mbar_wait_warp(&pv_done[x], ucount & 1, plan, s_abort)) {
         *s_abort = 1;
         break;
       }
+      ++ucount;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
