@@ -38,7 +38,10 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
+// Bounds on one tile's row sum of p = 2^(s * scale - m_ref) between which the
+// reference m_ref stays put (see the softmax role).
+constexpr float kSumHigh = 65536.0f;               // 2^16
+constexpr float kSumLow = 5.421010862427522e-20f;  // 2^-64
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
@@ -402,7 +405,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full[x]);
       }
-      float m_ref = -INFINITY, l = 0.f;
+      // m_ref: the row's reference in the log2 domain (p = 2^(s * scale - m_ref));
+      // l: the row's running sum of p
+      float m_ref = 0.f, l = 0.f;
       bool aborted = false;
       for (int j = kb; j < endX; ++j) {
         const uint32_t jj = jt + (j - kb);
@@ -436,7 +441,6 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         }
         const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
         uint32_t pk[kExtendKeys / 2];  // P as bf16 pairs, written to TMEM once final
-        uint64_t acc[4] = {0, 0, 0, 0};
         // S read 64 columns per TMEM wait; masked keys become -inf
         auto load_s = [&](int cc, uint32_t* sr) {
           tmem_ld32(lane_base + s_col + cc * 32, sr);
@@ -447,60 +451,67 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             mask32(sr + 32, key0 + cc * 32 + 32, limit);
           }
         };
-        if (j == kb) {
-          // first tile of the unit: the reference is this tile's row max
-          float mx = -INFINITY;
+        // P of the tile against the reference; returns the tile's row sum
+        auto exp_pass = [&]() {
+          const uint64_t nref2 = f2_pack(-m_ref, -m_ref);
+          uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
           for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
             uint32_t sr[64];
             load_s(cc, sr);
-            mx = max32(sr + 32, max32(sr, mx));
-          }
-          m_ref = mx * a.scale_log2;
-        }
-        // P against the running reference, row max alongside. If the max grew
-        // past the reference by more than 2^8 (rare), move the reference,
-        // rescale O and run the pass again: S is still intact in TMEM.
-#pragma unroll 1
-        for (int attempt = 0; attempt < 2; ++attempt) {
-          const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-          const uint64_t nref2 = f2_pack(-ref, -ref);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = 0;
-          float mx = -INFINITY;
-#pragma unroll
-          for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
-            uint32_t sr[64];
-            load_s(cc, sr);
-            mx = max32(sr + 32, max32(sr, mx));
             exp32(sr, sc2, nref2, pk + cc * 16, acc);
             exp32(sr + 32, sc2, nref2, pk + cc * 16 + 16, acc);
           }
+          const uint64_t accs = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+          return f2_lo(accs) + f2_hi(accs);
+        };
+        float tsum = exp_pass();
+        // The tile sum bounds every p of the row: while it is at most 2^16 no p
+        // can overflow bf16 P or the fp32 O and l, and the reference (which
+        // cancels in O / l) stays put, so the common path needs no row max.
+        // Otherwise (a score far above the reference, or a row with no mass
+        // yet whose visible scores sit far below it) take the tile's exact
+        // max, move the reference, rescale O and l, and run the pass again: S
+        // is still intact in TMEM. TMEM loads and stores are warp-collective,
+        // so the whole warp takes this branch when any of its rows needs it;
+        // the other rows keep their reference and get the same P again. A row
+        // that sees no key of this tile (limit < key0) never needs it.
+        const bool need = (!(tsum <= kSumHigh) || (l == 0.f && tsum < kSumLow)) && limit >= key0;
+        if (__any_sync(0xffffffffu, need)) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
+            uint32_t sr[64];
+            load_s(cc, sr);
+            mx = max32(sr + 32, max32(sr, mx));
+          }
           const float mt = mx * a.scale_log2;
-          if (!(mt > m_ref + kRescaleThreshold)) break;
+          const bool move = need && mt != -INFINITY && (mt > m_ref || l == 0.f);
           // O_X holds every earlier PV: the s_full commit waited on above was
           // issued after PV_X of the previous tile
-          const float alpha = fast_exp2(m_ref - mt);
+          const float alpha = move && l > 0.f ? fast_exp2(m_ref - mt) : 1.f;
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + o_col + c * 32, o);
-            tmem_wait_ld();
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(lane_base + o_col + c * 32, o);
+              tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(lane_base + o_col + c * 32, o);
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(lane_base + o_col + c * 32, o);
+            }
+            tmem_wait_st();
           }
-          tmem_wait_st();
-          l *= alpha;
-          m_ref = mt;
+          if (move) {
+            l *= alpha;
+            m_ref = mt;
+          }
+          tsum = exp_pass();
         }
-        if (aborted) break;
         // P overwrites the first half of this tile's S columns
         tmem_st32(lane_base + s_col, pk);
         tmem_st32(lane_base + s_col + 32, pk + 32);
-        const uint64_t acc01 = f2_add(acc[0], acc[1]), acc23 = f2_add(acc[2], acc[3]);
-        const uint64_t accs = f2_add(acc01, acc23);
-        l += f2_lo(accs) + f2_hi(accs);
+        l += tsum;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();

@@ -300,6 +300,44 @@ def test_extend_parity(case):
     full_check(W)
 
 
+def _shift_scores(W, q_scale=1.0, heads=None, bias=0.0):
+    """Moves the scores far outside the N(0,1) range of the presets: Q (or only
+    the given query heads) is multiplied by q_scale, and bias is added to the
+    first component of every Q row and subtracted from that of every K row,
+    which shifts q.k by about -bias^2. The oracle sees the same bf16 values."""
+    q = W.q.float()
+    sel = slice(None) if heads is None else list(heads)
+    q[:, sel] = q[:, sel] * q_scale
+    if bias:
+        q[:, :, 0] += bias
+        for name in ("k_pool", "k_new"):
+            t = getattr(W, name).float()
+            t[..., 0] -= bias
+            setattr(W, name, t.bfloat16())
+    W.q = q.bfloat16()
+    return W
+
+
+@pytest.mark.parametrize("case", ["large_scores", "mixed_heads", "far_below"])
+@pytest.mark.parametrize("mode", ["extend", "decode"])
+def test_scores_far_from_reference(mode, case):
+    """Scores of magnitude ~2^5 to ~2^7 in the exponent: the softmax reference
+    has to move up for every row (large_scores), for some rows of a warp only
+    (mixed_heads: two query heads scaled), or down for rows whose scores all
+    sit far below zero (far_below: without a move every p would flush to 0)."""
+    if mode == "extend":
+        W = make_workload("sx_" + case, "extend", 3, 8, 2, 128, [40, 0, 300], [150, 70, 9])
+    else:
+        W = make_workload("sd_" + case, "decode", 4, 8, 2, 128, [37, 100, 211, 1300], [1, 1, 1, 1])
+    if case == "large_scores":
+        _shift_scores(W, q_scale=12.0)
+    elif case == "mixed_heads":
+        _shift_scores(W, q_scale=12.0, heads=[1, 6])
+    else:
+        _shift_scores(W, bias=34.0)
+    full_check(W)
+
+
 def test_extend_rows_exceeding_group_tiles():
     # group 16: a 128-row tile holds 8 tokens
     W = make_workload("g16", "extend", 3, 64, 4, 128, [10, 500, 0], [20, 9, 130])
