@@ -11,16 +11,20 @@
 //
 // Warp roles (352 threads, one CTA per SM, persistent over units):
 //   warps 0-3  softmax A, warps 4-7 softmax B: thread r of a warpgroup owns
-//              row r of its tile (TMEM lane r). It copies its Q row into shared
-//              memory at the start of a unit, reads S from TMEM, masks, keeps
-//              the running max / sum in the log2 domain, writes P (bf16) back
-//              into the first half of its S columns, rescales O in TMEM only
-//              when the max grows by more than 2^8 (the factor cancels in
-//              O / l), and writes the output rows.
+//              row r of its tile (TMEM lane r). It reads S from TMEM, masks,
+//              keeps the running sum against a reference in the log2 domain,
+//              writes P (bf16) back into the first half of its S columns,
+//              moves the reference and rescales O in TMEM only when the tile
+//              sum leaves a fixed range (the factor cancels in O / l), and
+//              writes the output rows.
 //   warps 8, 10 producers: gather K (warp 8) and V (warp 10) pages with TMA
 //              (one 16-token box per page and 128-byte column block, 128-byte
 //              swizzle) into separate K and V rings; lane p reads the tile's
-//              p-th page index and an elected lane issues the copies.
+//              p-th page index and an elected lane issues the copies. Warp 8
+//              also fills the Q tiles of the next unit as soon as the last QK
+//              on them has finished: one TMA box of 128/G tokens x the G heads
+//              of the group per column block when G divides 128 and the box
+//              lies inside the batch, else the softmax warps copy their rows.
 //   warp 9     MMA: owns 512 TMEM columns and issues tcgen05.mma
 //              (kind::f16, bf16 in, fp32 accumulate) from an elected lane of
 //              the converged warp:
@@ -30,6 +34,7 @@
 //              tile's softmax runs while the tensor core works on the other.
 // TMEM columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
 #include <math.h>
+#include <string.h>
 
 #include "pkv_internal.cuh"
 
@@ -115,7 +120,7 @@ struct ExtCfg {
   static constexpr int kKOff = 2 * kQBytes;
   static constexpr int kVOff = kKOff + NK * kTileBytes;
   static constexpr int kBarOff = kVOff + NV * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6;
+  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6 + 4;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAbortOff = kTmemSlotOff + 8;
   static constexpr int kSmemBytes = kAbortOff + 8 + 1024;
@@ -131,11 +136,14 @@ struct ExtendArgs {
   float* lse;
   int num_q_heads, num_kv_heads, group;
   float scale_log2;
+  int q_tma;         // 1 when the group divides 128: a Q tile is one TMA box of 128/G tokens x G heads
+  int q_box_tokens;  // 128 / group
 };
 
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                    const __grid_constant__ CUtensorMap tmap_v,
+                                                                   const __grid_constant__ CUtensorMap tmap_q,
                                                                    ExtendArgs a) {
   constexpr int D = C::D;
   constexpr int NK = C::NK, NV = C::NV;
@@ -151,6 +159,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   uint64_t* s_full = v_empty + NV;      // [2] S_X computed
   uint64_t* p_full = s_full + 2;        // [2] P_X written
   uint64_t* pv_done = p_full + 2;       // [2] last PV_X of a unit finished
+  uint64_t* q_empty = pv_done + 2;      // [2] last QK_X of a unit finished: Q_X may be refilled
+  uint64_t* q_written = q_empty + 2;    // [2] softmax warps wrote Q_X (tiles not loaded by TMA)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
@@ -160,10 +170,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&q_full[x], 4);  // one arrival per softmax warp
+      mbar_init(&q_full[x], 1);  // the K producer (plus the TMA bytes when Q comes by TMA)
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 4);
+      mbar_init(&p_full[x], 4);  // one arrival per softmax warp
       mbar_init(&pv_done[x], 1);
+      mbar_init(&q_empty[x], 1);
+      mbar_init(&q_written[x], 4);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
@@ -195,6 +207,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   const int n_units = plan[kExtendTiles] * a.num_kv_heads;
   const int G = a.group;
   const uint32_t smem_base = smem_u32(smem);
+  const int total_q = plan[kTotalQ];
+  // Tile X of unit u takes its Q by TMA when the box of 128/G tokens lies
+  // inside the batch's tokens (never past the end of the caller's q buffer);
+  // otherwise the softmax warps write it.
+  auto q_by_tma = [&](const ExtendTile& u, int x) {
+    return a.q_tma != 0 && a.m.qo_indptr[u.b] + (u.row0 + x * kExtendRows) / G + a.q_box_tokens <= total_q;
+  };
 
   if (warp == C::kProducerWarp || warp == C::kVProducerWarp) {
     // ------------------------------------------------------------ producers
@@ -208,10 +227,15 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     const int ring_off = is_v ? C::kVOff : C::kKOff;
     // the whole warp runs the loop; lane p loads the tile's p-th page index and
     // one elected lane issues the copies
-    if (elect_one()) prefetch_tmap(tmap);
+    if (elect_one()) {
+      prefetch_tmap(tmap);
+      if (!is_v && a.q_tma) prefetch_tmap(&tmap_q);
+    }
     const uint64_t pol = policy_evict_first();
     uint32_t jt = 0;
     uint32_t armed = 0, armed_ph = 0;
+    uint32_t qcount[2] = {0, 0};   // Q tiles issued per X (phase of q_full / q_empty)
+    uint32_t qtcount[2] = {0, 0};  // of those, written by the softmax warps (phase of q_written)
     bool stop = false;
     for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
       const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
@@ -219,6 +243,37 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       const int kend = min(u.kv1, max(u.kv_a, u.kv_b));
       const int np = a.m.kv_indptr[u.b + 1] - a.m.kv_indptr[u.b];
       const int page_base = a.m.kv_indptr[u.b];
+      if (!is_v) {
+        // the unit's Q tiles, each once the previous unit's last QK on it has
+        // finished: by TMA (a box of 128/G tokens x the group's G heads), or
+        // forwarded from the softmax warps that wrote it
+        for (int x = 0; x < 2; ++x) {
+          if (min(u.kv1, x == 0 ? u.kv_a : u.kv_b) <= u.kv0) continue;  // no KV tile for X
+          if (!mbar_wait_warp(&q_empty[x], (qcount[x] & 1) ^ 1, plan, s_abort)) {
+            stop = true;
+            break;
+          }
+          if (q_by_tma(u, x)) {
+            if (elect_one()) {
+              mbar_arrive_expect_tx(&q_full[x], (uint32_t)C::kQBytes);
+              const int tok = a.m.qo_indptr[u.b] + (u.row0 + x * kExtendRows) / G;
+#pragma unroll
+              for (int cb = 0; cb < C::kColBlocks; ++cb)
+                tma_load_3d(smem + C::kQOff + x * C::kQBytes + cb * (kExtendRows * 128), &tmap_q, cb * 64, g * G,
+                            tok, &q_full[x]);
+            }
+          } else {
+            if (!mbar_wait_warp(&q_written[x], qtcount[x] & 1, plan, s_abort)) {
+              stop = true;
+              break;
+            }
+            ++qtcount[x];
+            if (elect_one()) mbar_arrive(&q_full[x]);
+          }
+          ++qcount[x];
+        }
+        if (stop) break;
+      }
       for (int j = u.kv0; j < kend; ++j, ++jt) {
         const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
         const int my_pg = lane < npg ? __ldg(a.m.kv_indices + page_base + j * kPagesPerTile + lane) : 0;
@@ -246,10 +301,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       }
     }
     if (stop && lane == 0) *s_abort = 1;
-    // never leave the CTA with a TMA still writing into shared memory (this
-    // wait ignores the abort flag on purpose)
+    // never leave the CTA with a TMA still writing into shared memory (these
+    // waits ignore the abort flag on purpose). The last phase of each Q
+    // barrier completes only after every earlier one.
     for (int s2 = 0; s2 < depth; ++s2)
       if (armed & (1u << s2)) mbar_wait(&full[s2], (armed_ph >> s2) & 1, plan);
+    for (int x = 0; x < 2; ++x)
+      if (qcount[x] > 0) mbar_wait(&q_full[x], (qcount[x] - 1) & 1, plan);
     __syncwarp();
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -263,7 +321,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     const uint64_t v_desc0 = umma_desc_sw128(smem_base + C::kVOff, kExtendKeys * 128, 1024);
     uint32_t jt = 0;
     uint32_t tcount[2] = {0, 0};  // tiles processed per X (phase of s_full / p_full)
-    uint32_t ucount[2] = {0, 0};  // units processed per X (phase of q_full / pv_done)
+    uint32_t ucount[2] = {0, 0};  // units processed per X (phase of q_full)
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       if (ok && !mbar_wait_warp(bar, parity, plan, s_abort)) ok = false;
@@ -305,8 +363,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       // prologue: S_X of the first tile for both tiles
       if (!wait(&k_full[jt % NK], (jt / NK) & 1)) break;
       tc_fence_after();
-      for (int x = 0; x < 2; ++x)
-        if (n[x] > 0) issue_qk(x, jt % NK);
+      for (int x = 0; x < 2; ++x) {
+        if (n[x] == 0) continue;
+        issue_qk(x, jt % NK);
+        if (n[x] == 1) umma_commit_warp(&q_empty[x]);  // the unit's last QK_X: Q_X may be refilled
+      }
       umma_commit_warp(&k_empty[jt % NK]);
       for (int j = 0; j < nT && ok; ++j) {
         const uint32_t jj = jt + j;
@@ -319,6 +380,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             if (!wait(&v_full[vs], (jj / NV) & 1)) break;
             v_ready = true;
           }
+          // The unit's first PV_X overwrites O_X. The previous unit's epilogue
+          // has read it: the softmax warps release p_full of this tile only
+          // after finishing that epilogue.
           tc_fence_after();
           issue_pv(x, vs, j == 0, j + 1 == n[x]);
           ++tcount[x];
@@ -329,6 +393,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
               k_ready = true;
             }
             issue_qk(x, (jj + 1) % NK);
+            if (j + 2 == n[x]) umma_commit_warp(&q_empty[x]);  // the unit's last QK_X
           }
         }
         if (!ok) break;
@@ -388,9 +453,10 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         jt += nT;
         continue;
       }
-      // this row of Q -> shared memory (swizzled, K-major); the tile's previous
-      // QKs finished before the previous epilogue saw its last PV complete
-      {
+      // Q tiles the producer does not load by TMA: this row of Q -> shared
+      // memory (swizzled, K-major); the tile's previous QKs finished before the
+      // previous epilogue saw its last PV complete
+      if (!q_by_tma(u, x)) {
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {  // 128 bytes of the row at a time
           uint4 v[8];
@@ -403,7 +469,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full[x]);
+        if (lane == 0) mbar_arrive(&q_written[x]);
       }
       // m_ref: the row's reference in the log2 domain (p = 2^(s * scale - m_ref));
       // l: the row's running sum of p
@@ -596,10 +662,29 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.num_kv_heads = c.cfg.num_kv_heads;
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
   a.scale_log2 = sm_scale * kLog2e;
+  // Q as [tokens][heads][head_dim]: a box of 64 elements x G heads x 128/G
+  // tokens is one 128-row tile column block, rows ordered (token, head) like
+  // the tile's rows. The token extent only bounds the map; the kernel loads a
+  // box only when all its tokens are inside the batch.
+  CUtensorMap tq;
+  memset(&tq, 0, sizeof(tq));
+  a.q_tma = 0;
+  a.q_box_tokens = 0;
+  if (kExtendRows % a.group == 0) {
+    const uint32_t box_tok = kExtendRows / a.group;
+    const uint64_t tokens = (uint64_t)(c.cfg.max_q_tokens > (int)box_tok ? c.cfg.max_q_tokens : (int)box_tok);
+    if (encode_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(q), C::D,
+                       (uint64_t)c.cfg.num_q_heads, tokens, (uint64_t)C::D * 2,
+                       (uint64_t)c.cfg.num_q_heads * C::D * 2, 64, (uint32_t)a.group, box_tok,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+      return PKV_ERR_CUDA;
+    a.q_tma = 1;
+    a.q_box_tokens = (int)box_tok;
+  }
   if (cudaFuncSetAttribute(extend_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return PKV_ERR_CUDA;
-  if (launch_pdl(extend_tc_kernel<C>, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, a) !=
+  if (launch_pdl(extend_tc_kernel<C>, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, tq, a) !=
       cudaSuccess)
     return PKV_ERR_CUDA;
   // requests whose rows fit one unit were split along their KV range

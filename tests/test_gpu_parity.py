@@ -282,7 +282,7 @@ def test_graph_replay_with_new_lengths():
 
 
 # ------------------------------------------------------------------ extend (tcgen05) and verify on the prefill path
-@pytest.mark.parametrize("case", ["small", "ragged", "d64", "mha", "prefix_zero", "long_new"])
+@pytest.mark.parametrize("case", ["small", "ragged", "d64", "mha", "prefix_zero", "long_new", "g3", "g6_d64"])
 def test_extend_parity(case):
     if case == "small":
         W = make_workload("e", "extend", 3, 8, 2, 128, [0, 37, 200], [130, 9, 61])
@@ -297,6 +297,10 @@ def test_extend_parity(case):
         W = make_workload("ez", "extend", 2, 16, 4, 128, [0, 0], [1, 383])
     elif case == "long_new":
         W = preset("prefix_extend", bs=2, len_scale=0.3)
+    elif case == "g3":  # group size that does not divide the 128-row tile
+        W = make_workload("e3", "extend", 3, 12, 4, 128, [20, 300, 0], [77, 140, 33])
+    elif case == "g6_d64":
+        W = make_workload("e6", "extend", 2, 6, 1, 64, [100, 7], [90, 200])
     full_check(W)
 
 
