@@ -104,6 +104,45 @@ __device__ __forceinline__ void exp32(const uint32_t* sr, uint64_t sc2, uint64_t
   }
 }
 
+// The two tiles' KV ranges inside a unit, and the order in which the unit's
+// KV tiles pass through the K and V rings. A shared unit streams KV tile
+// kv0 + j once, for both tiles; a dual unit (both tiles hold the same rows,
+// tile A the first half of the KV range, tile B the rest) streams, for each
+// step j, tile A's tile and then tile B's. Producers, MMA warp and softmax
+// warps all walk this same sequence.
+struct UnitKV {
+  int s0, s1, n0, n1;  // tile A's and tile B's KV tiles: [s0, s0 + n0), [s1, s1 + n1)
+  bool dual;
+  __device__ __forceinline__ int start(int x) const { return x == 0 ? s0 : s1; }
+  __device__ __forceinline__ int n(int x) const { return x == 0 ? n0 : n1; }
+  __device__ __forceinline__ int steps() const { return max(n0, n1); }
+  __device__ __forceinline__ int len() const { return dual ? n0 + n1 : max(n0, n1); }
+  // position in the unit's ring sequence of tile X's j-th KV tile
+  __device__ __forceinline__ int pos(int x, int j) const {
+    if (!dual) return j;
+    return x == 0 ? j + min(j, n1) : j + min(j + 1, n0);
+  }
+  // tile X's QKs read Q tile X (a dual unit's tiles both read Q tile A)
+  __device__ __forceinline__ bool uses_q(int x) const { return dual ? x == 0 : n(x) > 0; }
+};
+
+__device__ __forceinline__ UnitKV unit_kv(const ExtendTile& u) {
+  UnitKV k;
+  k.dual = u.dual != 0;
+  if (k.dual) {
+    const int n = max(0, min(u.kv1, u.kv_a) - u.kv0);
+    k.s0 = u.kv0;
+    k.n0 = (n + 1) >> 1;
+    k.s1 = u.kv0 + k.n0;
+    k.n1 = n - k.n0;
+  } else {
+    k.s0 = k.s1 = u.kv0;
+    k.n0 = max(0, min(u.kv1, u.kv_a) - u.kv0);
+    k.n1 = max(0, min(u.kv1, u.kv_b) - u.kv0);
+  }
+  return k;
+}
+
 template <int D_, int NK_, int NV_>
 struct ExtCfg {
   static constexpr int D = D_;
@@ -120,8 +159,9 @@ struct ExtCfg {
   static constexpr int kKOff = 2 * kQBytes;
   static constexpr int kVOff = kKOff + NK * kTileBytes;
   static constexpr int kBarOff = kVOff + NV * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6 + 4;
-  static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
+  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6 + 4 + 2;
+  static constexpr int kMergeOff = kBarOff + kNumBars * 8;           // dual units: tile B's (m, l) per row
+  static constexpr int kTmemSlotOff = kMergeOff + 2 * kExtendRows * 4;
   static constexpr int kAbortOff = kTmemSlotOff + 8;
   static constexpr int kSmemBytes = kAbortOff + 8 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -161,6 +201,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   uint64_t* pv_done = p_full + 2;       // [2] last PV_X of a unit finished
   uint64_t* q_empty = pv_done + 2;      // [2] last QK_X of a unit finished: Q_X may be refilled
   uint64_t* q_written = q_empty + 2;    // [2] softmax warps wrote Q_X (tiles not loaded by TMA)
+  uint64_t* b_done = q_written + 2;     // dual unit: tile B's O is final and its (m, l) are in smem
+  uint64_t* a_read = b_done + 1;        // dual unit: tile A has read tile B's O and (m, l)
+  float* s_merge = reinterpret_cast<float*>(smem + C::kMergeOff);  // [2][128]: m, l of tile B's rows
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
@@ -177,6 +220,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       mbar_init(&q_empty[x], 1);
       mbar_init(&q_written[x], 4);
     }
+    mbar_init(b_done, 4);  // one arrival per softmax warp
+    mbar_init(a_read, 4);
     for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -240,7 +285,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
       const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
       const int g = w % a.num_kv_heads;
-      const int kend = min(u.kv1, max(u.kv_a, u.kv_b));
+      const UnitKV ukv = unit_kv(u);
       const int np = a.m.kv_indptr[u.b + 1] - a.m.kv_indptr[u.b];
       const int page_base = a.m.kv_indptr[u.b];
       if (!is_v) {
@@ -248,7 +293,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         // finished: by TMA (a box of 128/G tokens x the group's G heads), or
         // forwarded from the softmax warps that wrote it
         for (int x = 0; x < 2; ++x) {
-          if (min(u.kv1, x == 0 ? u.kv_a : u.kv_b) <= u.kv0) continue;  // no KV tile for X
+          if (!ukv.uses_q(x)) continue;
           if (!mbar_wait_warp(&q_empty[x], (qcount[x] & 1) ^ 1, plan, s_abort)) {
             stop = true;
             break;
@@ -274,7 +319,17 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         }
         if (stop) break;
       }
-      for (int j = u.kv0; j < kend; ++j, ++jt) {
+      for (int e = 0; e < ukv.len(); ++e, ++jt) {
+        // e-th KV tile of the unit's sequence
+        int j;
+        if (ukv.dual) {
+          const int m = min(ukv.n0, ukv.n1);
+          const int step = e < 2 * m ? e >> 1 : e - m;
+          const int x = e < 2 * m ? (e & 1) : (ukv.n0 > ukv.n1 ? 0 : 1);
+          j = ukv.start(x) + step;
+        } else {
+          j = ukv.s0 + e;
+        }
         const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
         const int my_pg = lane < npg ? __ldg(a.m.kv_indices + page_base + j * kPagesPerTile + lane) : 0;
         const int st = jt % depth;
@@ -319,16 +374,17 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     const uint64_t q_desc0 = umma_desc_sw128(smem_base + C::kQOff, 16, 1024);
     const uint64_t k_desc0 = umma_desc_sw128(smem_base + C::kKOff, 16, 1024);
     const uint64_t v_desc0 = umma_desc_sw128(smem_base + C::kVOff, kExtendKeys * 128, 1024);
-    uint32_t jt = 0;
+    uint32_t kt = 0, vt = 0;      // K and V ring tiles consumed so far
     uint32_t tcount[2] = {0, 0};  // tiles processed per X (phase of s_full / p_full)
-    uint32_t ucount[2] = {0, 0};  // units processed per X (phase of q_full)
+    uint32_t ucount[2] = {0, 0};  // units that used Q tile X (phase of q_full)
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       if (ok && !mbar_wait_warp(bar, parity, plan, s_abort)) ok = false;
       return ok;
     };
-    auto issue_qk = [&](int x, int ks) {
-      const uint64_t qd = q_desc0 + (uint32_t)((x * C::kQBytes) >> 4);
+    // S_X = Q_qx K^T for the K tile in ring slot ks
+    auto issue_qk = [&](int x, int qx, int ks) {
+      const uint64_t qd = q_desc0 + (uint32_t)((qx * C::kQBytes) >> 4);
       const uint64_t kd = k_desc0 + (uint32_t)((ks * C::kTileBytes) >> 4);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -351,58 +407,93 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     };
     for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
       const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
-      // tiles [kb, kb + n[x]) of this unit's KV range for tile X
-      const int kb = u.kv0;
-      const int n[2] = {max(0, min(u.kv1, u.kv_a) - kb), max(0, min(u.kv1, u.kv_b) - kb)};
-      const int nT = max(n[0], n[1]);
+      const UnitKV ukv = unit_kv(u);
+      const int n[2] = {ukv.n0, ukv.n1};
+      const int nT = ukv.steps();
       if (nT == 0) continue;
       for (int x = 0; x < 2; ++x)
-        if (n[x] > 0 && !wait(&q_full[x], ucount[x] & 1)) break;
+        if (ukv.uses_q(x) && !wait(&q_full[x], ucount[x] & 1)) break;
       if (!ok) break;
       tc_fence_after();
-      // prologue: S_X of the first tile for both tiles
-      if (!wait(&k_full[jt % NK], (jt / NK) & 1)) break;
-      tc_fence_after();
-      for (int x = 0; x < 2; ++x) {
-        if (n[x] == 0) continue;
-        issue_qk(x, jt % NK);
-        if (n[x] == 1) umma_commit_warp(&q_empty[x]);  // the unit's last QK_X: Q_X may be refilled
-      }
-      umma_commit_warp(&k_empty[jt % NK]);
-      for (int j = 0; j < nT && ok; ++j) {
-        const uint32_t jj = jt + j;
-        const int vs = jj % NV;
-        bool v_ready = false, k_ready = false;
+      if (!ukv.dual) {
+        // ---- shared unit: both tiles consume KV tile kv0 + j
+        // prologue: S_X of the first tile for both tiles
+        if (!wait(&k_full[kt % NK], (kt / NK) & 1)) break;
+        tc_fence_after();
         for (int x = 0; x < 2; ++x) {
-          if (j >= n[x]) continue;
-          if (!wait(&p_full[x], tcount[x] & 1)) break;
-          if (!v_ready) {
-            if (!wait(&v_full[vs], (jj / NV) & 1)) break;
-            v_ready = true;
-          }
-          // The unit's first PV_X overwrites O_X. The previous unit's epilogue
-          // has read it: the softmax warps release p_full of this tile only
-          // after finishing that epilogue.
-          tc_fence_after();
-          issue_pv(x, vs, j == 0, j + 1 == n[x]);
-          ++tcount[x];
-          if (j + 1 < n[x]) {
-            if (!k_ready) {
-              if (!wait(&k_full[(jj + 1) % NK], ((jj + 1) / NK) & 1)) break;
-              tc_fence_after();
-              k_ready = true;
+          if (n[x] == 0) continue;
+          issue_qk(x, x, kt % NK);
+          if (n[x] == 1) umma_commit_warp(&q_empty[x]);  // the unit's last QK_X: Q_X may be refilled
+        }
+        umma_commit_warp(&k_empty[kt % NK]);
+        ++kt;
+        for (int j = 0; j < nT && ok; ++j) {
+          const int vs = vt % NV;
+          bool v_ready = false, k_ready = false;
+          for (int x = 0; x < 2; ++x) {
+            if (j >= n[x]) continue;
+            if (!wait(&p_full[x], tcount[x] & 1)) break;
+            if (!v_ready) {
+              if (!wait(&v_full[vs], (vt / NV) & 1)) break;
+              v_ready = true;
             }
-            issue_qk(x, (jj + 1) % NK);
-            if (j + 2 == n[x]) umma_commit_warp(&q_empty[x]);  // the unit's last QK_X
+            // The unit's first PV_X overwrites O_X. The previous unit's epilogue
+            // has read it: the softmax warps release p_full of this tile only
+            // after finishing that epilogue.
+            tc_fence_after();
+            issue_pv(x, vs, j == 0, j + 1 == n[x]);
+            ++tcount[x];
+            if (j + 1 < n[x]) {
+              if (!k_ready) {
+                if (!wait(&k_full[kt % NK], (kt / NK) & 1)) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_qk(x, x, kt % NK);
+              if (j + 2 == n[x]) umma_commit_warp(&q_empty[x]);  // the unit's last QK_X
+            }
+          }
+          if (!ok) break;
+          umma_commit_warp(&v_empty[vs]);
+          ++vt;
+          if (k_ready) {
+            umma_commit_warp(&k_empty[kt % NK]);
+            ++kt;
+          }
+        }
+      } else {
+        // ---- dual unit: each tile its own KV tiles, in ring order A(j), B(j);
+        // both tiles read Q tile A, refilled after the unit's last QK
+        const int qk_total = n[0] + n[1];
+        int qk_issued = 0;
+        auto qk_next = [&](int x) {
+          if (!wait(&k_full[kt % NK], (kt / NK) & 1)) return false;
+          tc_fence_after();
+          issue_qk(x, 0, kt % NK);
+          umma_commit_warp(&k_empty[kt % NK]);
+          ++kt;
+          if (++qk_issued == qk_total) umma_commit_warp(&q_empty[0]);
+          return true;
+        };
+        for (int x = 0; x < 2 && ok; ++x)
+          if (n[x] > 0) qk_next(x);
+        for (int j = 0; j < nT && ok; ++j) {
+          for (int x = 0; x < 2; ++x) {
+            if (j >= n[x]) continue;
+            if (!wait(&p_full[x], tcount[x] & 1)) break;
+            if (!wait(&v_full[vt % NV], (vt / NV) & 1)) break;
+            tc_fence_after();
+            issue_pv(x, vt % NV, j == 0, j + 1 == n[x]);
+            umma_commit_warp(&v_empty[vt % NV]);
+            ++vt;
+            ++tcount[x];
+            if (j + 1 < n[x] && !qk_next(x)) break;
           }
         }
         if (!ok) break;
-        umma_commit_warp(&v_empty[vs]);
-        if (k_ready) umma_commit_warp(&k_empty[(jj + 1) % NK]);
       }
-      jt += nT;
       for (int x = 0; x < 2; ++x)
-        if (n[x] > 0) ++ucount[x];
+        if (ukv.uses_q(x)) ++ucount[x];
     }
     if (!ok && lane == 0) *s_abort = 1;
   } else {
@@ -414,21 +505,21 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     uint8_t* qtile = smem + C::kQOff + x * C::kQBytes;
     uint32_t jt = 0, tcount = 0;
     uint32_t ucount = 0;  // units with work for this tile (phase of pv_done)
+    uint32_t du = 0;      // dual units with work (phase of b_done / a_read)
     for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
       const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
       const int g = w % a.num_kv_heads;
-      const int kb = u.kv0;
-      const int endA = min(u.kv1, u.kv_a);                        // tile A: KV tiles [kb, endA)
-      const int endX = min(u.kv1, x == 0 ? u.kv_a : u.kv_b);      // this warpgroup's tile
-      const int nX = max(0, endX - kb);
-      const int nT = max(0, min(u.kv1, max(u.kv_a, u.kv_b)) - kb);
+      const UnitKV ukv = unit_kv(u);
+      const int kb = ukv.start(x);  // this tile's KV tiles: [kb, kb + nX)
+      const int nX = ukv.n(x);
+      const int nA = ukv.n0;
       const bool split = u.split >= 0;
       const int b = u.b;
       const int q0 = a.m.qo_indptr[b];
       const int qo = a.m.qo_indptr[b + 1] - q0;
       const int L = a.m.kv_len[b];
       const int np = a.m.kv_indptr[b + 1] - a.m.kv_indptr[b];
-      const int R = u.row0 + x * kExtendRows + r;
+      const int R = u.row0 + (ukv.dual ? 0 : x * kExtendRows) + r;  // a dual unit's tiles hold the same rows
       const bool valid = R < qo * G;
       const int tok = min(R / G, qo - 1);
       const int limit = L - qo + tok;
@@ -439,7 +530,20 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           split ? ((long long)a.m.partial_indptr[b] + (long long)u.split * qo + R / G) * a.num_q_heads + g * G + R % G
                 : 0;
       if (nX == 0) {
-        if (valid) {
+        if (ukv.dual && x == 1) {
+          // a dual unit's tile B without KV tiles hands an empty half to tile A
+          if (ukv.n0 > 0) {
+            s_merge[r] = 0.f;
+            s_merge[kExtendRows + r] = 0.f;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_done);
+            if (!mbar_wait_warp(a_read, du & 1, plan, s_abort)) {
+              *s_abort = 1;
+              break;
+            }
+            ++du;
+          }
+        } else if (valid) {
           if (split) {
             for (int c = 0; c < D; c += 4)
               *reinterpret_cast<float4*>(a.m.partial_o + prow * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -450,13 +554,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             if (a.lse) a.lse[orow] = -INFINITY;
           }
         }
-        jt += nT;
+        jt += ukv.len();
         continue;
       }
       // Q tiles the producer does not load by TMA: this row of Q -> shared
       // memory (swizzled, K-major); the tile's previous QKs finished before the
       // previous epilogue saw its last PV complete
-      if (!q_by_tma(u, x)) {
+      if (ukv.uses_q(x) && !q_by_tma(u, x)) {
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {  // 128 bytes of the row at a time
           uint4 v[8];
@@ -475,8 +579,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       // l: the row's running sum of p
       float m_ref = 0.f, l = 0.f;
       bool aborted = false;
-      for (int j = kb; j < endX; ++j) {
-        const uint32_t jj = jt + (j - kb);
+      for (int jr = 0; jr < nX; ++jr) {
+        const int j = kb + jr;                      // absolute KV tile
+        const uint32_t jj = jt + ukv.pos(x, jr);    // its place in the V ring sequence
         // warp-uniform waits: every lane of the warp leaves the loop together
         if (!mbar_wait_warp(&s_full[x], tcount & 1, plan, s_abort)) {
           aborted = true;
@@ -487,7 +592,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         const bool diag = key0 + kExtendKeys - 1 > limit;  // some keys of this tile are masked for this row
         // the request's last page inside this KV tile: zero the V rows past L
         // (done by the first tile that reads this V tile, before its PV)
-        if ((x == 0 || j >= endA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
+        if ((ukv.dual || x == 0 || jr >= nA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
           const int vs = jj % NV;
           if (!mbar_wait_warp(&v_full[vs], (jj / NV) & 1, plan, s_abort)) {
             aborted = true;
@@ -595,33 +700,89 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       }
       ++ucount;
       tc_fence_after();
+      if (ukv.dual && x == 1) {
+        // dual unit, tile B: hand this half (O in TMEM, m and l in shared
+        // memory) to tile A, which merges and writes the row; O_B stays
+        // untouched until tile A has read it
+        s_merge[r] = m_ref;
+        s_merge[kExtendRows + r] = l;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_done);
+        if (!mbar_wait_warp(a_read, du & 1, plan, s_abort)) {
+          *s_abort = 1;
+          break;
+        }
+        ++du;
+        jt += ukv.len();
+        continue;
+      }
+      // weights of this tile's O (and, in a dual unit, of tile B's O), with 1/l folded in
+      float wa = 1.f, wb = 0.f;
+      if (ukv.dual) {
+        if (!mbar_wait_warp(b_done, du & 1, plan, s_abort)) {
+          *s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const float mb = s_merge[r], lb = s_merge[kExtendRows + r];
+        const float m = lb > 0.f && (l == 0.f || mb > m_ref) ? mb : m_ref;
+        wa = l > 0.f ? fast_exp2(m_ref - m) : 0.f;
+        wb = lb > 0.f ? fast_exp2(mb - m) : 0.f;
+        l = l * wa + lb * wb;
+        m_ref = m;
+      }
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      wa *= inv;
+      wb *= inv;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_base + o_col + c * 32, o);
-        tmem_wait_ld();
+        if (ukv.dual) {
+          uint32_t ob[32];
+          tmem_ld32(lane_base + 256 + kExtendRows + c * 32, ob);  // tile B's O, same rows
+          tmem_wait_ld();
+          // tile B's O counts only with a nonzero weight: without KV tiles its
+          // TMEM columns may hold anything (even NaN patterns)
+          const bool use_b = wb != 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float fb = use_b ? __uint_as_float(ob[i]) * wb : 0.f;
+            o[i] = __float_as_uint(__uint_as_float(o[i]) * wa + fb);
+          }
+        } else {
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * wa);
+        }
         if (valid) {
           if (split) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
               *reinterpret_cast<float4*>(a.m.partial_o + prow * D + c * 32 + i) =
-                  make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                              __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+                  make_float4(__uint_as_float(o[i]), __uint_as_float(o[i + 1]), __uint_as_float(o[i + 2]),
+                              __uint_as_float(o[i + 3]));
           } else {
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
               uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[i + 0]) * inv, __uint_as_float(o[i + 1]) * inv);
-              v.y = pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
-              v.z = pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
-              v.w = pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
+              v.x = pack_bf16(__uint_as_float(o[i + 0]), __uint_as_float(o[i + 1]));
+              v.y = pack_bf16(__uint_as_float(o[i + 2]), __uint_as_float(o[i + 3]));
+              v.z = pack_bf16(__uint_as_float(o[i + 4]), __uint_as_float(o[i + 5]));
+              v.w = pack_bf16(__uint_as_float(o[i + 6]), __uint_as_float(o[i + 7]));
               *reinterpret_cast<uint4*>(a.out + orow * D + c * 32 + i) = v;
             }
           }
         }
       }
       tc_fence_before();
+      if (ukv.dual) {
+        // tile B's O and (m, l) have been read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_read);
+        ++du;
+      }
       if (valid) {
         const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
         if (split)
@@ -629,7 +790,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         else if (a.lse)
           a.lse[orow] = lse_v;
       }
-      jt += nT;
+      jt += ukv.len();
     }
   }
 

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
 
   // ---- 3. scan the range tile by tile; per-element writes spread over the CTA ----
   Scan5 carry{{(int)base.np, (int)base.qo, (int)base.ns, (int)base.pr, (int)base.qt}};
-  enum { kNp, kPBase, kQo, kQBase, kNs, kSBase, kQt, kTBase, kL, kInfo };
+  enum { kNp, kPBase, kQo, kQBase, kNs, kSBase, kQt, kTBase, kL, kEs, kInfo };
   __shared__ int s_info[kThreads][kInfo];
   for (int t0 = b0; t0 < b1; t0 += kThreads) {
     const int b = t0 + threadIdx.x;
@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
       inf[kQt] = r.qtiles;
       inf[kTBase] = p_qt;
       inf[kL] = r.L;
+      inf[kEs] = r.esplit;
     }
     __syncthreads();
     const int nreq = min(kThreads, b1 - t0);
@@ -333,8 +334,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
         const int last_tok = (row_end - 1) / a.group;
         return L > 0 ? (L - qo + last_tok + 1 + kExtendKeys - 1) / kExtendKeys : 0;
       };
-      const int qunits = (rows + kExtendUnitRows - 1) / kExtendUnitRows;
-      const bool split = qunits == 1 && ns > 1 && qt > 1;
+      const bool split = inf[kEs] > 1;
       const int chunk_tiles = (ichunk + kPagesPerKvTile - 1) / kPagesPerKvTile;
       for (int t = threadIdx.x; t < qt; t += kThreads) {
         if (tbase + t < a.max_tiles) {
@@ -347,7 +347,9 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
           et.split = split ? t : -1;
           et.kv0 = split ? t * chunk_tiles : 0;
           et.kv1 = split ? (t + 1) * chunk_tiles : 0x7fffffff;
-          et.pad = 0;
+          // rows that fit one 128-row tile: both tiles hold them, each takes
+          // half of the unit's KV range, and the halves are merged in the CTA
+          et.dual = rows <= kExtendRows ? 1 : 0;
           a.tiles[tbase + t] = et;
         }
       }

@@ -56,8 +56,11 @@ struct DecodeItem {
 // range [kv0, kv1) it covers. A request whose rows fit one unit is split along
 // its KV range like the decode path (split >= 0: the unit writes fp32
 // partials merged afterwards); otherwise split = -1 and the range is whole.
+// dual = 1: the rows fit one 128-row tile; both tiles hold them, tile A takes
+// the first half of the unit's KV tiles and tile B the rest, and the two
+// halves are merged by LSE inside the CTA before anything is written.
 struct ExtendTile {
-  int b, row0, kv_a, kv_b, split, kv0, kv1, pad;
+  int b, row0, kv_a, kv_b, split, kv0, kv1, dual;
 };
 
 // Byte offsets of every buffer inside the caller's workspace.
