@@ -95,67 +95,89 @@ __device__ __forceinline__ int ocol(int nt, int q, int e) {
   }
 }
 
-// Combine the nsplit partial rows of one (request, KV head) group:
+// Combine the nsplit partial rows of one (token, query head) row:
 //   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s.
-// One warp per row, lanes across head_dim. Lane s holds split s's weight, so
-// the loads of the partial rows do not depend on each other and are issued
-// in batches. Partials were written by other CTAs, so they are read through
-// L2 (ld.global.cg), never from a stale L1 line.
+// One warp per row, lanes across head_dim. Lane s reads split s's LSE in the
+// same round trip as the first kMergeBatch partial rows (their addresses do
+// not depend on the weights); the weights then come from a warp max and sum.
+// Partials were written by other CTAs, so they are read through L2
+// (ld.global.cg), never from a stale L1 line.
+constexpr int kMergeBatch = 8;
+
 template <int D>
-__device__ __forceinline__ void merge_rows(const DecodeArgs& a, int b, int g, int q0, int qo, int nsplit, int r0,
-                                           int lane, int rstep = 1 << 30) {
-  const int G = a.group;
-  const long long pbase = a.m.partial_indptr[b];
-  constexpr int PER = D / 32;
-  for (int r = r0; r < qo * G; r += rstep) {
-    const int i = r / G, h = g * G + r % G;
-    auto lse_of = [&](int sp) {
-      return __ldcg(a.m.partial_lse + (pbase + (long long)sp * qo + i) * a.num_q_heads + h);
-    };
-    float M = -INFINITY;
-    for (int s0 = 0; s0 < nsplit; s0 += 32)
-      if (s0 + lane < nsplit) M = fmaxf(M, lse_of(s0 + lane));
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Z = 0.f;
-    if (M != -INFINITY)
-      for (int s0 = 0; s0 < nsplit; s0 += 32)
-        if (s0 + lane < nsplit) Z += fast_exp2((lse_of(s0 + lane) - M) * kLog2e);
-    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-    const float invZ = Z > 0.f ? 1.f / Z : 0.f;
-    float acc[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-    for (int s0 = 0; s0 < nsplit; s0 += 32) {
-      float my_w = 0.f;
-      if (M != -INFINITY && s0 + lane < nsplit) my_w = fast_exp2((lse_of(s0 + lane) - M) * kLog2e) * invZ;
-      const int n = min(32, nsplit - s0);
-#pragma unroll 8
-      for (int j = 0; j < n; ++j) {
-        const float wgt = __shfl_sync(0xffffffffu, my_w, j);
-        const long long pr = pbase + (long long)(s0 + j) * qo + i;
-        const float* src = a.m.partial_o + (pr * a.num_q_heads + h) * D + lane * PER;
-        if constexpr (PER == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-          acc[0] += wgt * x.x;
-          acc[1] += wgt * x.y;
-          acc[2] += wgt * x.z;
-          acc[3] += wgt * x.w;
-        } else {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-          acc[0] += wgt * x.x;
-          acc[1] += wgt * x.y;
-        }
-      }
-    }
-    const long long orow = (long long)(q0 + i) * a.num_q_heads + h;
-    uint16_t* dst = a.out + orow * D + lane * PER;
-    if constexpr (PER == 4) {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
-    }
-    if (a.lse && lane == 0) a.lse[orow] = Z > 0.f ? M + __logf(Z) : -INFINITY;
+struct MergeVec;
+template <>
+struct MergeVec<128> {
+  using T = float4;
+  __device__ static T load(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+  __device__ static void fma(float* acc, float w, const T& x) {
+    acc[0] += w * x.x;
+    acc[1] += w * x.y;
+    acc[2] += w * x.z;
+    acc[3] += w * x.w;
   }
+};
+template <>
+struct MergeVec<64> {
+  using T = float2;
+  __device__ static T load(const float* p) { return __ldcg(reinterpret_cast<const float2*>(p)); }
+  __device__ static void fma(float* acc, float w, const T& x) {
+    acc[0] += w * x.x;
+    acc[1] += w * x.y;
+  }
+};
+
+template <int D>
+__device__ __forceinline__ void merge_row(const DecodeArgs& a, long long pbase, int qo, int i, int h, int nsplit,
+                                          long long orow, int lane) {
+  constexpr int PER = D / 32;
+  using V = MergeVec<D>;
+  auto prow = [&](int sp) { return (pbase + (long long)sp * qo + i) * a.num_q_heads + h; };
+  auto lse_of = [&](int sp) { return __ldcg(a.m.partial_lse + prow(sp)); };
+  auto part = [&](int sp) { return V::load(a.m.partial_o + prow(sp) * D + lane * PER); };
+  typename V::T x[kMergeBatch];
+#pragma unroll
+  for (int sp = 0; sp < kMergeBatch; ++sp)
+    if (sp < nsplit) x[sp] = part(sp);
+  const float l0 = lane < nsplit ? lse_of(lane) : -INFINITY;
+  float M = l0;
+  for (int s0 = 32; s0 < nsplit; s0 += 32)
+    if (s0 + lane < nsplit) M = fmaxf(M, lse_of(s0 + lane));
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float w0 = M != -INFINITY && lane < nsplit ? fast_exp2((l0 - M) * kLog2e) : 0.f;
+  float Z = w0;
+  if (M != -INFINITY)
+    for (int s0 = 32; s0 < nsplit; s0 += 32)
+      if (s0 + lane < nsplit) Z += fast_exp2((lse_of(s0 + lane) - M) * kLog2e);
+  for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+  const float invZ = Z > 0.f ? 1.f / Z : 0.f;
+  w0 *= invZ;
+  float acc[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < kMergeBatch; ++sp)
+    if (sp < nsplit) V::fma(acc, __shfl_sync(0xffffffffu, w0, sp), x[sp]);
+  for (int s0 = kMergeBatch; s0 < nsplit; s0 += kMergeBatch) {
+#pragma unroll
+    for (int sp = 0; sp < kMergeBatch; ++sp)
+      if (s0 + sp < nsplit) x[sp] = part(s0 + sp);
+#pragma unroll
+    for (int sp = 0; sp < kMergeBatch; ++sp) {
+      if (s0 + sp >= nsplit) break;
+      // splits past the 32nd (rare) read their LSE again
+      const float w = s0 + sp < 32 ? __shfl_sync(0xffffffffu, w0, (s0 + sp) & 31)
+                                   : (M != -INFINITY ? fast_exp2((lse_of(s0 + sp) - M) * kLog2e) * invZ : 0.f);
+      V::fma(acc, w, x[sp]);
+    }
+  }
+  uint16_t* dst = a.out + orow * D + lane * PER;
+  if constexpr (PER == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
+  }
+  if (a.lse && lane == 0) a.lse[orow] = Z > 0.f ? M + __logf(Z) : -INFINITY;
 }
 
 template <class C>
@@ -649,25 +671,25 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
 // rows per head than max_rows_per_head (those were not split on the calling
 // path), are skipped. The extend path merges its own (tile-aligned) split
 // counts, the decode path the decode plan's.
+// One warp per (token, query head) row of the batch; rows of requests that
+// were not split on this path are skipped.
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a, int row_blocks, int max_rows_per_head,
-                                                           int n_items, int count_word, int extend_path) {
+__global__ void __launch_bounds__(256, 3) split_merge_kernel(DecodeArgs a, int max_rows_per_head, int count_word,
+                                                          int extend_path) {
   pdl_wait();  // the partial rows come from the preceding attention grid
   if (a.m.plan[count_word] == 0) return;  // nothing was split on this path
-  const int bs = a.m.plan[kBatch];
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int grp = item / row_blocks, rb = item % row_blocks;
-    const int b = grp / a.num_kv_heads, g = grp % a.num_kv_heads;
-    if (b >= bs) continue;
+  const int rows = a.m.plan[kTotalQ] * a.num_q_heads;
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nwarps) {
+    const int t = row / a.num_q_heads, h = row - t * a.num_q_heads;
+    const int b = a.m.token_req[t];
     const int nsplit = extend_path ? a.m.ext_splits[b] : a.m.n_splits[b];
     if (nsplit <= 1) continue;
     const int q0 = a.m.qo_indptr[b];
     const int qo = a.m.qo_indptr[b + 1] - q0;
-    const int rows = qo * a.group;
-    if (rows > max_rows_per_head) continue;
-    const int r = rb * 4 + (threadIdx.x >> 5);
-    if (r >= rows) continue;
-    merge_rows<D>(a, b, g, q0, qo, nsplit, r, threadIdx.x & 31);
+    if (qo * a.group > max_rows_per_head) continue;
+    merge_row<D>(a, a.m.partial_indptr[b], qo, t - q0, h, nsplit, (long long)row, lane);
   }
 }
 
@@ -778,19 +800,18 @@ int launch_split_merge(Ctx& c, void* out, float* lse, int max_rows_per_head, boo
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
   a.scale_log2 = 0.f;
   a.v_scale = 1.f;
-  const long long rows_cap = std::min<long long>(max_rows_per_head, (long long)c.cfg.max_q_tokens * a.group);
-  const int row_blocks = (int)((rows_cap + 3) / 4);
-  const long long items = (long long)c.cfg.max_batch * c.cfg.num_kv_heads * row_blocks;
-  const long long grid = std::min<long long>(items, (long long)c.num_sms * 8);
-  if (items <= 0) return PKV_OK;
+  // one warp per (token, head) row, 8 warps per CTA, 3 CTAs per SM
+  const long long rows = (long long)c.cfg.max_q_tokens * c.cfg.num_q_heads;
+  const long long grid = std::min<long long>((rows + 7) / 8, (long long)c.num_sms * 3);
+  if (rows <= 0) return PKV_OK;
   const int word = extend_path ? kSplitExtend : kSplitDecode;
   cudaError_t e;
   if (c.cfg.head_dim == 128)
-    e = launch_pdl(decode_merge_kernel<128>, dim3((unsigned)grid), dim3(128), 0, st, a, row_blocks, max_rows_per_head,
-                   (int)items, word, extend_path ? 1 : 0);
+    e = launch_pdl(split_merge_kernel<128>, dim3((unsigned)grid), dim3(256), 0, st, a, max_rows_per_head, word,
+                   extend_path ? 1 : 0);
   else
-    e = launch_pdl(decode_merge_kernel<64>, dim3((unsigned)grid), dim3(128), 0, st, a, row_blocks, max_rows_per_head,
-                   (int)items, word, extend_path ? 1 : 0);
+    e = launch_pdl(split_merge_kernel<64>, dim3((unsigned)grid), dim3(256), 0, st, a, max_rows_per_head, word,
+                   extend_path ? 1 : 0);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

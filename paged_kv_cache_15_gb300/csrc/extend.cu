@@ -319,19 +319,32 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         }
         if (stop) break;
       }
-      for (int e = 0; e < ukv.len(); ++e, ++jt) {
-        // e-th KV tile of the unit's sequence
-        int j;
-        if (ukv.dual) {
-          const int m = min(ukv.n0, ukv.n1);
-          const int step = e < 2 * m ? e >> 1 : e - m;
-          const int x = e < 2 * m ? (e & 1) : (ukv.n0 > ukv.n1 ? 0 : 1);
-          j = ukv.start(x) + step;
-        } else {
-          j = ukv.s0 + e;
+      // e-th KV tile of the unit's sequence
+      auto seq_tile = [&](int e) {
+        if (!ukv.dual) return ukv.s0 + e;
+        const int m = min(ukv.n0, ukv.n1);
+        const int step = e < 2 * m ? e >> 1 : e - m;
+        const int x = e < 2 * m ? (e & 1) : (ukv.n0 > ukv.n1 ? 0 : 1);
+        return ukv.start(x) + step;
+      };
+      // page indices of 4 consecutive tiles of the sequence: lane 8k + p holds
+      // page p of tile e0 + k; the next group is loaded while this one is used
+      const int len = ukv.len();
+      auto load_group = [&](int e0) {
+        const int e = e0 + (lane >> 3), p = lane & 7;
+        if (e >= len) return 0;
+        const int jj = seq_tile(e);
+        return p < np - jj * kPagesPerTile ? __ldg(a.m.kv_indices + page_base + jj * kPagesPerTile + p) : 0;
+      };
+      int grp = load_group(0);
+      int grp_next = load_group(4);
+      for (int e = 0; e < len; ++e, ++jt) {
+        if (e > 0 && (e & 3) == 0) {
+          grp = grp_next;
+          grp_next = load_group(e + 4);
         }
+        const int j = seq_tile(e);
         const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
-        const int my_pg = lane < npg ? __ldg(a.m.kv_indices + page_base + j * kPagesPerTile + lane) : 0;
         const int st = jt % depth;
         const uint32_t ph = (jt / depth) & 1;
         if (!mbar_wait_warp(&empty[st], ph ^ 1, plan, s_abort)) {
@@ -343,7 +356,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         uint8_t* dst = smem + ring_off + st * C::kTileBytes;
 #pragma unroll
         for (int p = 0; p < kPagesPerTile; ++p) {
-          const int pg = __shfl_sync(0xffffffffu, my_pg, p);
+          const int pg = __shfl_sync(0xffffffffu, grp, ((e & 3) << 3) + p);
           if (p < npg && leader) {
 #pragma unroll
             for (int cb = 0; cb < C::kColBlocks; ++cb)

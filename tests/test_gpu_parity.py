@@ -418,6 +418,19 @@ def test_extend_mixed_split_and_unsplit_requests():
     full_check(W)
 
 
+@pytest.mark.parametrize("mode", ["decode", "verify"])
+def test_merge_of_more_than_32_splits(mode):
+    """One 100k-token request alone in the batch: the plan cuts its KV range
+    into hundreds of splits, so the merge runs its path for more than 32
+    partials per row."""
+    if mode == "decode":
+        W = make_workload("m32d", "decode", 1, 8, 1, 128, [100000], [1])
+        full_check(W)
+    else:
+        W = make_workload("m32v", "verify", 1, 16, 1, 128, [100000], [5])
+        full_check(W, spec_mode=B.PKV_SPEC_PREFILL)
+
+
 def test_verify_prefill_path_long_context_split():
     W = make_workload("vlong", "verify", 4, 64, 4, 128, [20000, 300, 12000, 5000], [8, 4, 6, 7])
     full_check(W, spec_mode=B.PKV_SPEC_PREFILL)
