@@ -43,15 +43,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (profiles/), valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "6f5043deb3beb7af", "bytes_per_launch": 1386761472,
+    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "9a55b152f50ab670", "bytes_per_launch": 1386653696,
                                              "source": "profiles/decode_splitkv_llama3_8b_decode.md"},
-    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "6f5043deb3beb7af", "bytes_per_launch": 1471666176,
+    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "9a55b152f50ab670", "bytes_per_launch": 1471703808,
                                             "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("decode_splitkv", "spec_verify"): {"src_sha": "6f5043deb3beb7af", "bytes_per_launch": 601986304,
+    ("decode_splitkv", "spec_verify"): {"src_sha": "9a55b152f50ab670", "bytes_per_launch": 601844736,
                                         "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("extend_tc", "prefix_extend"): {"src_sha": "b873d5a3bcc2d58c", "bytes_per_launch": 855017984,
+    ("extend_tc", "prefix_extend"): {"src_sha": "e1b4d01b84b54807", "bytes_per_launch": 896172288,
                                      "source": "profiles/extend_tc_prefix_extend.md"},
-    ("extend_tc", "spec_verify"): {"src_sha": "b873d5a3bcc2d58c", "bytes_per_launch": 602822912,
+    ("extend_tc", "spec_verify"): {"src_sha": "e1b4d01b84b54807", "bytes_per_launch": 602501376,
                                    "source": "profiles/dram_traffic_fp8_and_verify.md"},
 }
 
