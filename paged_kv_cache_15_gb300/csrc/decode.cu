@@ -61,7 +61,8 @@ struct DecodeCfg {
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kMlOffset = kBarOffset + 2 * STAGES * 8;
   static constexpr int kAbortOffset = kMlOffset + WK * 16 * 2 * 4;
-  static constexpr int kSmemBytes = kAbortOffset + 16 + 1024;  // + alignment slack
+  static constexpr int kUnitQOffset = kAbortOffset + 16;  // unit queue: 2 full + 2 empty barriers, 2 ids
+  static constexpr int kSmemBytes = kUnitQOffset + 40 + 1024;  // + alignment slack
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
   static_assert(KPW % 16 == 0 && kStageKeys % kPageSize == 0, "stage must hold whole pages");
   static_assert(!(WK > 1) || (WK * 16 * D * 4 <= kStageBytes), "merge scratch must fit in one stage");
@@ -191,6 +192,11 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
   uint64_t* empty = full + C::STAGES;
   float* s_ml = reinterpret_cast<float*>(smem + C::kMlOffset);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kAbortOffset);
+  // queue of the units this CTA runs, filled by the producer: ids in s_uq,
+  // uq_full[q] (producer arrives), uq_empty[q] (one arrival per consumer warp)
+  uint64_t* uq_full = reinterpret_cast<uint64_t*>(smem + C::kUnitQOffset);
+  uint64_t* uq_empty = uq_full + 2;
+  volatile int* s_uq = reinterpret_cast<volatile int*>(uq_empty + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* plan = a.m.plan;
@@ -200,6 +206,10 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::kConsumerWarps);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&uq_full[q], 1);
+      mbar_init(&uq_empty[q], C::kConsumerWarps);
     }
     *s_abort = 0;
     fence_mbar_init();
@@ -225,7 +235,23 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
       int slot = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_phase = 0;
-      for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
+      // Units: blockIdx.x first, then whatever the batch-wide counter hands
+      // out as CTAs free up (units differ in length: the last split of a
+      // request is short). The next claim is made when a unit starts, and
+      // each id is published to the consumer warps through the queue.
+      int w = (int)blockIdx.x < n_units ? (int)blockIdx.x : -1;
+      bool stop = false;
+      for (int iu = 0; !stop; ++iu) {
+        const int q = iu & 1;
+        if (!mbar_wait_ab(&uq_empty[q], ((iu >> 1) & 1) ^ 1, plan, s_abort)) {
+          *s_abort = 1;
+          break;
+        }
+        s_uq[q] = w;
+        mbar_arrive(&uq_full[q]);
+        if (w < 0) break;
+        // (no claim when the first wave already covers every unit)
+        const int claimed = n_units > (int)gridDim.x ? (int)gridDim.x + atomicAdd(&plan[kDecodeNext], 1) : n_units;
         const DecodeItem it = a.m.decode_items[w / a.num_kv_heads];
         const int g = w % a.num_kv_heads;
         const int base = a.m.kv_indptr[it.b] + it.p0;
@@ -234,6 +260,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
         for (int st = 0; st < nst; ++st) {
           if (!mbar_wait_ab(&empty[slot], phase ^ 1, plan, s_abort)) {
             *s_abort = 1;
+            stop = true;
             break;
           }
           const int np = min(C::kStagePages, npages - st * C::kStagePages);
@@ -257,6 +284,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             phase ^= 1;
           }
         }
+        w = claimed < n_units ? claimed : -1;
       }
       for (int s = 0; s < C::STAGES; ++s)
         if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1, plan);
@@ -274,8 +302,19 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
   uint32_t phase = 0;
   bool aborted = false;
 
-  for (int w = blockIdx.x; w < n_units; w += gridDim.x) {
-    if (named_bar_or(1, C::kConsumerWarps * 32, *s_abort)) break;
+  for (int iu = 0;; ++iu) {
+    // next unit from the producer's queue; all consumer warps read the same id
+    // and leave together (the vote also ends the loop after an abort)
+    const int q = iu & 1;
+    int w = -1;
+    if (!aborted && !mbar_wait_ab(&uq_full[q], (iu >> 1) & 1, plan, s_abort)) {
+      *s_abort = 1;
+      aborted = true;
+    }
+    if (!aborted) w = s_uq[q];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&uq_empty[q]);
+    if (named_bar_or(1, C::kConsumerWarps * 32, *s_abort || w < 0)) break;
     const DecodeItem it = a.m.decode_items[w / a.num_kv_heads];
     const int g = w % a.num_kv_heads;
     const int b = it.b;
@@ -677,6 +716,8 @@ template <int D>
 __global__ void __launch_bounds__(256, 3) split_merge_kernel(DecodeArgs a, int max_rows_per_head, int count_word,
                                                           int extend_path) {
   pdl_wait();  // the partial rows come from the preceding attention grid
+  // the decode grid has finished: its unit counter starts from zero next time
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.m.plan[kDecodeNext] = 0;
   if (a.m.plan[count_word] == 0) return;  // nothing was split on this path
   const int rows = a.m.plan[kTotalQ] * a.num_q_heads;
   const int lane = threadIdx.x & 31;

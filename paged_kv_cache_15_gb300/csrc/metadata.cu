@@ -231,6 +231,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
       a.plan[kMaxQo] = 0;
       a.plan[kSplitDecode] = 0;
       a.plan[kSplitExtend] = 0;
+      a.plan[kDecodeNext] = 0;
     }
     return;
   }
@@ -377,6 +378,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
     a.plan[kMaxQo] = tot.maxqo;
     a.plan[kSplitDecode] = items_over ? 0 : all.splitd;
     a.plan[kSplitExtend] = items_over ? 0 : all.splite;
+    a.plan[kDecodeNext] = 0;
   }
 }
 

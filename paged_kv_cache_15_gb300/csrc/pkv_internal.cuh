@@ -43,6 +43,7 @@ enum PlanWord : int {
   kMaxQo = 9,          // max qo_len in the batch
   kSplitDecode = 10,   // requests with more than one split on the decode path
   kSplitExtend = 11,   // requests split along their KV range on the extend path
+  kDecodeNext = 12,    // decode units claimed past the first wave (zeroed after every decode)
   kPlanWords = 32
 };
 
