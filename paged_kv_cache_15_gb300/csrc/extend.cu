@@ -73,6 +73,14 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 
 constexpr uint32_t kNegInfBits = 0xff800000u;
 
+// 32-byte global store (sm_100+): a whole sector per lane, half the store
+// instructions of 16-byte vectors. The address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // Masks raw scores of keys past the row's limit (sets them to -inf).
 __device__ __forceinline__ void mask32(uint32_t* sr, int key_base, int limit) {
 #pragma unroll
@@ -178,6 +186,7 @@ struct ExtendArgs {
   float scale_log2;
   int q_tma;         // 1 when the group divides 128: a Q tile is one TMA box of 128/G tokens x G heads
   int q_box_tokens;  // 128 / group
+  int out_32B;       // out is 32-byte aligned: output rows are written with 32-byte stores
 };
 
 template <class C>
@@ -769,22 +778,26 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * wa);
         }
+        // the rows of a warp are scattered (one 256- or 128-byte row per lane),
+        // so each store instruction costs one transaction per lane: 32-byte
+        // stores halve their number (partial rows live in the 256-byte aligned
+        // workspace; out only when the caller's buffer is 32-byte aligned)
         if (valid) {
           if (split) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(a.m.partial_o + prow * D + c * 32 + i) =
-                  make_float4(__uint_as_float(o[i]), __uint_as_float(o[i + 1]), __uint_as_float(o[i + 2]),
-                              __uint_as_float(o[i + 3]));
+            for (int i = 0; i < 32; i += 8) st_global_32B(a.m.partial_o + prow * D + c * 32 + i, o + i);
           } else {
+            uint32_t v[16];
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[i + 0]), __uint_as_float(o[i + 1]));
-              v.y = pack_bf16(__uint_as_float(o[i + 2]), __uint_as_float(o[i + 3]));
-              v.z = pack_bf16(__uint_as_float(o[i + 4]), __uint_as_float(o[i + 5]));
-              v.w = pack_bf16(__uint_as_float(o[i + 6]), __uint_as_float(o[i + 7]));
-              *reinterpret_cast<uint4*>(a.out + orow * D + c * 32 + i) = v;
+            for (int i = 0; i < 16; ++i) v[i] = pack_bf16(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+            uint16_t* dst = a.out + orow * D + c * 32;
+            if (a.out_32B) {
+              st_global_32B(dst, v);
+              st_global_32B(dst + 16, v + 8);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(v[i], v[i + 1], v[i + 2], v[i + 3]);
             }
           }
         }
@@ -836,6 +849,7 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.num_kv_heads = c.cfg.num_kv_heads;
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
   a.scale_log2 = sm_scale * kLog2e;
+  a.out_32B = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
   // Q as [tokens][heads][head_dim]: a box of 64 elements x G heads x 128/G
   // tokens is one 128-row tile column block, rows ordered (token, head) like
   // the tile's rows. The token extent only bounds the map; the kernel loads a

@@ -418,6 +418,22 @@ def test_extend_mixed_split_and_unsplit_requests():
     full_check(W)
 
 
+def test_extend_output_buffer_only_16_byte_aligned():
+    """The API asks for 16-byte aligned buffers; the extend epilogue's 32-byte
+    stores are used only when the output is 32-byte aligned."""
+    W = make_workload("a16", "extend", 3, 8, 2, 128, [0, 37, 200], [130, 9, 61])
+    d = DeviceBatch(W)
+    big = torch.empty(d.out.numel() + 8, dtype=d.out.dtype, device=d.out.device)
+    d.out = big[8:].view_as(d.q)  # 16 bytes past a 256-byte aligned allocation
+    assert d.out.data_ptr() % 32 == 16
+    d.step()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    ref_o, ref_lse = oracle_reference(W)
+    check_close(d.out.double().cpu().numpy(), ref_o, "o")
+    check_close(d.lse.double().cpu().numpy(), ref_lse, "lse")
+
+
 @pytest.mark.parametrize("mode", ["decode", "verify"])
 def test_merge_of_more_than_32_splits(mode):
     """One 100k-token request alone in the batch: the plan cuts its KV range
