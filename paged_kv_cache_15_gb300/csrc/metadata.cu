@@ -190,6 +190,10 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   // the attention kernel launched next may start its prologue now; it waits
   // for this grid before reading any metadata
   pdl_launch_dependents();
+  // launched with programmatic serialization too: the lengths and page table
+  // (and the workspace the previous kernels read) only after the previous
+  // grid has finished
+  pdl_wait();
   // ---- 1. batch totals (identical in every CTA) ----
   Sums s{0, 0, 0, 0, 0, 0, 0, 0, 0};
   for (int b = threadIdx.x; b < a.bs; b += kThreads) {
@@ -416,8 +420,8 @@ int launch_build_metadata(Ctx& c, int batch, const int32_t* seq_lens, const int3
   a.max_items = c.lay.max_decode_items;
   a.max_tiles = c.lay.max_extend_tiles;
   int grid = batch < 1 ? 1 : (batch < kMaxCtas ? batch : kMaxCtas);
-  build_metadata_kernel<<<grid, kThreads, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return launch_pdl(build_metadata_kernel, dim3(grid), dim3(kThreads), 0, st, a) == cudaSuccess ? PKV_OK
+                                                                                      : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -40,6 +40,11 @@ __global__ void __launch_bounds__(kThreads) set_kv_kernel(void* __restrict__ k_p
                                                           const uint4* __restrict__ v_new, long long n_vec,
                                                           int vec_per_token, long long num_slots, float k_inv,
                                                           float v_inv, int* plan) {
+  // launched with programmatic serialization: the next kernel may start
+  // launching now, and this one touches memory only after the previous grid
+  // (which may have produced the new K/V or the slots) has finished
+  pdl_launch_dependents();
+  pdl_wait();
   for (long long u = (long long)blockIdx.x * kThreads + threadIdx.x; u < n_vec;
        u += (long long)gridDim.x * kThreads) {
     long long tok = u / vec_per_token;
@@ -74,13 +79,14 @@ int launch_set_kv_buffer(Ctx& c, void* k_pool, void* v_pool, const int32_t* loc,
   int grid = (int)(blocks < cap ? blocks : cap);
   long long num_slots = (long long)c.cfg.num_pages * c.cfg.page_size;
   int* plan = make_meta(c).plan;
+  cudaError_t e;
   if (c.cfg.kv_dtype == PKV_KV_FP8_E4M3)
-    set_kv_kernel<true><<<grid, kThreads, 0, st>>>(k_pool, v_pool, loc, (const uint4*)k, (const uint4*)v, n_vec,
-                                                   vec_per_token, num_slots, k_inv, v_inv, plan);
+    e = launch_pdl(set_kv_kernel<true>, dim3(grid), dim3(kThreads), 0, st, k_pool, v_pool, loc, (const uint4*)k,
+                   (const uint4*)v, n_vec, vec_per_token, num_slots, k_inv, v_inv, plan);
   else
-    set_kv_kernel<false><<<grid, kThreads, 0, st>>>(k_pool, v_pool, loc, (const uint4*)k, (const uint4*)v, n_vec,
-                                                    vec_per_token, num_slots, k_inv, v_inv, plan);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    e = launch_pdl(set_kv_kernel<false>, dim3(grid), dim3(kThreads), 0, st, k_pool, v_pool, loc, (const uint4*)k,
+                   (const uint4*)v, n_vec, vec_per_token, num_slots, k_inv, v_inv, plan);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv
