@@ -348,6 +348,19 @@ def test_extend_rows_exceeding_group_tiles():
     full_check(W)
 
 
+@pytest.mark.parametrize("case", ["d64_g8", "g3"])
+@pytest.mark.parametrize("spec", ["prefill", "decode"])
+def test_verify_other_shapes_both_paths(case, spec):
+    """Verify batches outside the preset's shape: head_dim 64 with a group of
+    8, and a group of 3 (Q tiles copied by the softmax warps, not by TMA),
+    both with contexts long enough to be split along KV."""
+    if case == "d64_g8":
+        W = make_workload("v64", "verify", 4, 16, 2, 64, [900, 3000, 40, 12000], [5, 8, 3, 6])
+    else:
+        W = make_workload("vg3", "verify", 3, 12, 4, 128, [7000, 150, 2600], [4, 7, 5])
+    full_check(W, spec_mode=B.PKV_SPEC_PREFILL if spec == "prefill" else B.PKV_SPEC_DECODE)
+
+
 @pytest.mark.parametrize("bs,len_scale", [(8, 0.1), (3, 0.02)])
 def test_verify_prefill_path_parity(bs, len_scale):
     W = preset("spec_verify", bs=bs, len_scale=len_scale)
