@@ -58,7 +58,7 @@ extern "C" {
 /* ---- status codes ------------------------------------------------------- */
 #define PKV_OK 0
 #define PKV_ERR_INVALID_ARG 1 /* null pointer, negative size, bad enum, misaligned pointer */
-#define PKV_ERR_UNSUPPORTED 2 /* shape or feature this build does not implement */
+#define PKV_ERR_UNSUPPORTED 2 /* shape or feature the library does not implement */
 #define PKV_ERR_CAPACITY 3    /* batch or workspace larger than the configured capacity */
 #define PKV_ERR_CUDA 4        /* a CUDA runtime / driver call failed */
 #define PKV_ERR_DEVICE 5      /* the device recorded a data error (see pkv_get_device_error) */

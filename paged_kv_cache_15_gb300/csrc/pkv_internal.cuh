@@ -16,7 +16,7 @@ namespace pkv {
 // ---------------------------------------------------------------------------
 // Fixed tiling constants
 // ---------------------------------------------------------------------------
-constexpr int kPageSize = 16;           // the only page size this build accepts
+constexpr int kPageSize = 16;           // the only page size the library accepts
 constexpr int kDecodeTargetWaves = 4;   // split-KV aims at this many work units per CTA slot
 constexpr int kDecodeMinChunkPages = 8; // never cut a (request, head) range finer than 128 keys
 constexpr int kExtendRows = 128;        // query rows (token x head-in-group) per extend tile
