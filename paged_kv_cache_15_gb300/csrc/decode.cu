@@ -107,24 +107,25 @@ constexpr int kMergeBatch = 8;
 
 template <int D>
 struct MergeVec;
+// partial rows are bf16: 4 (D = 128) or 2 (D = 64) elements per lane
 template <>
 struct MergeVec<128> {
-  using T = float4;
-  __device__ static T load(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+  using T = uint2;
+  __device__ static T load(const uint16_t* p) { return __ldcg(reinterpret_cast<const uint2*>(p)); }
   __device__ static void fma(float* acc, float w, const T& x) {
-    acc[0] += w * x.x;
-    acc[1] += w * x.y;
-    acc[2] += w * x.z;
-    acc[3] += w * x.w;
+    acc[0] += w * bf16lo(x.x);
+    acc[1] += w * bf16hi(x.x);
+    acc[2] += w * bf16lo(x.y);
+    acc[3] += w * bf16hi(x.y);
   }
 };
 template <>
 struct MergeVec<64> {
-  using T = float2;
-  __device__ static T load(const float* p) { return __ldcg(reinterpret_cast<const float2*>(p)); }
+  using T = uint32_t;
+  __device__ static T load(const uint16_t* p) { return __ldcg(reinterpret_cast<const unsigned int*>(p)); }
   __device__ static void fma(float* acc, float w, const T& x) {
-    acc[0] += w * x.x;
-    acc[1] += w * x.y;
+    acc[0] += w * bf16lo(x);
+    acc[1] += w * bf16hi(x);
   }
 };
 
@@ -555,18 +556,18 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
 
     const bool direct = nsplit == 1;
     const int split = it.split;
-    auto out_row = [&](int r, float*& prow, uint16_t*& orow, float*& lrow) {
+    // destination row of row r: the output, or (split units) a bf16 partial
+    // row of the same layout plus its LSE
+    auto out_row = [&](int r, uint16_t*& orow, float*& lrow) {
       const int i = r / G, h = g * G + r % G;
       const long long t = q0 + i;
       if (direct) {
         orow = a.out + (t * a.num_q_heads + h) * D;
         lrow = a.lse ? a.lse + t * a.num_q_heads + h : nullptr;
-        prow = nullptr;
       } else {
         const long long pr = (long long)a.m.partial_indptr[b] + (long long)split * qo + i;
-        prow = a.m.partial_o + (pr * a.num_q_heads + h) * D;
+        orow = a.m.partial_o + (pr * a.num_q_heads + h) * D;
         lrow = a.m.partial_lse + pr * a.num_q_heads + h;
-        orow = nullptr;
       }
     };
 
@@ -578,27 +579,21 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           const bool v = half ? vb : va;
           const float m = half ? m_b : m_a, l = half ? l_b : l_a;
           if (!v) continue;
-          float* prow;
           uint16_t* orow;
           float* lrow;
-          out_row(r, prow, orow, lrow);
+          out_row(r, orow, lrow);
           const float inv = l > 0.f ? a.v_scale / l : 0.f;
           const float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll
           for (int nt = 0; nt < C::kNT; ++nt) {
             const float x0 = o[nt][2 * half] * inv, x1 = o[nt][2 * half + 1] * inv;
             const int c0 = ocol<C::FP8>(nt, qd, 0), c1 = ocol<C::FP8>(nt, qd, 1);
-            if (orow) {
-              if constexpr (!C::FP8) {
-                *reinterpret_cast<uint32_t*>(orow + c0) = pack_bf16(x0, x1);
-              } else {
-                uint32_t pk = pack_bf16(x0, x1);
-                orow[c0] = (uint16_t)(pk & 0xffff);
-                orow[c1] = (uint16_t)(pk >> 16);
-              }
+            if constexpr (!C::FP8) {
+              *reinterpret_cast<uint32_t*>(orow + c0) = pack_bf16(x0, x1);
             } else {
-              prow[c0] = x0;
-              prow[c1] = x1;
+              uint32_t pk = pack_bf16(x0, x1);
+              orow[c0] = (uint16_t)(pk & 0xffff);
+              orow[c1] = (uint16_t)(pk >> 16);
             }
           }
           if (qd == 0 && lrow) *lrow = lse;
@@ -612,14 +607,10 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           for (int half = 0; half < 2; ++half) {
             const int r = half ? rb : ra;
             if (!(half ? vb : va) || skip) continue;
-            float* prow;
             uint16_t* orow;
             float* lrow;
-            out_row(r, prow, orow, lrow);
-            for (int c = qd; c < D; c += 4) {
-              if (orow) orow[c] = 0;
-              else prow[c] = 0.f;
-            }
+            out_row(r, orow, lrow);
+            for (int c = qd; c < D; c += 4) orow[c] = 0;
             if (qd == 0 && lrow) *lrow = -INFINITY;
           }
         }
@@ -678,15 +669,10 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           acc.y *= inv;
           acc.z *= inv;
           acc.w *= inv;
-          float* prow;
           uint16_t* orow;
           float* lrow;
-          out_row(r, prow, orow, lrow);
-          if (orow) {
-            *reinterpret_cast<uint2*>(orow + c4 * 4) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
-          } else {
-            *reinterpret_cast<float4*>(prow + c4 * 4) = acc;
-          }
+          out_row(r, orow, lrow);
+          *reinterpret_cast<uint2*>(orow + c4 * 4) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
           if (c4 == 0 && lrow) *lrow = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
         }
         fence_proxy_async_smem();

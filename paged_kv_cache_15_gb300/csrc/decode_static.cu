@@ -21,7 +21,7 @@ namespace pkv {
 namespace {
 
 // Scratch for one call: plan words, per-request metadata, the split-KV work
-// list and the fp32 partial outputs. Shared by every call on a device.
+// list and the partial outputs. Shared by every call on a device.
 static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;

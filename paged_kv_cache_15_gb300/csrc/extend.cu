@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       const int tok = min(R / G, qo - 1);
       const int limit = L - qo + tok;
       const long long orow = (long long)(q0 + R / G) * a.num_q_heads + g * G + R % G;
-      // split units write fp32 partial rows (normalised output and LSE) that
+      // split units write bf16 partial rows (normalised output) and fp32 LSE that
       // the merge kernel combines across the request's splits
       const long long prow =
           split ? ((long long)a.m.partial_indptr[b] + (long long)u.split * qo + R / G) * a.num_q_heads + g * G + R % G
@@ -567,8 +567,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           }
         } else if (valid) {
           if (split) {
-            for (int c = 0; c < D; c += 4)
-              *reinterpret_cast<float4*>(a.m.partial_o + prow * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = 0; c < D; c += 8)
+              *reinterpret_cast<uint4*>(a.m.partial_o + prow * D + c) = make_uint4(0, 0, 0, 0);
             a.m.partial_lse[prow] = -INFINITY;
           } else {
             for (int c = 0; c < D; c += 8)
@@ -783,15 +783,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         // stores halve their number (partial rows live in the 256-byte aligned
         // workspace; out only when the caller's buffer is 32-byte aligned)
         if (valid) {
-          if (split) {
+          // the output row, or (split units) a bf16 partial row of the same layout
+          uint32_t v[16];
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) st_global_32B(a.m.partial_o + prow * D + c * 32 + i, o + i);
-          } else {
-            uint32_t v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = pack_bf16(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
-            uint16_t* dst = a.out + orow * D + c * 32;
-            if (a.out_32B) {
+          for (int i = 0; i < 16; ++i) v[i] = pack_bf16(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+          {
+            uint16_t* dst = split ? a.m.partial_o + prow * D + c * 32 : a.out + orow * D + c * 32;
+            if (split || a.out_32B) {
               st_global_32B(dst, v);
               st_global_32B(dst + 16, v + 8);
             } else {

@@ -93,7 +93,7 @@ Layout make_layout(const pkv_config& cfg, int num_sms) {
   L.token_req = take(sizeof(int) * (size_t)cfg.max_q_tokens);
   L.decode_items = take(sizeof(DecodeItem) * (size_t)L.max_decode_items);
   L.extend_tiles = take(sizeof(ExtendTile) * (size_t)L.max_extend_tiles);
-  L.partial_o = take(sizeof(float) * (size_t)cap * cfg.num_q_heads * cfg.head_dim);
+  L.partial_o = take(sizeof(uint16_t) * (size_t)cap * cfg.num_q_heads * cfg.head_dim);
   L.partial_lse = take(sizeof(float) * (size_t)cap * cfg.num_q_heads);
   L.total = off;
   return L;
@@ -151,7 +151,7 @@ Meta make_meta(const Ctx& c) {
   m.token_req = reinterpret_cast<const int*>(w + c.lay.token_req);
   m.decode_items = reinterpret_cast<const DecodeItem*>(w + c.lay.decode_items);
   m.extend_tiles = reinterpret_cast<const ExtendTile*>(w + c.lay.extend_tiles);
-  m.partial_o = reinterpret_cast<float*>(w + c.lay.partial_o);
+  m.partial_o = reinterpret_cast<uint16_t*>(w + c.lay.partial_o);
   m.partial_lse = reinterpret_cast<float*>(w + c.lay.partial_lse);
   return m;
 }

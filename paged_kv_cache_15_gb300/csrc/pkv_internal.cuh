@@ -98,7 +98,7 @@ struct Meta {
   const int* token_req;
   const DecodeItem* decode_items;
   const ExtendTile* extend_tiles;
-  float* partial_o;
+  uint16_t* partial_o;  // bf16 [rows][Hq][D]: normalised partial outputs of split units
   float* partial_lse;
 };
 
