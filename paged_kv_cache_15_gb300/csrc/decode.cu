@@ -752,7 +752,6 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
       cudaSuccess)
     return PKV_ERR_CUDA;
   return launch_split_merge(c, out, lse, c.cfg.max_qo_len * a.group, false, st);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 // Tile shapes: decode packs one 16-row tile per unit and splits each stage's
@@ -784,10 +783,7 @@ int decode_row_warps(const pkv_config& cfg) {
 }
 
 int decode_stage_pages(const pkv_config& cfg) {
-  const int wr = decode_row_warps(cfg);
-  const bool fp8 = cfg.kv_dtype == PKV_KV_FP8_E4M3;
-  if (wr == 1) return fp8 ? 8 : 4;
-  return fp8 ? 8 : 4;
+  return cfg.kv_dtype == PKV_KV_FP8_E4M3 ? 8 : 4;
 }
 
 int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,

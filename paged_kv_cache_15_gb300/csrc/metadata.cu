@@ -15,7 +15,9 @@
 //     partial-output buffer cannot overflow;
 //   extend path: (request, first query row) units of 256 rows (two 128-row
 //     tiles), where a row is (token, head-in-group), with the number of
-//     128-key KV tiles each tile reaches.
+//     128-key KV tiles each tile reaches; a request whose rows fit one unit
+//     and whose decode plan splits it is cut along its KV range into equal
+//     splits instead, the split size priced against the extend grid.
 //
 // Work split: CTA j owns a contiguous range of requests. Every CTA first
 // reduces the batch totals (they fix chunk_pages and the capacity checks) and
@@ -42,7 +44,9 @@ struct ReqInfo {
 
 struct Sums {
   long long np, qo, ns, pr, qt, npqo;
+  long long et;  // KV tiles of the requests whose rows fit one extend unit
   int maxqo, splitd, splite;
+  int maxnp;  // pages of the longest request
 };
 
 struct MetaArgs {
@@ -67,7 +71,8 @@ struct MetaArgs {
   int group;  // num_q_heads / num_kv_heads
   int num_kv_heads;
   int stage_pages;  // the decode kernel's pages per pipeline stage
-  int units_target;
+  int units_target;      // decode work units to aim for
+  int ext_grid;          // CTAs of the extend kernel (units are dealt to them by a fixed stride)
   int partial_cap;
   int max_pages_total;
   int max_q_tokens;
@@ -85,19 +90,35 @@ __device__ __forceinline__ void raw_lengths(const MetaArgs& a, int b, int& L, in
   }
 }
 
-__device__ __forceinline__ ReqInfo req_info(const MetaArgs& a, int b, int chunk) {
+// Requests whose validated lengths the first pass keeps in shared memory;
+// every later pass reads them from there (the rest from global memory).
+constexpr int kLenCache = 2048;
+__shared__ int2 s_len_cache[kLenCache];  // {L, qo | bad << 31}
+
+__device__ __forceinline__ void lengths(const MetaArgs& a, int b, int& L, int& qo, bool& bad) {
+  if (b < kLenCache) {
+    const int2 v = s_len_cache[b];
+    L = v.x;
+    qo = v.y & 0x7fffffff;
+    bad = v.y < 0;
+  } else {
+    raw_lengths(a, b, L, qo, bad);
+  }
+}
+
+__device__ __forceinline__ int kv_tiles_of(int np) { return (np + kPagesPerKvTile - 1) / kPagesPerKvTile; }
+
+__device__ __forceinline__ ReqInfo req_info(const MetaArgs& a, int b, int chunk, int ext_ct) {
   ReqInfo r;
-  raw_lengths(a, b, r.L, r.qo, r.bad);
+  lengths(a, b, r.L, r.qo, r.bad);
   r.np = (r.L + kPageSize - 1) / kPageSize;
   r.nsplit = r.np > 0 ? (r.np + chunk - 1) / chunk : 1;
   r.prow = r.nsplit > 1 ? r.nsplit * r.qo : 0;
   r.qtiles = (r.qo * a.group + kExtendUnitRows - 1) / kExtendUnitRows;
-  // rows that fit one extend unit: cut the KV range into chunks of whole
-  // 128-key tiles, at least as long as the decode chunks (so the split count
-  // never exceeds the decode plan's and its partial rows fit)
-  const int ct = (chunk + kPagesPerKvTile - 1) / kPagesPerKvTile;  // KV tiles per extend split
-  const int ntiles = (r.np + kPagesPerKvTile - 1) / kPagesPerKvTile;
-  r.esplit = (r.qtiles == 1 && r.nsplit > 1) ? (ntiles + ct - 1) / ct : 1;
+  // rows that fit one extend unit: cut the KV range into equal splits of at
+  // most ext_ct 128-key tiles; ext_ct spans at least one decode chunk, so the
+  // split count never exceeds the decode plan's and its partial rows fit
+  r.esplit = (r.qtiles == 1 && r.nsplit > 1) ? (kv_tiles_of(r.np) + ext_ct - 1) / ext_ct : 1;
   if (r.esplit > 1) r.qtiles = r.esplit;
   return r;
 }
@@ -115,8 +136,8 @@ __device__ __forceinline__ int warp_max(int v) {
 
 // Block-wide sum of a Sums record (result valid in every thread).
 __device__ Sums block_sum(Sums s) {
-  __shared__ long long red[6][kThreads / 32];
-  __shared__ int redm[kThreads / 32], redd[kThreads / 32], rede[kThreads / 32];
+  __shared__ long long red[7][kThreads / 32];
+  __shared__ int redm[kThreads / 32], redd[kThreads / 32], rede[kThreads / 32], redp[kThreads / 32];
   int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   s.np = warp_sum(s.np);
   s.qo = warp_sum(s.qo);
@@ -124,7 +145,9 @@ __device__ Sums block_sum(Sums s) {
   s.pr = warp_sum(s.pr);
   s.qt = warp_sum(s.qt);
   s.npqo = warp_sum(s.npqo);
+  s.et = warp_sum(s.et);
   s.maxqo = warp_max(s.maxqo);
+  s.maxnp = warp_max(s.maxnp);
   s.splitd = warp_sum(s.splitd);
   s.splite = warp_sum(s.splite);
   __syncthreads();
@@ -135,7 +158,9 @@ __device__ Sums block_sum(Sums s) {
     red[3][w] = s.pr;
     red[4][w] = s.qt;
     red[5][w] = s.npqo;
+    red[6][w] = s.et;
     redm[w] = s.maxqo;
+    redp[w] = s.maxnp;
     redd[w] = s.splitd;
     rede[w] = s.splite;
   }
@@ -150,9 +175,75 @@ __device__ Sums block_sum(Sums s) {
     t.pr += red[3][i];
     t.qt += red[4][i];
     t.npqo += red[5][i];
+    t.et += red[6][i];
     t.maxqo = max(t.maxqo, redm[i]);
+    t.maxnp = max(t.maxnp, redp[i]);
   }
   return t;
+}
+
+// Tiles per extend KV split. The extend kernel deals its units to CTAs by a
+// fixed stride, so a step lasts about as long as its busiest CTA:
+// ceil(units / grid) units of up to ct tiles, each with a fixed cost (Q load,
+// the in-CTA merge, output stores) of about two tiles. Candidates start where
+// about eight units fall to each CTA (finer splits only add fixed costs),
+// never below one decode chunk; the cheapest wins, ties going to the larger
+// split. Thread t prices candidate t % 64 over every fourth request. A batch
+// of single-row requests (decode) keeps the smallest candidate without
+// pricing: the decode path does not read these splits. Called by every thread
+// of the block; identical in every CTA.
+constexpr int kExtCandidates = 64;
+constexpr int kExtUnitCostTiles = 2;
+constexpr int kExtMaxUnitsPerCta = 8;
+constexpr int kExtGroups = kThreads / kExtCandidates;
+static_assert(kThreads % kExtCandidates == 0 && kExtCandidates == 64, "two warps of candidates");
+
+__device__ int extend_split_tiles(const MetaArgs& a, int chunk, const Sums& tot) {
+  __shared__ int s_units[kExtGroups][kExtCandidates];
+  __shared__ unsigned long long s_key[2];
+  const int ct_min = kv_tiles_of(chunk);
+  const long long grid = a.ext_grid > 0 ? a.ext_grid : 1;
+  // tot.et counts the tiles of every request whose rows fit one unit, a bound
+  // on those that get split
+  const long long per = (long long)kExtMaxUnitsPerCta * grid;
+  long long lo = (tot.et * a.num_kv_heads + per - 1) / per;
+  if (lo < ct_min) lo = ct_min;
+  if (lo > (1 << 24)) lo = 1 << 24;
+  const int ct_lo = (int)lo;
+  if (tot.maxqo <= 1 || tot.et == 0) return ct_lo;
+  const int c = threadIdx.x % kExtCandidates, grp = threadIdx.x / kExtCandidates;
+  const int ct = ct_lo + c;
+  int split_units = 0, fixed_units = 0;
+  for (int b = grp; b < a.bs; b += kExtGroups) {
+    int L, qo;
+    bool bad;
+    lengths(a, b, L, qo, bad);
+    const int np = (L + kPageSize - 1) / kPageSize;
+    const int qt = (qo * a.group + kExtendUnitRows - 1) / kExtendUnitRows;
+    if (qt == 1 && np > chunk)
+      split_units += (kv_tiles_of(np) + ct - 1) / ct;
+    else
+      fixed_units += qt;
+  }
+  s_units[grp][c] = split_units + fixed_units;
+  __syncthreads();
+  if (threadIdx.x < kExtCandidates) {
+    int u = 0;
+#pragma unroll
+    for (int g = 0; g < kExtGroups; ++g) u += s_units[g][c];
+    const long long units = (long long)u * a.num_kv_heads;
+    const unsigned long long cost = (unsigned long long)((units + grid - 1) / grid) * (ct + kExtUnitCostTiles);
+    // cheapest, ties to the larger split: minimum of cost * 64 + (63 - c)
+    unsigned long long key = cost * kExtCandidates + (kExtCandidates - 1 - c);
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, key, o);
+      if (y < key) key = y;
+    }
+    if ((threadIdx.x & 31) == 0) s_key[threadIdx.x >> 5] = key;
+  }
+  __syncthreads();
+  const unsigned long long best = s_key[0] < s_key[1] ? s_key[0] : s_key[1];
+  return ct_lo + (kExtCandidates - 1 - (int)(best % kExtCandidates));
 }
 
 // Exclusive block scan of five ints; returns this thread's prefix and the tile total.
@@ -200,11 +291,14 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
     int L, qo;
     bool bad;
     raw_lengths(a, b, L, qo, bad);
+    if (b < kLenCache) s_len_cache[b] = make_int2(L, bad ? (int)((unsigned)qo | 0x80000000u) : qo);
     long long np = (L + kPageSize - 1) / kPageSize;
     s.np += np;
     s.qo += qo;
     s.npqo += np * qo;
     s.maxqo = max(s.maxqo, qo);
+    s.maxnp = max(s.maxnp, (int)np);
+    if (qo > 0 && (long long)qo * a.group <= kExtendUnitRows) s.et += kv_tiles_of((int)np);
   }
   Sums tot = block_sum(s);
   bool over = tot.np > a.max_pages_total || tot.qo > a.max_q_tokens || tot.qo >= a.partial_cap;
@@ -213,6 +307,9 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   // keep sum over split requests of nsplit*qo below the partial buffer
   long long chunk = (tot.np * a.num_kv_heads + a.units_target - 1) / a.units_target;
   if (chunk < kDecodeMinChunkPages) chunk = kDecodeMinChunkPages;
+  // at most kMaxSplitsPerRequest splits of any request (the merge reads them one per lane)
+  const long long cmax = (tot.maxnp + kMaxSplitsPerRequest - 1) / kMaxSplitsPerRequest;
+  if (chunk < cmax) chunk = cmax;
   long long room = (long long)a.partial_cap - tot.qo;
   if (room > 0) {
     long long c2 = (tot.npqo + room - 1) / room;
@@ -221,6 +318,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   chunk = (chunk + a.stage_pages - 1) / a.stage_pages * a.stage_pages;
   if (chunk > (1 << 30)) chunk = 1 << 30;
   int ichunk = (int)chunk;
+  const int ext_ct = extend_split_tiles(a, ichunk, tot);
 
   if (over) {
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -245,7 +343,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   int b0 = min(a.bs, (int)blockIdx.x * per), b1 = min(a.bs, b0 + per);
   Sums pre{0, 0, 0, 0, 0, 0, 0, 0, 0};
   for (int b = threadIdx.x; b < b0; b += kThreads) {
-    ReqInfo r = req_info(a, b, ichunk);
+    ReqInfo r = req_info(a, b, ichunk, ext_ct);
     pre.np += r.np;
     pre.qo += r.qo;
     pre.ns += r.nsplit;
@@ -257,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   Sums all{0, 0, 0, 0, 0, 0, 0, 0, 0};
   if (blockIdx.x == 0) {
     for (int b = threadIdx.x; b < a.bs; b += kThreads) {
-      ReqInfo r = req_info(a, b, ichunk);
+      ReqInfo r = req_info(a, b, ichunk, ext_ct);
       all.ns += r.nsplit;
       all.pr += r.prow;
       all.qt += r.qtiles;
@@ -275,7 +373,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
     const int b = t0 + threadIdx.x;
     ReqInfo r{0, 0, 0, 0, 1, 0, 0, false};
     const bool live = b < b1;
-    if (live) r = req_info(a, b, ichunk);
+    if (live) r = req_info(a, b, ichunk, ext_ct);
     Scan5 x{{r.np, r.qo, r.nsplit, r.prow, r.qtiles}};
     if (!live) x = Scan5{{0, 0, 0, 0, 0}};
     Scan5 tile_tot;
@@ -340,7 +438,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
         return L > 0 ? (L - qo + last_tok + 1 + kExtendKeys - 1) / kExtendKeys : 0;
       };
       const bool split = inf[kEs] > 1;
-      const int chunk_tiles = (ichunk + kPagesPerKvTile - 1) / kPagesPerKvTile;
+      const int es = inf[kEs], ntiles = kv_tiles_of(np);
       for (int t = threadIdx.x; t < qt; t += kThreads) {
         if (tbase + t < a.max_tiles) {
           const int row0 = split ? 0 : t * kExtendUnitRows;
@@ -350,8 +448,9 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
           et.kv_a = kv_tiles_to(min(row0 + kExtendRows, rows));
           et.kv_b = row0 + kExtendRows < rows ? kv_tiles_to(min(row0 + kExtendUnitRows, rows)) : 0;
           et.split = split ? t : -1;
-          et.kv0 = split ? t * chunk_tiles : 0;
-          et.kv1 = split ? (t + 1) * chunk_tiles : 0x7fffffff;
+          // split t takes an equal share of the request's KV tiles
+          et.kv0 = split ? (int)((long long)t * ntiles / es) : 0;
+          et.kv1 = split ? (int)((long long)(t + 1) * ntiles / es) : 0x7fffffff;
           // rows that fit one 128-row tile: both tiles hold them, each takes
           // half of the unit's KV range, and the halves are merged in the CTA
           et.dual = rows <= kExtendRows ? 1 : 0;
@@ -412,8 +511,9 @@ int launch_build_metadata(Ctx& c, int batch, const int32_t* seq_lens, const int3
   a.num_pages = c.cfg.num_pages;
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
   a.num_kv_heads = c.cfg.num_kv_heads;
-  a.stage_pages = c.cfg.kv_dtype == PKV_KV_FP8_E4M3 ? 8 : 4;
-  a.units_target = c.decode_ctas * kDecodeTargetWaves;
+  a.stage_pages = decode_stage_pages(c.cfg);
+  a.units_target = c.decode_ctas * (decode_row_warps(c.cfg) == 1 ? kDecodeTargetWaves : kVerifyTargetWaves);
+  a.ext_grid = c.extend_ctas;
   a.partial_cap = c.lay.partial_rows_cap;
   a.max_pages_total = c.cfg.max_pages_total;
   a.max_q_tokens = c.cfg.max_q_tokens;

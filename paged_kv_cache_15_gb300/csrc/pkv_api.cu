@@ -10,9 +10,6 @@
 
 namespace pkv {
 
-int decode_row_warps(const pkv_config& cfg);
-int decode_stage_pages(const pkv_config& cfg);
-
 namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -17,7 +17,14 @@ namespace pkv {
 // Fixed tiling constants
 // ---------------------------------------------------------------------------
 constexpr int kPageSize = 16;           // the only page size the library accepts
-constexpr int kDecodeTargetWaves = 4;   // split-KV aims at this many work units per CTA slot
+// split-KV aims at this many work units per CTA slot: 16-row decode units
+// are light and balance best when fine; the verify shapes' units carry up to
+// 128 rows each and pay more per unit
+constexpr int kDecodeTargetWaves = 8;
+constexpr int kVerifyTargetWaves = 4;
+// decode splits of one request at most: the merge reads one per lane (so at
+// most 32), and on long requests fewer, longer splits stream faster
+constexpr int kMaxSplitsPerRequest = 24;
 constexpr int kDecodeMinChunkPages = 8; // never cut a (request, head) range finer than 128 keys
 constexpr int kExtendRows = 128;        // query rows (token x head-in-group) per extend tile
 constexpr int kExtendUnitRows = 256;    // an extend work unit holds two tiles (A, B) sharing K/V
@@ -117,6 +124,10 @@ int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool,
 // max_rows_per_head (the decode path: its largest tile; the extend path: 256,
 // the requests it split).
 int launch_split_merge(Ctx& c, void* out, float* lse, int max_rows_per_head, bool extend_path, cudaStream_t st);
+// decode-path tile shape of a configuration: warps of 16 rows per unit (0 if
+// max_qo_len * group exceeds 128) and K/V pages per pipeline stage
+int decode_row_warps(const pkv_config& cfg);
+int decode_stage_pages(const pkv_config& cfg);
 
 // Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
 int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t outer,
