@@ -43,15 +43,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (profiles/), valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "9a55b152f50ab670", "bytes_per_launch": 1386653696,
+    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "7978a7b619b91bfc", "bytes_per_launch": 1386582528,
                                              "source": "profiles/decode_splitkv_llama3_8b_decode.md"},
-    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "9a55b152f50ab670", "bytes_per_launch": 1471703808,
+    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "7978a7b619b91bfc", "bytes_per_launch": 1509188864,
                                             "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("decode_splitkv", "spec_verify"): {"src_sha": "9a55b152f50ab670", "bytes_per_launch": 601844736,
+    ("decode_splitkv", "spec_verify"): {"src_sha": "7978a7b619b91bfc", "bytes_per_launch": 601608704,
                                         "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("extend_tc", "prefix_extend"): {"src_sha": "e1b4d01b84b54807", "bytes_per_launch": 896172288,
+    ("extend_tc", "prefix_extend"): {"src_sha": "fd7d32f9906cdca2", "bytes_per_launch": 1050398464,
                                      "source": "profiles/extend_tc_prefix_extend.md"},
-    ("extend_tc", "spec_verify"): {"src_sha": "e1b4d01b84b54807", "bytes_per_launch": 602501376,
+    ("extend_tc", "spec_verify"): {"src_sha": "fd7d32f9906cdca2", "bytes_per_launch": 599987712,
                                    "source": "profiles/dram_traffic_fp8_and_verify.md"},
 }
 
