@@ -5,20 +5,27 @@
 //
 // Split-KV flash decoding:
 //   * The metadata build cut every (request, KV head) key range into chunks of
-//     chunk_pages pages; one work unit = (request, split, KV head). A persistent
-//     grid walks the units with a grid stride.
+//     chunk_pages pages; one work unit = (request, split, KV head). CTA j of the
+//     persistent grid starts on unit j and claims further units from a
+//     batch-wide counter as it frees up.
 //   * GQA packing: the group's query heads (times the request's query tokens on
-//     the verify path) form the rows of one 16-row MMA tile per row-warp, so every
-//     K/V byte fetched from HBM is used by all heads of its group.
+//     the verify path) are the query rows of one MMA tile, so every K/V byte
+//     fetched from HBM is used by all heads of its group.
 //   * A producer warp gathers pages with TMA (one 2-D box of 16 token rows x 128
 //     bytes per page, 128-byte swizzle) into a ring of shared-memory stages; the
-//     consumer warps wait on the stage's mbarrier, compute S = Q K^T and O += P V
+//     consumer warps wait on the stage's mbarrier, compute scores and outputs
 //     with m16n8k16 tensor-core MMAs, and keep an online softmax per row
 //     (running max m, running sum l) in registers, in the log2 domain.
+//   * Decode shapes (at most 16 query rows per unit) use key-major tiles:
+//     S^T = K Q^T with 16 keys along the MMA's M and the rows along N in one or
+//     two 8-row tiles, then O^T += V^T P^T, P^T reaching the B operand through
+//     an in-register 8x8 transpose (movmatrix). Four key warps split each
+//     stage's keys and combine through shared memory. The verify shapes (up to
+//     128 rows) use query-major 16-row tiles, one per row warp.
 //   * Each unit ends with its normalised output and LSE. A request with one split
-//     writes the final bf16 output directly; otherwise the unit writes an fp32
-//     partial row, and a small merge kernel (one CTA per split (request, KV
-//     head) group) combines them:
+//     writes the final bf16 output directly; otherwise the unit writes a bf16
+//     partial row and an fp32 LSE, and the merge kernel (one warp per
+//     (token, query head) row) combines them:
 //        lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s.
 //   * FP8 E4M3 pools: codes are widened to f16 in registers (cvt e4m3x2 -> f16x2,
 //     exact), the MMAs run in f16 (Q and P rounded to f16), and the per-pool
@@ -38,10 +45,13 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D_, bool FP8_, int WR_, int WK_, int KPW_, int STAGES_>
+template <int D_, bool FP8_, int WR_, int WK_, int KPW_, int STAGES_, int RT_ = 0>
 struct DecodeCfg {
   static constexpr int D = D_;
   static constexpr bool FP8 = FP8_;
+  // RT > 0: key-major tile (keys along the MMA's M, RT tiles of 8 query rows
+  // along N), one row warp; RT == 0: query-major tile, WR row warps
+  static constexpr int RT = RT_;
   static constexpr int WR = WR_;  // row warps (16 rows each)
   static constexpr int WK = WK_;  // key warps (split each stage's keys)
   static constexpr int KPW = KPW_;  // keys per key-warp per stage (multiple of 16)
@@ -49,7 +59,7 @@ struct DecodeCfg {
   static constexpr int kConsumerWarps = WR * WK;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
   static constexpr int kMinBlocks = kThreads <= 160 ? 2 : 1;  // two CTAs per SM hide latency for the decode shapes
-  static constexpr int kRows = 16 * WR;
+  static constexpr int kRows = RT > 0 ? 8 * RT : 16 * WR;
   static constexpr int kStageKeys = WK * KPW;
   static constexpr int kStagePages = kStageKeys / kPageSize;
   static constexpr int kElem = FP8 ? 1 : 2;
@@ -66,6 +76,8 @@ struct DecodeCfg {
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
   static_assert(KPW % 16 == 0 && kStageKeys % kPageSize == 0, "stage must hold whole pages");
   static_assert(!(WK > 1) || (WK * 16 * D * 4 <= kStageBytes), "merge scratch must fit in one stage");
+  static_assert(RT == 0 || (WR == 1 && WK > 1 && RT <= 2), "key-major tiles: one row warp, key warps combined");
+  static_assert(RT > 0 || WK == 1, "query-major tiles: each warp holds all keys of a stage");
 };
 
 struct DecodeArgs {
@@ -141,16 +153,12 @@ __device__ __forceinline__ void merge_row(const DecodeArgs& a, long long pbase, 
 #pragma unroll
   for (int sp = 0; sp < kMergeBatch; ++sp)
     if (sp < nsplit) x[sp] = part(sp);
+  static_assert(kMaxSplitsPerRequest <= 32, "one split per lane");
   const float l0 = lane < nsplit ? lse_of(lane) : -INFINITY;
   float M = l0;
-  for (int s0 = 32; s0 < nsplit; s0 += 32)
-    if (s0 + lane < nsplit) M = fmaxf(M, lse_of(s0 + lane));
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float w0 = M != -INFINITY && lane < nsplit ? fast_exp2((l0 - M) * kLog2e) : 0.f;
   float Z = w0;
-  if (M != -INFINITY)
-    for (int s0 = 32; s0 < nsplit; s0 += 32)
-      if (s0 + lane < nsplit) Z += fast_exp2((lse_of(s0 + lane) - M) * kLog2e);
   for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
   const float invZ = Z > 0.f ? 1.f / Z : 0.f;
   w0 *= invZ;
@@ -167,10 +175,7 @@ __device__ __forceinline__ void merge_row(const DecodeArgs& a, long long pbase, 
 #pragma unroll
     for (int sp = 0; sp < kMergeBatch; ++sp) {
       if (s0 + sp >= nsplit) break;
-      // splits past the 32nd (rare) read their LSE again
-      const float w = s0 + sp < 32 ? __shfl_sync(0xffffffffu, w0, (s0 + sp) & 31)
-                                   : (M != -INFINITY ? fast_exp2((lse_of(s0 + sp) - M) * kLog2e) * invZ : 0.f);
-      V::fma(acc, w, x[sp]);
+      V::fma(acc, __shfl_sync(0xffffffffu, w0, s0 + sp), x[sp]);
     }
   }
   uint16_t* dst = a.out + orow * D + lane * PER;
@@ -332,214 +337,552 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
     const int npages = it.p1 - it.p0;
     const int nst = (npages + C::kStagePages - 1) / C::kStagePages;
 
-    // rows of this thread: ra = wr*16 + rq, rb = ra + 8 -> (token i, head-in-group)
-    const int ra = wr * 16 + rq, rb = ra + 8;
-    const bool va = ra < rows_valid, vb = rb < rows_valid;
-    const int prefix = L - qo;
-    const int lim_a = prefix + min(ra / G, qo - 1);
-    const int lim_b = prefix + min(rb / G, qo - 1);
-    const long long qrow_a = ((long long)(q0 + ra / G) * a.num_q_heads + g * G + ra % G) * D;
-    const long long qrow_b = ((long long)(q0 + rb / G) * a.num_q_heads + g * G + rb % G) * D;
-
-    // Q fragments (A operand), D/16 k-steps x 4 registers
-    uint32_t qf[D / 16][4];
-    if constexpr (!C::FP8) {
+    if constexpr (C::RT > 0) {
+      // ---------------------------------------------- key-major tile (decode)
+      // S^T = K Q^T with the stage's keys along the MMA's M (16 per block) and
+      // the unit's query rows along N (RT tiles of 8), then O^T += V^T P^T with
+      // head-dim columns along M. With GQA groups of 8 or fewer rows no MMA
+      // row is padding on the key side, so the MMAs and exponentials per key
+      // are half those of a 16-row query tile. Lane (g8 = lane/4, t4 = lane%4)
+      // holds rows 8j + 2*t4 + {0,1} of every row tile j.
+      constexpr int RT = C::RT;
+      constexpr int MT = D / 16;  // 16-column m-tiles of O^T
+      const int t4 = lane & 3, g8 = lane >> 2;
+      const int prefix = L - qo;
+      int lim[RT][2];
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int c0 = kk * 16 + 2 * qd;
-        qf[kk][0] = va ? *reinterpret_cast<const uint32_t*>(a.q + qrow_a + c0) : 0u;
-        qf[kk][1] = vb ? *reinterpret_cast<const uint32_t*>(a.q + qrow_b + c0) : 0u;
-        qf[kk][2] = va ? *reinterpret_cast<const uint32_t*>(a.q + qrow_a + c0 + 8) : 0u;
-        qf[kk][3] = vb ? *reinterpret_cast<const uint32_t*>(a.q + qrow_b + c0 + 8) : 0u;
-      }
-    } else {
-      // permuted contraction order matching the 8-byte K loads below:
-      // k-step 2p  : logical k {2q,2q+1} <- D 32p+8q+{0,1}, {2q+8,2q+9} <- D 32p+8q+{2,3}
-      // k-step 2p+1: logical k {2q,2q+1} <- D 32p+8q+{4,5}, {2q+8,2q+9} <- D 32p+8q+{6,7}
+      for (int j = 0; j < RT; ++j)
 #pragma unroll
-      for (int p = 0; p < D / 32; ++p) {
-        const int c0 = p * 32 + 8 * qd;
-        uint4 xa = va ? *reinterpret_cast<const uint4*>(a.q + qrow_a + c0) : make_uint4(0, 0, 0, 0);
-        uint4 xb = vb ? *reinterpret_cast<const uint4*>(a.q + qrow_b + c0) : make_uint4(0, 0, 0, 0);
-        qf[2 * p][0] = pack_f16(bf16lo(xa.x), bf16hi(xa.x));
-        qf[2 * p][1] = pack_f16(bf16lo(xb.x), bf16hi(xb.x));
-        qf[2 * p][2] = pack_f16(bf16lo(xa.y), bf16hi(xa.y));
-        qf[2 * p][3] = pack_f16(bf16lo(xb.y), bf16hi(xb.y));
-        qf[2 * p + 1][0] = pack_f16(bf16lo(xa.z), bf16hi(xa.z));
-        qf[2 * p + 1][1] = pack_f16(bf16lo(xb.z), bf16hi(xb.z));
-        qf[2 * p + 1][2] = pack_f16(bf16lo(xa.w), bf16hi(xa.w));
-        qf[2 * p + 1][3] = pack_f16(bf16lo(xb.w), bf16hi(xb.w));
-      }
-    }
+        for (int e = 0; e < 2; ++e) lim[j][e] = prefix + min((8 * j + 2 * t4 + e) / G, qo - 1);
 
-    float o[C::kNT][4];
+      // Q^T fragments (B operand): column g8 of row tile j is query row 8j + g8
+      uint32_t qf[D / 16][RT][2];
 #pragma unroll
-    for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-    for (int st = 0; st < nst; ++st) {
-      // a failed wait keeps this warp on the common control flow (so every
-      // named barrier still sees all consumer warps); the loop-top vote ends it
-      if (!aborted && !mbar_wait_ab(&full[slot], phase, plan, s_abort)) {
-        *s_abort = 1;
-        aborted = true;
-      }
-      const uint32_t kbase = smem_u32(smem + slot * C::kStageBytes);
-      const uint32_t vbase = kbase + C::kTileBytes;
-      const int stage_key0 = key_begin + st * C::kStageKeys;
-      // last page of the request with a partial fill: zero the V rows past L
-      const bool tail = (it.p1 == np_req) && (st == nst - 1) && (L % kPageSize) != 0;
-      if (tail) {
-        const int r0 = L - stage_key0;
-        const int r1 = min(C::kStagePages, npages - st * C::kStagePages) * kPageSize;
-        uint8_t* vb8 = smem + slot * C::kStageBytes + C::kTileBytes;
-        const int n16 = (r1 - r0) * C::kColBlocks * 8;
-        for (int i = cw * 32 + lane; i < n16; i += C::kConsumerWarps * 32) {
-          const int row = r0 + i / (C::kColBlocks * 8);
-          const int rest = i % (C::kColBlocks * 8);
-          const int cb = rest / 8, ch = rest % 8;
-          *reinterpret_cast<uint4*>(vb8 + cb * C::kStageKeys * 128 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < RT; ++j) {
+        const int rn = 8 * j + g8;
+        const bool vn = rn < rows_valid;
+        const long long qrow = ((long long)(q0 + rn / G) * a.num_q_heads + g * G + rn % G) * D;
+        if constexpr (!C::FP8) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int c0 = kk * 16 + 2 * t4;
+            qf[kk][j][0] = vn ? *reinterpret_cast<const uint32_t*>(a.q + qrow + c0) : 0u;
+            qf[kk][j][1] = vn ? *reinterpret_cast<const uint32_t*>(a.q + qrow + c0 + 8) : 0u;
+          }
+        } else {
+          // contraction order permuted to match the 8-byte K loads below:
+          // k-step 2p  : slots {2t,2t+1} <- D 32p+8t+{0,1}, {2t+8,2t+9} <- D 32p+8t+{2,3}
+          // k-step 2p+1: slots {2t,2t+1} <- D 32p+8t+{4,5}, {2t+8,2t+9} <- D 32p+8t+{6,7}
+#pragma unroll
+          for (int p = 0; p < D / 32; ++p) {
+            const uint4 x = vn ? *reinterpret_cast<const uint4*>(a.q + qrow + p * 32 + 8 * t4) : make_uint4(0, 0, 0, 0);
+            qf[2 * p][j][0] = pack_f16(bf16lo(x.x), bf16hi(x.x));
+            qf[2 * p][j][1] = pack_f16(bf16lo(x.y), bf16hi(x.y));
+            qf[2 * p + 1][j][0] = pack_f16(bf16lo(x.z), bf16hi(x.z));
+            qf[2 * p + 1][j][1] = pack_f16(bf16lo(x.w), bf16hi(x.w));
+          }
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1, C::kConsumerWarps * 32);
       }
 
-      // a row-warp whose 16 rows are all padding (fewer drafts than the tile
-      // holds) still takes part in the stage protocol but computes nothing
-      if (!skip && (C::WR == 1 || wr * 16 < rows_valid)) {
+      // O^T accumulators: o[mt][j] = {(c, 8j+2t4), (c, 8j+2t4+1), (c', 8j+2t4), (c', 8j+2t4+1)}
+      // with columns c = kcol(mt, 0), c' = kcol(mt, 1)
+      float o[MT][RT][4];
 #pragma unroll
-        for (int kb = 0; kb < C::KPW / 16; ++kb) {
-          const int kr0 = wk * C::KPW + kb * 16;  // first stage row of this 16-key block
-          const int abs0 = stage_key0 + kr0;
-          if (abs0 >= key_end) break;
-          // ---- S = Q K^T for 16 keys (two n-tiles of 8) ----
-          float s[2][4];
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-          if constexpr (!C::FP8) {
-            const int key = kr0 + (lane & 7) + ((lane >> 4) << 3);
+        for (int j = 0; j < RT; ++j) o[mt][j][0] = o[mt][j][1] = o[mt][j][2] = o[mt][j][3] = 0.f;
+      float m[RT][2], l[RT][2];
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const int chunk = 2 * kk + ((lane >> 3) & 1);
-              const uint32_t addr = kbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
-              uint32_t b00, b01, b10, b11;
-              ldsm_x4(addr, b00, b01, b10, b11);
-              mma_bf16(s[0], qf[kk], b00, b01);
-              mma_bf16(s[1], qf[kk], b10, b11);
-            }
-          } else {
+      for (int j = 0; j < RT; ++j) m[j][0] = m[j][1] = -INFINITY, l[j][0] = l[j][1] = 0.f;
+      auto kcol = [&](int mt, int hi) { return C::FP8 ? 16 * mt + 2 * g8 + hi : 16 * mt + 8 * hi + g8; };
+
+      for (int st = 0; st < nst; ++st) {
+        // a failed wait keeps this warp on the common control flow (so every
+        // named barrier still sees all consumer warps); the loop-top vote ends it
+        if (!aborted && !mbar_wait_ab(&full[slot], phase, plan, s_abort)) {
+          *s_abort = 1;
+          aborted = true;
+        }
+        const uint32_t kbase = smem_u32(smem + slot * C::kStageBytes);
+        const uint32_t vbase = kbase + C::kTileBytes;
+        const int stage_key0 = key_begin + st * C::kStageKeys;
+        // last page of the request with a partial fill: zero the V rows past L
+        const bool tail = (it.p1 == np_req) && (st == nst - 1) && (L % kPageSize) != 0;
+        if (tail) {
+          const int r0 = L - stage_key0;
+          const int r1 = min(C::kStagePages, npages - st * C::kStagePages) * kPageSize;
+          uint8_t* vb8 = smem + slot * C::kStageBytes + C::kTileBytes;
+          const int n16 = (r1 - r0) * C::kColBlocks * 8;
+          for (int i = cw * 32 + lane; i < n16; i += C::kConsumerWarps * 32) {
+            const int row = r0 + i / (C::kColBlocks * 8);
+            const int rest = i % (C::kColBlocks * 8);
+            const int cb = rest / 8, ch = rest % 8;
+            *reinterpret_cast<uint4*>(vb8 + cb * C::kStageKeys * 128 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, C::kConsumerWarps * 32);
+        }
+
+        if (!skip) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              const int key = kr0 + nt * 8 + rq;
+          for (int kb = 0; kb < C::KPW / 16; ++kb) {
+            const int kr0 = wk * C::KPW + kb * 16;  // first stage row of this 16-key block
+            const int abs0 = stage_key0 + kr0;
+            if (abs0 >= key_end) break;
+            // ---- S^T = K Q^T: s[j] = {(key g8, row 2t4), (g8, 2t4+1), (g8+8, 2t4), (g8+8, 2t4+1)}
+            float s[RT][4];
+#pragma unroll
+            for (int j = 0; j < RT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+            if constexpr (!C::FP8) {
+              const int key = kr0 + (lane & 15);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const int chunk = 2 * kk + (lane >> 4);
+                const uint32_t addr = kbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
+                uint32_t ka[4];
+                ldsm_x4(addr, ka[0], ka[1], ka[2], ka[3]);
+#pragma unroll
+                for (int j = 0; j < RT; ++j) mma_bf16(s[j], ka, qf[kk][j][0], qf[kk][j][1]);
+              }
+            } else {
 #pragma unroll
               for (int p = 0; p < D / 32; ++p) {
-                const int byte = p * 32 + 8 * qd;
-                const uint32_t addr = kbase + swz(key, byte >> 4) + (byte & 15);
-                uint32_t x0, x1;
-                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x0), "=r"(x1) : "r"(addr));
-                mma_f16(s[nt], qf[2 * p], e4m3x2_to_f16x2((uint16_t)(x0 & 0xffff)),
-                        e4m3x2_to_f16x2((uint16_t)(x0 >> 16)));
-                mma_f16(s[nt], qf[2 * p + 1], e4m3x2_to_f16x2((uint16_t)(x1 & 0xffff)),
-                        e4m3x2_to_f16x2((uint16_t)(x1 >> 16)));
+                const int byte = p * 32 + 8 * t4;
+                uint32_t x0[2], x1[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const uint32_t addr = kbase + swz(kr0 + g8 + 8 * h, byte >> 4) + (byte & 15);
+                  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x0[h]), "=r"(x1[h]) : "r"(addr));
+                }
+                const uint32_t ka0[4] = {e4m3x2_to_f16x2((uint16_t)(x0[0] & 0xffff)),
+                                         e4m3x2_to_f16x2((uint16_t)(x0[1] & 0xffff)),
+                                         e4m3x2_to_f16x2((uint16_t)(x0[0] >> 16)),
+                                         e4m3x2_to_f16x2((uint16_t)(x0[1] >> 16))};
+                const uint32_t ka1[4] = {e4m3x2_to_f16x2((uint16_t)(x1[0] & 0xffff)),
+                                         e4m3x2_to_f16x2((uint16_t)(x1[1] & 0xffff)),
+                                         e4m3x2_to_f16x2((uint16_t)(x1[0] >> 16)),
+                                         e4m3x2_to_f16x2((uint16_t)(x1[1] >> 16))};
+#pragma unroll
+                for (int j = 0; j < RT; ++j) {
+                  mma_f16(s[j], ka0, qf[2 * p][j][0], qf[2 * p][j][1]);
+                  mma_f16(s[j], ka1, qf[2 * p + 1][j][0], qf[2 * p + 1][j][1]);
+                }
+              }
+            }
+            // ---- mask, online softmax over the 16 keys (log2 domain) ----
+            float al[RT][2];
+            bool rescale = false;
+#pragma unroll
+            for (int j = 0; j < RT; ++j) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int kp = abs0 + g8 + 8 * h;
+                const bool ok = kp < key_end;
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                  s[j][2 * h + e] = (ok && kp <= lim[j][e]) ? s[j][2 * h + e] * a.scale_log2 : -INFINITY;
+              }
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                float mx = fmaxf(s[j][e], s[j][2 + e]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(m[j][e], mx);
+                const float ref = mn == -INFINITY ? 0.f : mn;
+                al[j][e] = fast_exp2(m[j][e] - ref);
+                m[j][e] = mn;
+                s[j][e] = fast_exp2(s[j][e] - ref);
+                s[j][2 + e] = fast_exp2(s[j][2 + e] - ref);
+                l[j][e] = l[j][e] * al[j][e] + s[j][e] + s[j][2 + e];
+                rescale |= al[j][e] != 1.f;
+              }
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int j = 0; j < RT; ++j) {
+                  o[mt][j][0] *= al[j][0];
+                  o[mt][j][1] *= al[j][1];
+                  o[mt][j][2] *= al[j][0];
+                  o[mt][j][3] *= al[j][1];
+                }
+            }
+            // ---- P^T as the B operand: the accumulator layout of keys 0-7 and
+            // 8-15 is that of an ldmatrix fragment, and its transpose is B's
+            uint32_t pb[RT][2];
+#pragma unroll
+            for (int j = 0; j < RT; ++j) {
+              pb[j][0] = movmatrix_trans(C::FP8 ? pack_f16(s[j][0], s[j][1]) : pack_bf16(s[j][0], s[j][1]));
+              pb[j][1] = movmatrix_trans(C::FP8 ? pack_f16(s[j][2], s[j][3]) : pack_bf16(s[j][2], s[j][3]));
+            }
+            // ---- O^T += V^T P^T ----
+            if constexpr (!C::FP8) {
+              const int key = kr0 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                const int chunk = 2 * mt + ((lane >> 3) & 1);
+                const uint32_t addr = vbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
+                uint32_t va[4];
+                ldsm_x4_t(addr, va[0], va[1], va[2], va[3]);
+#pragma unroll
+                for (int j = 0; j < RT; ++j) mma_bf16(o[mt][j], va, pb[j][0], pb[j][1]);
+              }
+            } else {
+              const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+              for (int mp = 0; mp < D / 32; ++mp) {
+                // 16-byte chunks 2mp (D 32mp..+15) and 2mp+1 (D 32mp+16..+31);
+                // r0: keys 0-7 / chunk 2mp, r1: keys 8-15 / chunk 2mp, r2, r3: chunk 2mp+1.
+                // bytes of r: V[2t][2g], V[2t][2g+1], V[2t+1][2g], V[2t+1][2g+1], so
+                // m-row g of a tile is column 2g and m-row g+8 is column 2g+1
+                const int chunk = 2 * mp + (lane >> 4);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_t(vbase + swz(key, chunk), r0, r1, r2, r3);
+                const uint32_t va0[4] = {e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0020)),
+                                         e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0031)),
+                                         e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0020)),
+                                         e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0031))};
+                const uint32_t va1[4] = {e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0020)),
+                                         e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0031)),
+                                         e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0020)),
+                                         e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0031))};
+#pragma unroll
+                for (int j = 0; j < RT; ++j) {
+                  mma_f16(o[2 * mp][j], va0, pb[j][0], pb[j][1]);
+                  mma_f16(o[2 * mp + 1][j], va1, pb[j][0], pb[j][1]);
+                }
               }
             }
           }
-          // ---- mask, online softmax (log2 domain) ----
-          float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int kp = abs0 + nt * 8 + 2 * qd + e;
-              const bool ok = kp < key_end;
-              s[nt][e] = (ok && kp <= lim_a) ? s[nt][e] * a.scale_log2 : -INFINITY;
-              s[nt][2 + e] = (ok && kp <= lim_b) ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
-              mx_a = fmaxf(mx_a, s[nt][e]);
-              mx_b = fmaxf(mx_b, s[nt][2 + e]);
-            }
-          }
-          mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-          mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-          mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-          mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-          const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-          const float ref_a = mn_a == -INFINITY ? 0.f : mn_a;
-          const float ref_b = mn_b == -INFINITY ? 0.f : mn_b;
-          const float al_a = fast_exp2(m_a - ref_a), al_b = fast_exp2(m_b - ref_b);
-          m_a = mn_a;
-          m_b = mn_b;
-          float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              s[nt][e] = fast_exp2(s[nt][e] - ref_a);
-              s[nt][2 + e] = fast_exp2(s[nt][2 + e] - ref_b);
-              ps_a += s[nt][e];
-              ps_b += s[nt][2 + e];
-            }
-          }
-          l_a = l_a * al_a + ps_a;
-          l_b = l_b * al_b + ps_b;
-          if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {
-#pragma unroll
-            for (int nt = 0; nt < C::kNT; ++nt) {
-              o[nt][0] *= al_a;
-              o[nt][1] *= al_a;
-              o[nt][2] *= al_b;
-              o[nt][3] *= al_b;
-            }
-          }
-          // ---- O += P V ----
-          uint32_t pf[4];
-          if constexpr (!C::FP8) {
-            pf[0] = pack_bf16(s[0][0], s[0][1]);
-            pf[1] = pack_bf16(s[0][2], s[0][3]);
-            pf[2] = pack_bf16(s[1][0], s[1][1]);
-            pf[3] = pack_bf16(s[1][2], s[1][3]);
-            const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-            for (int jj = 0; jj < D / 16; ++jj) {
-              const int chunk = 2 * jj + (lane >> 4);
-              const uint32_t addr = vbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
-              uint32_t b0e, b1e, b0o, b1o;
-              ldsm_x4_t(addr, b0e, b1e, b0o, b1o);
-              mma_bf16(o[2 * jj], pf, b0e, b1e);
-              mma_bf16(o[2 * jj + 1], pf, b0o, b1o);
-            }
-          } else {
-            pf[0] = pack_f16(s[0][0], s[0][1]);
-            pf[1] = pack_f16(s[0][2], s[0][3]);
-            pf[2] = pack_f16(s[1][0], s[1][1]);
-            pf[3] = pack_f16(s[1][2], s[1][3]);
-            const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-            for (int jp = 0; jp < D / 32; ++jp) {
-              // 16-byte chunks 2jp (D 32jp..+15) and 2jp+1 (D 32jp+16..+31)
-              const int chunk = 2 * jp + (lane >> 4);
-              const uint32_t addr = vbase + swz(key, chunk);
-              uint32_t r0, r1, r2, r3;
-              ldsm_x4_t(addr, r0, r1, r2, r3);
-              // r0: keys 0-7 / chunk 2jp, r1: keys 8-15 / chunk 2jp, r2, r3: chunk 2jp+1.
-              // bytes of r: V[2q][2c], V[2q][2c+1], V[2q+1][2c], V[2q+1][2c+1]
-              const uint32_t e0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0020));
-              const uint32_t o0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0031));
-              const uint32_t e1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0020));
-              const uint32_t o1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0031));
-              const uint32_t e2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0020));
-              const uint32_t o2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0031));
-              const uint32_t e3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0020));
-              const uint32_t o3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0031));
-              mma_f16(o[4 * jp + 0], pf, e0, e1);
-              mma_f16(o[4 * jp + 1], pf, o0, o1);
-              mma_f16(o[4 * jp + 2], pf, e2, e3);
-              mma_f16(o[4 * jp + 3], pf, o2, o3);
-            }
+        }
+        const bool hold = st == nst - 1;  // last stage doubles as merge scratch
+        if (!hold) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+          if (++slot == C::STAGES) {
+            slot = 0;
+            phase ^= 1;
           }
         }
       }
-      const bool hold = (C::WK > 1) && (st == nst - 1);  // last stage doubles as merge scratch
-      if (!hold) {
+      // ------------------------------------------------ epilogue (key-major)
+      // each lane summed its own keys: add over the eight lanes of a row
+#pragma unroll
+      for (int j = 0; j < RT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          l[j][e] += __shfl_xor_sync(0xffffffffu, l[j][e], 4);
+          l[j][e] += __shfl_xor_sync(0xffffffffu, l[j][e], 8);
+          l[j][e] += __shfl_xor_sync(0xffffffffu, l[j][e], 16);
+        }
+      const bool direct = nsplit == 1;
+      const int split = it.split;
+      auto out_row = [&](int r, uint16_t*& orow, float*& lrow) {
+        const int i = r / G, h = g * G + r % G;
+        const long long t = q0 + i;
+        if (direct) {
+          orow = a.out + (t * a.num_q_heads + h) * D;
+          lrow = a.lse ? a.lse + t * a.num_q_heads + h : nullptr;
+        } else {
+          const long long pr = (long long)a.m.partial_indptr[b] + (long long)split * qo + i;
+          orow = a.m.partial_o + (pr * a.num_q_heads + h) * D;
+          lrow = a.m.partial_lse + pr * a.num_q_heads + h;
+        }
+      };
+      // scratch columns XOR-swizzled by row so a store's 32 lanes hit 32 banks
+      auto kswz = [](int r) { return ((r >> 1) & 3) << (C::FP8 ? 4 : 3); };
+      if (nst == 0) {
+        // empty key range (padding request): zero output, -inf LSE
+        if (wk == 0 && !skip) {
+          for (int idx = lane; idx < rows_valid * (D / 2); idx += 32) {
+            const int r = idx / (D / 2), c2 = idx % (D / 2);
+            uint16_t* orow;
+            float* lrow;
+            out_row(r, orow, lrow);
+            *reinterpret_cast<uint32_t*>(orow + 2 * c2) = 0u;
+            if (c2 == 0 && lrow) *lrow = -INFINITY;
+          }
+        }
+      } else {
+        named_bar_sync(1, C::kConsumerWarps * 32);  // everyone done reading the held stage
+        float* scr = reinterpret_cast<float*>(smem + slot * C::kStageBytes);  // [WK][16][D]
+        float* my = scr + wk * 16 * D;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int j = 0; j < RT; ++j)
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int r = 8 * j + 2 * t4 + e;
+                my[r * D + (kcol(mt, hi) ^ kswz(r))] = o[mt][j][2 * hi + e];
+              }
+        if (g8 == 0) {
+#pragma unroll
+          for (int j = 0; j < RT; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int r = 8 * j + 2 * t4 + e;
+              s_ml[(wk * 16 + r) * 2 + 0] = m[j][e];
+              s_ml[(wk * 16 + r) * 2 + 1] = l[j][e];
+            }
+        }
+        named_bar_sync(1, C::kConsumerWarps * 32);
+        // each consumer thread finishes float4 pieces of the rows x D tile
+        const int nthr = C::kConsumerWarps * 32;
+        const int ctid = cw * 32 + lane;
+        const int nrows = skip ? 0 : min(rows_valid, C::kRows);
+        for (int idx = ctid; idx < nrows * (D / 4); idx += nthr) {
+          const int r = idx / (D / 4), c4 = idx % (D / 4);
+          float mw[C::WK], lw[C::WK];
+          float M = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < C::WK; ++k) {
+            mw[k] = s_ml[(k * 16 + r) * 2 + 0];
+            lw[k] = s_ml[(k * 16 + r) * 2 + 1];
+            M = fmaxf(M, mw[k]);
+          }
+          float Lsum = 0.f, wgt[C::WK];
+#pragma unroll
+          for (int k = 0; k < C::WK; ++k) {
+            wgt[k] = (M == -INFINITY) ? 0.f : fast_exp2(mw[k] - M);
+            Lsum += lw[k] * wgt[k];
+          }
+          const float inv = Lsum > 0.f ? a.v_scale / Lsum : 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < C::WK; ++k) {
+            const float4 x = *reinterpret_cast<const float4*>(scr + (k * 16 + r) * D + ((c4 * 4) ^ kswz(r)));
+            acc.x += x.x * wgt[k];
+            acc.y += x.y * wgt[k];
+            acc.z += x.z * wgt[k];
+            acc.w += x.w * wgt[k];
+          }
+          uint16_t* orow;
+          float* lrow;
+          out_row(r, orow, lrow);
+          *reinterpret_cast<uint2*>(orow + c4 * 4) =
+              make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+          if (c4 == 0 && lrow) *lrow = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, C::kConsumerWarps * 32);  // scratch reads done before the stage is refilled
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == C::STAGES) {
+          slot = 0;
+          phase ^= 1;
+        }
+      }
+    } else {
+      // rows of this thread: ra = wr*16 + rq, rb = ra + 8 -> (token i, head-in-group)
+      const int ra = wr * 16 + rq, rb = ra + 8;
+      const bool va = ra < rows_valid, vb = rb < rows_valid;
+      const int prefix = L - qo;
+      const int lim_a = prefix + min(ra / G, qo - 1);
+      const int lim_b = prefix + min(rb / G, qo - 1);
+      const long long qrow_a = ((long long)(q0 + ra / G) * a.num_q_heads + g * G + ra % G) * D;
+      const long long qrow_b = ((long long)(q0 + rb / G) * a.num_q_heads + g * G + rb % G) * D;
+
+      // Q fragments (A operand), D/16 k-steps x 4 registers
+      uint32_t qf[D / 16][4];
+      if constexpr (!C::FP8) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c0 = kk * 16 + 2 * qd;
+          qf[kk][0] = va ? *reinterpret_cast<const uint32_t*>(a.q + qrow_a + c0) : 0u;
+          qf[kk][1] = vb ? *reinterpret_cast<const uint32_t*>(a.q + qrow_b + c0) : 0u;
+          qf[kk][2] = va ? *reinterpret_cast<const uint32_t*>(a.q + qrow_a + c0 + 8) : 0u;
+          qf[kk][3] = vb ? *reinterpret_cast<const uint32_t*>(a.q + qrow_b + c0 + 8) : 0u;
+        }
+      } else {
+        // permuted contraction order matching the 8-byte K loads below:
+        // k-step 2p  : logical k {2q,2q+1} <- D 32p+8q+{0,1}, {2q+8,2q+9} <- D 32p+8q+{2,3}
+        // k-step 2p+1: logical k {2q,2q+1} <- D 32p+8q+{4,5}, {2q+8,2q+9} <- D 32p+8q+{6,7}
+#pragma unroll
+        for (int p = 0; p < D / 32; ++p) {
+          const int c0 = p * 32 + 8 * qd;
+          uint4 xa = va ? *reinterpret_cast<const uint4*>(a.q + qrow_a + c0) : make_uint4(0, 0, 0, 0);
+          uint4 xb = vb ? *reinterpret_cast<const uint4*>(a.q + qrow_b + c0) : make_uint4(0, 0, 0, 0);
+          qf[2 * p][0] = pack_f16(bf16lo(xa.x), bf16hi(xa.x));
+          qf[2 * p][1] = pack_f16(bf16lo(xb.x), bf16hi(xb.x));
+          qf[2 * p][2] = pack_f16(bf16lo(xa.y), bf16hi(xa.y));
+          qf[2 * p][3] = pack_f16(bf16lo(xb.y), bf16hi(xb.y));
+          qf[2 * p + 1][0] = pack_f16(bf16lo(xa.z), bf16hi(xa.z));
+          qf[2 * p + 1][1] = pack_f16(bf16lo(xb.z), bf16hi(xb.z));
+          qf[2 * p + 1][2] = pack_f16(bf16lo(xa.w), bf16hi(xa.w));
+          qf[2 * p + 1][3] = pack_f16(bf16lo(xb.w), bf16hi(xb.w));
+        }
+      }
+
+      float o[C::kNT][4];
+#pragma unroll
+      for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+      float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+      for (int st = 0; st < nst; ++st) {
+        // a failed wait keeps this warp on the common control flow (so every
+        // named barrier still sees all consumer warps); the loop-top vote ends it
+        if (!aborted && !mbar_wait_ab(&full[slot], phase, plan, s_abort)) {
+          *s_abort = 1;
+          aborted = true;
+        }
+        const uint32_t kbase = smem_u32(smem + slot * C::kStageBytes);
+        const uint32_t vbase = kbase + C::kTileBytes;
+        const int stage_key0 = key_begin + st * C::kStageKeys;
+        // last page of the request with a partial fill: zero the V rows past L
+        const bool tail = (it.p1 == np_req) && (st == nst - 1) && (L % kPageSize) != 0;
+        if (tail) {
+          const int r0 = L - stage_key0;
+          const int r1 = min(C::kStagePages, npages - st * C::kStagePages) * kPageSize;
+          uint8_t* vb8 = smem + slot * C::kStageBytes + C::kTileBytes;
+          const int n16 = (r1 - r0) * C::kColBlocks * 8;
+          for (int i = cw * 32 + lane; i < n16; i += C::kConsumerWarps * 32) {
+            const int row = r0 + i / (C::kColBlocks * 8);
+            const int rest = i % (C::kColBlocks * 8);
+            const int cb = rest / 8, ch = rest % 8;
+            *reinterpret_cast<uint4*>(vb8 + cb * C::kStageKeys * 128 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, C::kConsumerWarps * 32);
+        }
+
+        // a row-warp whose 16 rows are all padding (fewer drafts than the tile
+        // holds) still takes part in the stage protocol but computes nothing
+        if (!skip && (C::WR == 1 || wr * 16 < rows_valid)) {
+#pragma unroll
+          for (int kb = 0; kb < C::KPW / 16; ++kb) {
+            const int kr0 = wk * C::KPW + kb * 16;  // first stage row of this 16-key block
+            const int abs0 = stage_key0 + kr0;
+            if (abs0 >= key_end) break;
+            // ---- S = Q K^T for 16 keys (two n-tiles of 8) ----
+            float s[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            if constexpr (!C::FP8) {
+              const int key = kr0 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const int chunk = 2 * kk + ((lane >> 3) & 1);
+                const uint32_t addr = kbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4(addr, b00, b01, b10, b11);
+                mma_bf16(s[0], qf[kk], b00, b01);
+                mma_bf16(s[1], qf[kk], b10, b11);
+              }
+            } else {
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) {
+                const int key = kr0 + nt * 8 + rq;
+#pragma unroll
+                for (int p = 0; p < D / 32; ++p) {
+                  const int byte = p * 32 + 8 * qd;
+                  const uint32_t addr = kbase + swz(key, byte >> 4) + (byte & 15);
+                  uint32_t x0, x1;
+                  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x0), "=r"(x1) : "r"(addr));
+                  mma_f16(s[nt], qf[2 * p], e4m3x2_to_f16x2((uint16_t)(x0 & 0xffff)),
+                          e4m3x2_to_f16x2((uint16_t)(x0 >> 16)));
+                  mma_f16(s[nt], qf[2 * p + 1], e4m3x2_to_f16x2((uint16_t)(x1 & 0xffff)),
+                          e4m3x2_to_f16x2((uint16_t)(x1 >> 16)));
+                }
+              }
+            }
+            // ---- mask, online softmax (log2 domain) ----
+            float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int kp = abs0 + nt * 8 + 2 * qd + e;
+                const bool ok = kp < key_end;
+                s[nt][e] = (ok && kp <= lim_a) ? s[nt][e] * a.scale_log2 : -INFINITY;
+                s[nt][2 + e] = (ok && kp <= lim_b) ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
+                mx_a = fmaxf(mx_a, s[nt][e]);
+                mx_b = fmaxf(mx_b, s[nt][2 + e]);
+              }
+            }
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+            const float ref_a = mn_a == -INFINITY ? 0.f : mn_a;
+            const float ref_b = mn_b == -INFINITY ? 0.f : mn_b;
+            const float al_a = fast_exp2(m_a - ref_a), al_b = fast_exp2(m_b - ref_b);
+            m_a = mn_a;
+            m_b = mn_b;
+            float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                s[nt][e] = fast_exp2(s[nt][e] - ref_a);
+                s[nt][2 + e] = fast_exp2(s[nt][2 + e] - ref_b);
+                ps_a += s[nt][e];
+                ps_b += s[nt][2 + e];
+              }
+            }
+            l_a = l_a * al_a + ps_a;
+            l_b = l_b * al_b + ps_b;
+            if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {
+#pragma unroll
+              for (int nt = 0; nt < C::kNT; ++nt) {
+                o[nt][0] *= al_a;
+                o[nt][1] *= al_a;
+                o[nt][2] *= al_b;
+                o[nt][3] *= al_b;
+              }
+            }
+            // ---- O += P V ----
+            uint32_t pf[4];
+            if constexpr (!C::FP8) {
+              pf[0] = pack_bf16(s[0][0], s[0][1]);
+              pf[1] = pack_bf16(s[0][2], s[0][3]);
+              pf[2] = pack_bf16(s[1][0], s[1][1]);
+              pf[3] = pack_bf16(s[1][2], s[1][3]);
+              const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+              for (int jj = 0; jj < D / 16; ++jj) {
+                const int chunk = 2 * jj + (lane >> 4);
+                const uint32_t addr = vbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
+                uint32_t b0e, b1e, b0o, b1o;
+                ldsm_x4_t(addr, b0e, b1e, b0o, b1o);
+                mma_bf16(o[2 * jj], pf, b0e, b1e);
+                mma_bf16(o[2 * jj + 1], pf, b0o, b1o);
+              }
+            } else {
+              pf[0] = pack_f16(s[0][0], s[0][1]);
+              pf[1] = pack_f16(s[0][2], s[0][3]);
+              pf[2] = pack_f16(s[1][0], s[1][1]);
+              pf[3] = pack_f16(s[1][2], s[1][3]);
+              const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+              for (int jp = 0; jp < D / 32; ++jp) {
+                // 16-byte chunks 2jp (D 32jp..+15) and 2jp+1 (D 32jp+16..+31)
+                const int chunk = 2 * jp + (lane >> 4);
+                const uint32_t addr = vbase + swz(key, chunk);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_t(addr, r0, r1, r2, r3);
+                // r0: keys 0-7 / chunk 2jp, r1: keys 8-15 / chunk 2jp, r2, r3: chunk 2jp+1.
+                // bytes of r: V[2q][2c], V[2q][2c+1], V[2q+1][2c], V[2q+1][2c+1]
+                const uint32_t e0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0020));
+                const uint32_t o0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0031));
+                const uint32_t e1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0020));
+                const uint32_t o1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0031));
+                const uint32_t e2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0020));
+                const uint32_t o2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0031));
+                const uint32_t e3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0020));
+                const uint32_t o3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0031));
+                mma_f16(o[4 * jp + 0], pf, e0, e1);
+                mma_f16(o[4 * jp + 1], pf, o0, o1);
+                mma_f16(o[4 * jp + 2], pf, e2, e3);
+                mma_f16(o[4 * jp + 3], pf, o2, o3);
+              }
+            }
+          }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
         if (++slot == C::STAGES) {
@@ -547,31 +890,29 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           phase ^= 1;
         }
       }
-    }
-    // ---------------------------------------------------------- epilogue
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+      // ---------------------------------------------------------- epilogue
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
 
-    const bool direct = nsplit == 1;
-    const int split = it.split;
-    // destination row of row r: the output, or (split units) a bf16 partial
-    // row of the same layout plus its LSE
-    auto out_row = [&](int r, uint16_t*& orow, float*& lrow) {
-      const int i = r / G, h = g * G + r % G;
-      const long long t = q0 + i;
-      if (direct) {
-        orow = a.out + (t * a.num_q_heads + h) * D;
-        lrow = a.lse ? a.lse + t * a.num_q_heads + h : nullptr;
-      } else {
-        const long long pr = (long long)a.m.partial_indptr[b] + (long long)split * qo + i;
-        orow = a.m.partial_o + (pr * a.num_q_heads + h) * D;
-        lrow = a.m.partial_lse + pr * a.num_q_heads + h;
-      }
-    };
+      const bool direct = nsplit == 1;
+      const int split = it.split;
+      // destination row of row r: the output, or (split units) a bf16 partial
+      // row of the same layout plus its LSE
+      auto out_row = [&](int r, uint16_t*& orow, float*& lrow) {
+        const int i = r / G, h = g * G + r % G;
+        const long long t = q0 + i;
+        if (direct) {
+          orow = a.out + (t * a.num_q_heads + h) * D;
+          lrow = a.lse ? a.lse + t * a.num_q_heads + h : nullptr;
+        } else {
+          const long long pr = (long long)a.m.partial_indptr[b] + (long long)split * qo + i;
+          orow = a.m.partial_o + (pr * a.num_q_heads + h) * D;
+          lrow = a.m.partial_lse + pr * a.num_q_heads + h;
+        }
+      };
 
-    if constexpr (C::WK == 1) {
       if (!skip) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -597,90 +938,6 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             }
           }
           if (qd == 0 && lrow) *lrow = lse;
-        }
-      }
-    } else {
-      // combine the WK key-warps of each row through shared memory
-      if (nst == 0) {
-        // empty key range (padding request): zero output, -inf LSE
-        if (wk == 0) {
-          for (int half = 0; half < 2; ++half) {
-            const int r = half ? rb : ra;
-            if (!(half ? vb : va) || skip) continue;
-            uint16_t* orow;
-            float* lrow;
-            out_row(r, orow, lrow);
-            for (int c = qd; c < D; c += 4) orow[c] = 0;
-            if (qd == 0 && lrow) *lrow = -INFINITY;
-          }
-        }
-      } else {
-        named_bar_sync(1, C::kConsumerWarps * 32);  // everyone done reading the held stage
-        float* scr = reinterpret_cast<float*>(smem + slot * C::kStageBytes);  // [WK][16][D]
-        float* my = scr + wk * 16 * D;
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = ocol<C::FP8>(nt, qd, e);
-            // columns XOR-swizzled by row so the 8 rows of a store hit 8 bank groups
-            my[rq * D + (c ^ ((rq & 7) << 2))] = o[nt][e];
-            my[(rq + 8) * D + (c ^ ((rq & 7) << 2))] = o[nt][2 + e];
-          }
-        }
-        if (qd == 0) {
-          s_ml[(wk * 16 + rq) * 2 + 0] = m_a;
-          s_ml[(wk * 16 + rq) * 2 + 1] = l_a;
-          s_ml[(wk * 16 + rq + 8) * 2 + 0] = m_b;
-          s_ml[(wk * 16 + rq + 8) * 2 + 1] = l_b;
-        }
-        named_bar_sync(1, C::kConsumerWarps * 32);
-        // each consumer thread finishes float4 pieces of the 16 x D tile
-        const int nthr = C::kConsumerWarps * 32;
-        const int ctid = cw * 32 + lane;
-        for (int idx = ctid; idx < 16 * (D / 4); idx += nthr) {
-          const int r = idx / (D / 4), c4 = idx % (D / 4);
-          if (r >= rows_valid || skip) continue;
-          float mw[C::WK], lw[C::WK];
-          float M = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < C::WK; ++k) {
-            mw[k] = s_ml[(k * 16 + r) * 2 + 0];
-            lw[k] = s_ml[(k * 16 + r) * 2 + 1];
-            M = fmaxf(M, mw[k]);
-          }
-          float Lsum = 0.f, wgt[C::WK];
-#pragma unroll
-          for (int k = 0; k < C::WK; ++k) {
-            wgt[k] = (M == -INFINITY) ? 0.f : fast_exp2(mw[k] - M);
-            Lsum += lw[k] * wgt[k];
-          }
-          const float inv = Lsum > 0.f ? a.v_scale / Lsum : 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int k = 0; k < C::WK; ++k) {
-            const float4 x = *reinterpret_cast<const float4*>(scr + (k * 16 + r) * D + ((c4 * 4) ^ ((r & 7) << 2)));
-            acc.x += x.x * wgt[k];
-            acc.y += x.y * wgt[k];
-            acc.z += x.z * wgt[k];
-            acc.w += x.w * wgt[k];
-          }
-          acc.x *= inv;
-          acc.y *= inv;
-          acc.z *= inv;
-          acc.w *= inv;
-          uint16_t* orow;
-          float* lrow;
-          out_row(r, orow, lrow);
-          *reinterpret_cast<uint2*>(orow + c4 * 4) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
-          if (c4 == 0 && lrow) *lrow = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, C::kConsumerWarps * 32);  // scratch reads done before the stage is refilled
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (++slot == C::STAGES) {
-          slot = 0;
-          phase ^= 1;
         }
       }
     }
@@ -757,9 +1014,12 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
 // Tile shapes: decode packs one 16-row tile per unit and splits each stage's
 // keys over four warps; the verify shape gives each of up to eight warps its
 // own 16 rows and all keys of a stage.
-using DecBf16D128 = DecodeCfg<128, false, 1, 4, 16, 3>;
-using DecBf16D64 = DecodeCfg<64, false, 1, 4, 16, 4>;
-using DecFp8D128 = DecodeCfg<128, true, 1, 4, 32, 3>;
+using DecBf16D128_1 = DecodeCfg<128, false, 1, 4, 16, 3, 1>;
+using DecBf16D128_2 = DecodeCfg<128, false, 1, 4, 16, 3, 2>;
+using DecBf16D64_1 = DecodeCfg<64, false, 1, 4, 16, 4, 1>;
+using DecBf16D64_2 = DecodeCfg<64, false, 1, 4, 16, 4, 2>;
+using DecFp8D128_1 = DecodeCfg<128, true, 1, 4, 32, 3, 1>;
+using DecFp8D128_2 = DecodeCfg<128, true, 1, 4, 32, 3, 2>;
 using VerBf16D128_2 = DecodeCfg<128, false, 2, 1, 64, 3>;
 using VerBf16D128_4 = DecodeCfg<128, false, 4, 1, 64, 3>;
 using VerBf16D128_8 = DecodeCfg<128, false, 8, 1, 64, 3>;
@@ -791,19 +1051,30 @@ int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool,
   const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
   const int D = c.cfg.head_dim;
   const int wr = decode_row_warps(c.cfg);
+  // decode shapes (at most 16 rows): key-major tiles of one or two 8-row tiles
+  const bool rt1 = c.cfg.max_qo_len * (c.cfg.num_q_heads / c.cfg.num_kv_heads) <= 8;
 #define PKV_RUN(CFG) return run_decode<CFG>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st)
   if (!fp8 && D == 128) {
-    if (wr == 1) PKV_RUN(DecBf16D128);
+    if (wr == 1) {
+      if (rt1) PKV_RUN(DecBf16D128_1);
+      PKV_RUN(DecBf16D128_2);
+    }
     if (wr == 2) PKV_RUN(VerBf16D128_2);
     if (wr == 4) PKV_RUN(VerBf16D128_4);
     if (wr == 8) PKV_RUN(VerBf16D128_8);
   } else if (!fp8 && D == 64) {
-    if (wr == 1) PKV_RUN(DecBf16D64);
+    if (wr == 1) {
+      if (rt1) PKV_RUN(DecBf16D64_1);
+      PKV_RUN(DecBf16D64_2);
+    }
     if (wr == 2) PKV_RUN(VerBf16D64_2);
     if (wr == 4) PKV_RUN(VerBf16D64_4);
     if (wr == 8) PKV_RUN(VerBf16D64_8);
   } else if (fp8 && D == 128) {
-    if (wr == 1) PKV_RUN(DecFp8D128);
+    if (wr == 1) {
+      if (rt1) PKV_RUN(DecFp8D128_1);
+      PKV_RUN(DecFp8D128_2);
+    }
     if (wr == 2) PKV_RUN(VerFp8D128_2);
     if (wr == 4) PKV_RUN(VerFp8D128_4);
     if (wr == 8) PKV_RUN(VerFp8D128_8);

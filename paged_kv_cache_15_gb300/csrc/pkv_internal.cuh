@@ -312,6 +312,15 @@ __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held the way ldmatrix
+// leaves it (lane l: row l/4, columns 2(l%4) and 2(l%4)+1, low half first):
+// returns the same layout of the transposed matrix.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
 // Two E4M3 codes (low byte first) -> two f16 in one register (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;

@@ -162,6 +162,33 @@ def test_decode_parity(case):
     full_check(W)
 
 
+@pytest.mark.parametrize("case", ["g16", "g16_fp8", "g12_d64", "g3", "mha_d64", "g8_fp8", "verify_q2", "verify_q4"])
+def test_decode_tile_shapes(case):
+    """Decode-path units of 1 to 16 query rows: one 8-row key-major tile for
+    up to 8 rows, two for 9 to 16 (groups of 12 and 16, four drafts of a group
+    of 4), bf16 and FP8 pools, head_dim 64 and 128; the verify cases put
+    several tokens with different causal limits into one tile."""
+    rng = np.random.default_rng(31)
+    lens = lambda n: rng.integers(0, 900, n)
+    if case == "g16":
+        W = make_workload("t_g16", "decode", 5, 32, 2, 128, lens(5), np.ones(5))
+    elif case == "g16_fp8":
+        W = make_workload("t_g16f", "decode", 4, 32, 2, 128, lens(4), np.ones(4), kv_dtype="fp8_e4m3")
+    elif case == "g12_d64":
+        W = make_workload("t_g12", "decode", 5, 24, 2, 64, lens(5), np.ones(5))
+    elif case == "g3":
+        W = make_workload("t_g3", "decode", 6, 24, 8, 128, lens(6), np.ones(6))
+    elif case == "mha_d64":
+        W = make_workload("t_mha", "decode", 4, 8, 8, 64, lens(4), np.ones(4))
+    elif case == "g8_fp8":
+        W = make_workload("t_g8f", "decode", 3, 32, 4, 128, lens(3), np.ones(3), kv_dtype="fp8_e4m3")
+    elif case == "verify_q2":
+        W = make_workload("t_vq2", "verify", 4, 16, 4, 128, lens(4), [2, 1, 2, 2])
+    else:
+        W = make_workload("t_vq4", "verify", 4, 16, 4, 128, lens(4), [4, 3, 4, 1])
+    full_check(W, spec_mode=B.PKV_SPEC_DECODE)
+
+
 def test_decode_padding_requests_give_zero_and_neg_inf():
     W = make_workload("pad", "decode", 4, 8, 2, 64, [50, 0, 17, 0], [1, 0, 1, 0])
     W_dec = make_workload("pad", "decode", 4, 8, 2, 64, [50, 0, 17, 0], [1, 0, 1, 0])
@@ -448,16 +475,19 @@ def test_extend_output_buffer_only_16_byte_aligned():
 
 
 @pytest.mark.parametrize("mode", ["decode", "verify"])
-def test_merge_of_more_than_32_splits(mode):
-    """One 100k-token request alone in the batch: the plan cuts its KV range
-    into hundreds of splits, so the merge runs its path for more than 32
-    partials per row."""
+def test_merge_at_the_split_cap(mode):
+    """One 100k-token request alone in the batch: the plan would cut its KV
+    range into hundreds of splits but stops at the cap of 24 per request (the
+    merge reads one split per lane), and the merge combines all of them."""
     if mode == "decode":
         W = make_workload("m32d", "decode", 1, 8, 1, 128, [100000], [1])
-        full_check(W)
+        d = full_check(W)
     else:
         W = make_workload("m32v", "verify", 1, 16, 1, 128, [100000], [5])
-        full_check(W, spec_mode=B.PKV_SPEC_PREFILL)
+        d = full_check(W, spec_mode=B.PKV_SPEC_PREFILL)
+    # the plan words open the workspace; word 5 counts the (request, split) items
+    plan = workspace_ints(d, d.attn.workspace.data_ptr(), 16)
+    assert plan[5] == 24
 
 
 def test_verify_prefill_path_long_context_split():
