@@ -26,7 +26,9 @@
  * Parity pins (checked by the CPU test suite): brute-force unpaged attention,
  * page-permutation invariance, page_size 1 vs 16, single key, uniform scores,
  * rows of weights summing to one, extend == stacked decodes, the LSE-merge
- * identity, the full E4M3 code table, metadata closed forms.
+ * identity, the full E4M3 code table, metadata closed forms; for tree masks,
+ * brute force and torch SDPA with the same mask, and a chain-shaped tree
+ * reproducing the causal result exactly.
  */
 #include <math.h>
 #include <pthread.h>
@@ -243,6 +245,7 @@ typedef struct {
   const int32_t* kv_indices;
   const int32_t* kv_last_page_len;
   const int32_t* qo_indptr;
+  const uint64_t* tree_mask; /* NULL: chain drafts (bottom-right causal) */
   double sm_scale, k_scale, v_scale;
   int64_t n_rows; /* number of (token, q-head) rows to compute */
   const int32_t* row_token; /* NULL: every row in token-major order */
@@ -269,8 +272,17 @@ static int kv_len_of(const attn_job* j, int b) {
 /* One output row: token t (global index into the packed query rows) and
  * query head h. Request b owns tokens qo_indptr[b] .. qo_indptr[b+1]-1; its
  * i-th new token sits at KV position P_b + i with P_b = L_b - qo_len_b, so it
- * sees keys 0 .. P_b + i (decode: qo_len 1, all L_b keys). GQA: query head h
- * reads KV head h / (num_q_heads / num_kv_heads). */
+ * sees keys 0 .. P_b + i (decode: qo_len 1, all L_b keys). With a tree mask
+ * (speculative drafts with top-k above 1) the row sees every key before P_b
+ * and, of the request's new tokens P_b + j, those whose bit j is set in
+ * tree_mask[t]; at most 64 new tokens per request. GQA: query head h reads KV
+ * head h / (num_q_heads / num_kv_heads). */
+static int key_visible(const uint64_t* tree_mask, uint64_t word, int p, int prefix, int limit) {
+  if (p > limit) return 0;
+  if (!tree_mask || p < prefix) return 1;
+  return (int)((word >> (p - prefix)) & 1u);
+}
+
 static int attention_row(const attn_job* j, int t, int h, double* scores, double* o, double* lse) {
   int D = j->head_dim;
   int b = 0;
@@ -281,17 +293,23 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
   int L = kv_len_of(j, b);
   int prefix = L - qo_len;
   if (L > 0 && prefix < 0) return ORACLE_ERR_ARG;
-  int limit = L > 0 ? prefix + i : -1; /* last visible key position */
+  if (j->tree_mask && qo_len > 64) return ORACLE_ERR_ARG;
+  /* last key position the row may see */
+  int limit = L > 0 ? (j->tree_mask ? L - 1 : prefix + i) : -1;
+  uint64_t word = j->tree_mask ? j->tree_mask[t] : 0;
+  int n_vis = 0;
+  for (int p = 0; p <= limit; ++p) n_vis += key_visible(j->tree_mask, word, p, prefix, limit);
   int g = h / (j->num_q_heads / j->num_kv_heads);
   const uint16_t* qrow = j->q + ((int64_t)t * j->num_q_heads + h) * D;
   for (int d = 0; d < D; ++d) o[d] = 0.0;
-  if (limit < 0) { /* no visible key: empty request (graph padding) */
+  if (n_vis == 0) { /* no visible key: empty request (graph padding) or an empty mask row */
     *lse = -INFINITY;
     return ORACLE_OK;
   }
-  /* scores s_j = sm_scale * sum_d q_d k_jd */
+  /* scores s_j = sm_scale * sum_d q_d k_jd over the visible keys */
   double m = -INFINITY;
   for (int p = 0; p <= limit; ++p) {
+    if (!key_visible(j->tree_mask, word, p, prefix, limit)) continue;
     int32_t page = j->kv_indices[j->kv_indptr[b] + p / j->page_size];
     int64_t slot = (int64_t)page * j->page_size + p % j->page_size;
     int64_t base = (slot * j->num_kv_heads + g) * D;
@@ -302,8 +320,10 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
   }
   /* softmax weights and weighted sum of V */
   double z = 0.0;
-  for (int p = 0; p <= limit; ++p) z += exp(scores[p] - m);
+  for (int p = 0; p <= limit; ++p)
+    if (key_visible(j->tree_mask, word, p, prefix, limit)) z += exp(scores[p] - m);
   for (int p = 0; p <= limit; ++p) {
+    if (!key_visible(j->tree_mask, word, p, prefix, limit)) continue;
     double w = exp(scores[p] - m) / z;
     int32_t page = j->kv_indices[j->kv_indptr[b] + p / j->page_size];
     int64_t slot = (int64_t)page * j->page_size + p % j->page_size;
@@ -341,11 +361,12 @@ static void* attention_worker(void* arg) {
 /* Attention for the requested rows. With row_token == NULL every row of the
  * batch is computed (n_rows must equal qo_indptr[bs] * num_q_heads) and the
  * outputs are laid out [token][q_head][head_dim] / [token][q_head]. Rows are
- * independent; threads take them round-robin. */
+ * independent; threads take them round-robin. tree_mask: NULL, or one word
+ * per query token (see attention_row). */
 int oracle_attention(int bs, int num_q_heads, int num_kv_heads, int head_dim, int page_size, int kv_dtype,
                      const uint16_t* q, const void* k_pool, const void* v_pool, const int32_t* kv_indptr,
                      const int32_t* kv_indices, const int32_t* kv_last_page_len, const int32_t* qo_indptr,
-                     double sm_scale, double k_scale, double v_scale, int64_t n_rows, const int32_t* row_token,
+                     const uint64_t* tree_mask, double sm_scale, double k_scale, double v_scale, int64_t n_rows, const int32_t* row_token,
                      const int32_t* row_head, double* out_o, double* out_lse, int nthreads) {
   if (bs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || page_size <= 0)
     return ORACLE_ERR_ARG;
@@ -366,6 +387,7 @@ int oracle_attention(int bs, int num_q_heads, int num_kv_heads, int head_dim, in
   job.kv_indices = kv_indices;
   job.kv_last_page_len = kv_last_page_len;
   job.qo_indptr = qo_indptr;
+  job.tree_mask = tree_mask;
   job.sm_scale = sm_scale;
   job.k_scale = k_scale;
   job.v_scale = v_scale;

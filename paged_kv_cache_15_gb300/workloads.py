@@ -65,6 +65,10 @@ class Workload:
     v_scale: float = 1.0
     sm_scale: float = 1.0
     extra: dict = field(default_factory=dict)
+    # draft-tree visibility (verify batches): None for chain drafts, else
+    # uint64 [T], bit j of token t's word = it sees the j-th new token of its
+    # request (every cached key stays visible)
+    tree_mask: Optional[np.ndarray] = None
 
     @property
     def num_slots(self) -> int:
@@ -101,6 +105,32 @@ def pool_bits(t: torch.Tensor) -> np.ndarray:
 
 def _randn_bf16(gen: torch.Generator, shape) -> torch.Tensor:
     return torch.randn(shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+
+
+def random_tree_masks(qo_lens, seed: int = 5) -> np.ndarray:
+    """Visibility words of random draft trees, one per query token.
+
+    In each request draft 0 hangs off the cached prefix and draft j > 0 off a
+    uniformly drawn earlier draft or, with probability 1/(j+1), off the prefix
+    as well; every draft sees itself and its ancestors.
+    """
+    rng = np.random.default_rng(seed)
+    words = []
+    for n in np.asarray(qo_lens, dtype=np.int64):
+        if n > 64:
+            raise ValueError("a draft tree holds at most 64 tokens")
+        mask = []
+        for j in range(int(n)):
+            parent = int(rng.integers(-1, j)) if j > 0 else -1
+            mask.append((1 << j) | (mask[parent] if parent >= 0 else 0))
+        words.extend(mask)
+    return np.array(words, dtype=np.uint64)
+
+
+def chain_tree_masks(qo_lens) -> np.ndarray:
+    """The visibility words of chain drafts: token i sees new tokens 0..i."""
+    return np.array([(1 << (i + 1)) - 1 for n in np.asarray(qo_lens, dtype=np.int64) for i in range(int(n))],
+                    dtype=np.uint64)
 
 
 def make_workload(name: str, mode: str, bs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

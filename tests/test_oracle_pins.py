@@ -13,7 +13,8 @@ import pytest
 import torch
 
 import oracle
-from paged_kv_cache_15_gb300.workloads import (Workload, bf16_bits, make_workload, pool_bits, preset)
+from paged_kv_cache_15_gb300.workloads import (Workload, bf16_bits, chain_tree_masks, make_workload, pool_bits,
+                                               preset, random_tree_masks)
 from tests._pipeline import oracle_meta, oracle_pools, oracle_reference
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -133,6 +134,87 @@ def test_p1_bruteforce_torch_sdpa_fp64(mode):
         scores = (qb @ Kt.transpose(1, 2)) * W.sm_scale
         ref_lse = torch.logsumexp(scores.masked_fill(~mask, -math.inf), dim=-1)  # [Hq, N]
         assert torch.allclose(torch.from_numpy(lse[qo_indptr[b]:qo_indptr[b + 1]]).T, ref_lse, atol=1e-12, rtol=0)
+
+
+# ---------------------------------------------------------------- P13 draft-tree masks
+def _tree_case(seed_shift=0, hq=4, hkv=2):
+    W = _tiny("extend", "bf16", seed_shift=seed_shift, hq=hq, hkv=hkv)
+    W.tree_mask = random_tree_masks(W.qo_lens, seed=11 + seed_shift)
+    return W
+
+
+def _tree_visible(W, b, i, t):
+    """Key positions row i of request b may see: the cached prefix, and the
+    drafts whose bit is set in its word."""
+    P, N = int(W.prefix_lens[b]), int(W.qo_lens[b])
+    word = int(W.tree_mask[t])
+    return list(range(P)) + [P + j for j in range(N) if (word >> j) & 1]
+
+
+def test_p13_tree_mask_bruteforce_loops():
+    W = _tree_case()
+    o, lse = oracle_reference(W)
+    q = _q64(W)
+    G = W.num_q_heads // W.num_kv_heads
+    qo_indptr = np.concatenate([[0], np.cumsum(W.qo_lens)])
+    kv = _contiguous_kv(W)
+    worst = 0.0
+    seen_branch = False
+    for b in range(W.bs):
+        K, V = kv[b]
+        for i in range(int(W.qo_lens[b])):
+            t = qo_indptr[b] + i
+            vis = _tree_visible(W, b, i, t)
+            seen_branch |= int(W.tree_mask[t]) != (1 << (i + 1)) - 1
+            for h in range(W.num_q_heads):
+                g = h // G
+                s_ = [W.sm_scale * sum(q[t, h, d] * K[p, g, d] for d in range(W.head_dim)) for p in vis]
+                m = max(s_)
+                e = [math.exp(x - m) for x in s_]
+                z = sum(e)
+                ref_o = [sum(e[k] * V[p, g, d] for k, p in enumerate(vis)) / z for d in range(W.head_dim)]
+                worst = max(worst, max(abs(a - r) for a, r in zip(o[t, h], ref_o)), abs(lse[t, h] - (m + math.log(z))))
+    assert seen_branch  # the drawn trees are not all chains
+    assert worst < 1e-12
+
+
+def test_p13_tree_mask_torch_sdpa_fp64():
+    W = _tree_case(seed_shift=2, hq=6, hkv=2)
+    o, lse = oracle_reference(W)
+    q = torch.from_numpy(_q64(W))
+    G = W.num_q_heads // W.num_kv_heads
+    qo_indptr = np.concatenate([[0], np.cumsum(W.qo_lens)])
+    for b, (K, V) in enumerate(_contiguous_kv(W)):
+        L, N = int(W.seq_lens[b]), int(W.qo_lens[b])
+        mask = torch.zeros((N, L), dtype=torch.bool)
+        for i in range(N):
+            mask[i, _tree_visible(W, b, i, qo_indptr[b] + i)] = True
+        qb = q[qo_indptr[b]:qo_indptr[b + 1]].transpose(0, 1)
+        Kt = torch.from_numpy(K).transpose(0, 1).repeat_interleave(G, dim=0)
+        Vt = torch.from_numpy(V).transpose(0, 1).repeat_interleave(G, dim=0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qb, Kt, Vt, attn_mask=mask, scale=W.sm_scale)
+        got = torch.from_numpy(o[qo_indptr[b]:qo_indptr[b + 1]]).transpose(0, 1)
+        assert torch.allclose(got, ref, atol=1e-12, rtol=0)
+        scores = (qb @ Kt.transpose(1, 2)) * W.sm_scale
+        ref_lse = torch.logsumexp(scores.masked_fill(~mask, -math.inf), dim=-1)
+        assert torch.allclose(torch.from_numpy(lse[qo_indptr[b]:qo_indptr[b + 1]]).T, ref_lse, atol=1e-12, rtol=0)
+
+
+def test_p13_chain_shaped_tree_equals_causal():
+    W = _tiny("extend", "bf16", seed_shift=5)
+    o0, l0 = oracle_reference(W)
+    W.tree_mask = chain_tree_masks(W.qo_lens)
+    o1, l1 = oracle_reference(W)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def test_p13_tree_of_more_than_64_drafts_rejected():
+    W = make_workload("t65", "verify", 1, 2, 1, 8, [3], [65], page_size=4)
+    W.tree_mask = np.full(65, np.uint64(1))
+    with pytest.raises(ValueError):
+        oracle_reference(W)
+    with pytest.raises(ValueError):
+        random_tree_masks([65])
 
 
 # ---------------------------------------------------------------- P2 / P3 layout invariance
