@@ -274,9 +274,11 @@ static int kv_len_of(const attn_job* j, int b) {
  * i-th new token sits at KV position P_b + i with P_b = L_b - qo_len_b, so it
  * sees keys 0 .. P_b + i (decode: qo_len 1, all L_b keys). With a tree mask
  * (speculative drafts with top-k above 1) the row sees every key before P_b
- * and, of the request's new tokens P_b + j, those whose bit j is set in
- * tree_mask[t]; at most 64 new tokens per request. GQA: query head h reads KV
- * head h / (num_q_heads / num_kv_heads). */
+ * and, of the request's new tokens P_b + j with j <= i, those whose bit j is
+ * set in tree_mask[t]: drafts are ordered with every ancestor before its
+ * descendants, so bits above the row's own index are ignored. At most 64 new
+ * tokens per request. GQA: query head h reads KV head h / (num_q_heads /
+ * num_kv_heads). */
 static int key_visible(const uint64_t* tree_mask, uint64_t word, int p, int prefix, int limit) {
   if (p > limit) return 0;
   if (!tree_mask || p < prefix) return 1;
@@ -294,8 +296,7 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
   int prefix = L - qo_len;
   if (L > 0 && prefix < 0) return ORACLE_ERR_ARG;
   if (j->tree_mask && qo_len > 64) return ORACLE_ERR_ARG;
-  /* last key position the row may see */
-  int limit = L > 0 ? (j->tree_mask ? L - 1 : prefix + i) : -1;
+  int limit = L > 0 ? prefix + i : -1; /* last key position the row may see */
   uint64_t word = j->tree_mask ? j->tree_mask[t] : 0;
   int n_vis = 0;
   for (int p = 0; p <= limit; ++p) n_vis += key_visible(j->tree_mask, word, p, prefix, limit);

@@ -145,10 +145,10 @@ def _tree_case(seed_shift=0, hq=4, hkv=2):
 
 def _tree_visible(W, b, i, t):
     """Key positions row i of request b may see: the cached prefix, and the
-    drafts whose bit is set in its word."""
-    P, N = int(W.prefix_lens[b]), int(W.qo_lens[b])
+    drafts up to its own index whose bit is set in its word."""
+    P = int(W.prefix_lens[b])
     word = int(W.tree_mask[t])
-    return list(range(P)) + [P + j for j in range(N) if (word >> j) & 1]
+    return list(range(P)) + [P + j for j in range(i + 1) if (word >> j) & 1]
 
 
 def test_p13_tree_mask_bruteforce_loops():
@@ -204,6 +204,16 @@ def test_p13_chain_shaped_tree_equals_causal():
     W = _tiny("extend", "bf16", seed_shift=5)
     o0, l0 = oracle_reference(W)
     W.tree_mask = chain_tree_masks(W.qo_lens)
+    o1, l1 = oracle_reference(W)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def test_p13_bits_above_own_index_ignored():
+    """Drafts are ordered parents first, so a row never sees a later draft:
+    an all-ones mask is the causal (chain) result."""
+    W = _tiny("extend", "bf16", seed_shift=6)
+    o0, l0 = oracle_reference(W)
+    W.tree_mask = np.full(W.total_q, np.uint64(0xFFFFFFFFFFFFFFFF))
     o1, l1 = oracle_reference(W)
     assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
 
