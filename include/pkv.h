@@ -70,6 +70,7 @@ extern "C" {
 #define PKV_DEV_CAPACITY 3     /* total pages / query rows beyond the configured capacity */
 #define PKV_DEV_BAD_SLOT 4     /* set_kv_buffer loc outside [0, num_pages * page_size) */
 #define PKV_DEV_QO_TOO_LONG 5  /* decode path: qo_len beyond config.max_qo_len */
+#define PKV_DEV_TREE_TOO_LONG 6 /* draft-tree mask set and a request has more than 64 new tokens */
 
 /* ---- enumerations -------------------------------------------------------- */
 /* ForwardMode of the batch ("[SGLang] Hybrid Attention", section
@@ -180,6 +181,9 @@ int pkv_set_kv_buffer(pkv_ctx* ctx, void* d_k_pool, void* d_v_pool, const int32_
  * d_q: bf16 [T][num_q_heads][head_dim] (T = sum of qo_len), d_out: bf16 of the
  * same shape, d_lse: fp32 [T][num_q_heads] or NULL. k_scale / v_scale multiply
  * E4M3 codes (ignored for bf16 pools). Pointers must be 16-byte aligned.
+ * sm_scale must be positive and finite, and so must k_scale and v_scale with
+ * an E4M3 pool (INVALID_ARG otherwise). Verify batches follow the draft-tree
+ * mask when one is set (pkv_set_tree_mask).
  * Errors: INVALID_ARG, UNSUPPORTED (group size with max_qo_len beyond one
  * 128-row tile), CUDA. */
 int pkv_forward_decode(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, const void* d_v_pool, float sm_scale,
@@ -199,6 +203,26 @@ int pkv_forward_extend(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, cons
 int pkv_forward(pkv_ctx* ctx, int forward_mode, int spec_mode, const void* d_q, const void* d_k_pool,
                 const void* d_v_pool, float sm_scale, float k_scale, float v_scale, void* d_out, float* d_lse,
                 void* stream);
+
+/* Draft trees for target verify (speculative decoding with top-k above 1;
+ * "--attention-backend", sections "The obvious fix, and why it fails" and
+ * "Our position" name it as a feature that limits which backends can run).
+ * The pages give no mask format; this library's reading:
+ *   d_tree_mask: device uint64 [total query tokens], in qo_indptr order. Bit j
+ *   of token t's word lets t attend the j-th new (draft) token of its own
+ *   request, at KV position seq_len - qo_len + j; every earlier (cached) key
+ *   stays visible. Drafts are ordered with every ancestor before its
+ *   descendants, so bits above the token's own index are ignored (a draft
+ *   never sees a later one). A request may have at most 64 new tokens while a mask is
+ *   set; a longer one records PKV_DEV_TREE_TOO_LONG and its rows see no draft
+ *   past the 64th. NULL (the default) means chain drafts: token i sees new
+ *   tokens 0..i, the bottom-right causal rule.
+ * The mask applies to the forwards that follow a metadata build in
+ * TARGET_VERIFY or DRAFT_EXTEND mode, on both paths; EXTEND and DECODE batches
+ * ignore it. The caller owns the buffer and keeps it alive (with its contents
+ * for the step) until those forwards have run; the context keeps the pointer,
+ * so a captured graph replays with whatever the buffer holds then. */
+int pkv_set_tree_mask(pkv_ctx* ctx, const uint64_t* d_tree_mask);
 
 /* Synchronise `stream`, read the device error word into *code (PKV_DEV_*) and
  * clear it. Returns PKV_ERR_DEVICE when *code != PKV_DEV_OK. */

@@ -19,7 +19,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CAPACITY, PKV_ERR_CUDA, PKV_ERR_DEVICE = range(6)
-PKV_DEV_OK, PKV_DEV_BAD_LENGTH, PKV_DEV_BAD_PAGE, PKV_DEV_CAPACITY, PKV_DEV_BAD_SLOT, PKV_DEV_QO_TOO_LONG = range(6)
+(PKV_DEV_OK, PKV_DEV_BAD_LENGTH, PKV_DEV_BAD_PAGE, PKV_DEV_CAPACITY, PKV_DEV_BAD_SLOT, PKV_DEV_QO_TOO_LONG,
+ PKV_DEV_TREE_TOO_LONG) = range(7)
 PKV_MODE_EXTEND, PKV_MODE_DECODE, PKV_MODE_IDLE, PKV_MODE_TARGET_VERIFY, PKV_MODE_DRAFT_EXTEND = range(5)
 PKV_SPEC_PREFILL, PKV_SPEC_DECODE = 0, 1
 PKV_PATH_INVALID, PKV_PATH_DECODE, PKV_PATH_EXTEND = -1, 0, 1
@@ -29,7 +30,7 @@ PKV_KV_BF16, PKV_KV_FP8_E4M3 = 0, 1
 EXPORTS = ("pkv_status_string", "pkv_workspace_bytes", "pkv_pool_bytes", "pkv_create", "pkv_destroy",
            "pkv_select_backend", "pkv_build_metadata", "pkv_get_metadata", "pkv_set_kv_buffer",
            "pkv_forward_decode", "pkv_forward_extend", "pkv_forward", "pkv_get_device_error", "pkv_describe",
-           "pkv_forward_decode_static")
+           "pkv_forward_decode_static", "pkv_set_tree_mask")
 
 
 class PkvError(RuntimeError):
@@ -77,6 +78,7 @@ def lib():
                                                   vp, vp, vp]),
             "pkv_forward": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_float,
                                            ctypes.c_float, ctypes.c_float, vp, vp, vp]),
+            "pkv_set_tree_mask": (ctypes.c_int, [vp, vp]),
             "pkv_get_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), vp]),
             "pkv_describe": (ctypes.c_int, [vp, ctypes.c_char_p, sz]),
             "pkv_forward_decode_static": (ctypes.c_int, [cfgp, i32, vp, vp, i32, vp, vp, vp, ctypes.c_float,
@@ -185,6 +187,12 @@ def pkv_forward(ctx, forward_mode, spec_mode, q, k_pool, v_pool, sm_scale, out, 
     _check(lib().pkv_forward(ctx, int(forward_mode), int(spec_mode), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                              float(sm_scale), float(k_scale), float(v_scale), _ptr(out), _ptr(lse),
                              _stream(stream)), "pkv_forward")
+
+
+def pkv_set_tree_mask(ctx, tree_mask) -> None:
+    """Draft-tree mask words (uint64 device tensor, one per query token) for
+    the verify forwards that follow, or None for chain drafts."""
+    _check(lib().pkv_set_tree_mask(ctx, _ptr(tree_mask)), "pkv_set_tree_mask")
 
 
 def pkv_get_device_error(ctx, stream=None) -> int:

@@ -88,6 +88,7 @@ struct DecodeArgs {
   int num_q_heads, num_kv_heads, group;
   float scale_log2;  // sm_scale * k_scale * log2(e)
   float v_scale;     // multiplies the output (E4M3 pools), 1 for bf16
+  const uint64_t* tree;  // draft-tree mask word per query token, or null (chain drafts)
 };
 
 // Byte offset of (row, 16-byte chunk) inside a swizzled [rows][128 B] column block.
@@ -354,6 +355,18 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
       for (int j = 0; j < RT; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) lim[j][e] = prefix + min((8 * j + 2 * t4 + e) / G, qo - 1);
+      // draft trees: a row's mask word clears the drafts outside its tree (the
+      // causal limit above still bounds it)
+      const bool tree = a.tree != nullptr;
+      uint64_t tw[RT][2];
+#pragma unroll
+      for (int j = 0; j < RT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = 8 * j + 2 * t4 + e;
+          tw[j][e] = (tree && r < rows_valid) ? a.tree[q0 + r / G] : ~0ull;
+        }
+      if (tree && qo > 64 && lane == 0 && wk == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
 
       // Q^T fragments (B operand): column g8 of row tile j is query row 8j + g8
       uint32_t qf[D / 16][RT][2];
@@ -470,6 +483,19 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
               }
             }
             // ---- mask, online softmax over the 16 keys (log2 domain) ----
+            if (tree && abs0 + 15 >= prefix) {
+              // the block reaches the drafts: raw scores of drafts outside a
+              // row's tree to -inf (the scale below is positive)
+#pragma unroll
+              for (int j = 0; j < RT; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int dj = abs0 + g8 + 8 * h - prefix;
+#pragma unroll
+                  for (int e = 0; e < 2; ++e)
+                    if (dj >= 0 && !(dj < 64 && ((tw[j][e] >> dj) & 1ull))) s[j][2 * h + e] = -INFINITY;
+                }
+            }
             float al[RT][2];
             bool rescale = false;
 #pragma unroll
@@ -685,6 +711,11 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
       const int lim_b = prefix + min(rb / G, qo - 1);
       const long long qrow_a = ((long long)(q0 + ra / G) * a.num_q_heads + g * G + ra % G) * D;
       const long long qrow_b = ((long long)(q0 + rb / G) * a.num_q_heads + g * G + rb % G) * D;
+      // draft trees: each row's mask word clears the drafts outside its tree
+      const bool tree = a.tree != nullptr;
+      const uint64_t tw_a = (tree && va) ? a.tree[q0 + ra / G] : ~0ull;
+      const uint64_t tw_b = (tree && vb) ? a.tree[q0 + rb / G] : ~0ull;
+      if (tree && qo > 64 && lane == 0 && cw == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
 
       // Q fragments (A operand), D/16 k-steps x 4 registers
       uint32_t qf[D / 16][4];
@@ -790,6 +821,18 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
               }
             }
             // ---- mask, online softmax (log2 domain) ----
+            if (tree && abs0 + 15 >= prefix) {
+              // the block reaches the drafts: raw scores of drafts outside a
+              // row's tree to -inf (the scale below is positive)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int dj = abs0 + nt * 8 + 2 * qd + e - prefix;
+                  if (dj >= 0 && !(dj < 64 && ((tw_a >> dj) & 1ull))) s[nt][e] = -INFINITY;
+                  if (dj >= 0 && !(dj < 64 && ((tw_b >> dj) & 1ull))) s[nt][2 + e] = -INFINITY;
+                }
+            }
             float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -1002,6 +1045,7 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
   a.scale_log2 = sm_scale * (fp8 ? k_scale : 1.f) * kLog2e;
   a.v_scale = fp8 ? v_scale : 1.f;
+  a.tree = active_tree(c);
   cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
@@ -1094,6 +1138,7 @@ int launch_split_merge(Ctx& c, void* out, float* lse, int max_rows_per_head, boo
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
   a.scale_log2 = 0.f;
   a.v_scale = 1.f;
+  a.tree = nullptr;
   // one warp per (token, head) row, 8 warps per CTA, 3 CTAs per SM
   const long long rows = (long long)c.cfg.max_q_tokens * c.cfg.num_q_heads;
   const long long grid = std::min<long long>((rows + 7) / 8, (long long)c.num_sms * 3);

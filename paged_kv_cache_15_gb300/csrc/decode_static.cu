@@ -14,6 +14,8 @@
 // their scratch lives differs.
 #include <mutex>
 
+#include <cmath>
+
 #include "pkv_internal.cuh"
 
 namespace pkv {
@@ -67,6 +69,11 @@ extern "C" int pkv_forward_decode_static(const pkv_config* cfg, int32_t batch, c
   if (!a16(d_q) || !a16(d_k_pool) || !a16(d_v_pool) || !a16(d_out)) return PKV_ERR_INVALID_ARG;
   if (d_lse && (reinterpret_cast<uintptr_t>(d_lse) & 3)) return PKV_ERR_INVALID_ARG;
   if (d_error && (reinterpret_cast<uintptr_t>(d_error) & 3)) return PKV_ERR_INVALID_ARG;
+  // masked scores become -inf before the scale multiplies them: it must be positive
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return PKV_ERR_INVALID_ARG;
+  if (cfg->kv_dtype == PKV_KV_FP8_E4M3 &&
+      (!(k_scale > 0.f) || !std::isfinite(k_scale) || !(v_scale > 0.f) || !std::isfinite(v_scale)))
+    return PKV_ERR_INVALID_ARG;
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;

@@ -81,6 +81,31 @@ __device__ __forceinline__ void st_global_32B(void* p, const uint32_t* v) {
                : "memory");
 }
 
+// Visibility of the 32 keys key_base .. key_base + 31 for a row of a
+// draft-tree batch, one bit each: keys up to the row's limit, less the drafts
+// (keys from draft0 on) whose bit is clear in the row's tree word.
+__device__ __forceinline__ uint32_t visible32(int key_base, int limit, int draft0, uint64_t word) {
+  const int n = limit - key_base + 1;  // keys within the limit
+  const uint32_t v = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+  const int off = key_base - draft0;  // draft index of the first key
+  uint32_t t;
+  if (off >= 64)
+    t = 0u;
+  else if (off >= 0)
+    t = (uint32_t)(word >> off);
+  else if (off > -32)
+    t = (uint32_t)(word << (-off)) | ((1u << (-off)) - 1u);
+  else
+    t = 0xffffffffu;
+  return v & t;
+}
+
+// Raw scores of the keys whose bit is clear in vis to -inf.
+__device__ __forceinline__ void mask32_bits(uint32_t* sr, uint32_t vis) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) sr[c] = (vis >> c) & 1u ? sr[c] : kNegInfBits;
+}
+
 // Masks raw scores of keys past the row's limit (sets them to -inf).
 __device__ __forceinline__ void mask32(uint32_t* sr, int key_base, int limit) {
 #pragma unroll
@@ -187,9 +212,12 @@ struct ExtendArgs {
   int q_tma;         // 1 when the group divides 128: a Q tile is one TMA box of 128/G tokens x G heads
   int q_box_tokens;  // 128 / group
   int out_32B;       // out is 32-byte aligned: output rows are written with 32-byte stores
+  const uint64_t* tree;  // draft-tree mask word per query token, or null (chain drafts)
 };
 
-template <class C>
+// TREE: verify batches with draft-tree mask words (a separate instantiation,
+// so batches without a tree run the plain causal masking).
+template <class C, bool TREE>
 __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                    const __grid_constant__ CUtensorMap tmap_v,
                                                                    const __grid_constant__ CUtensorMap tmap_q,
@@ -545,6 +573,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       const bool valid = R < qo * G;
       const int tok = min(R / G, qo - 1);
       const int limit = L - qo + tok;
+      // draft trees: the row's mask word clears the drafts outside its tree
+      uint64_t tword = ~0ull;
+      int draft0 = 0x3fffffff;  // first draft key (none without a tree)
+      if constexpr (TREE) {
+        tword = valid ? a.tree[q0 + R / G] : ~0ull;
+        draft0 = L - qo;
+        if (qo > 64 && r == 0 && x == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
+      }
       const long long orow = (long long)(q0 + R / G) * a.num_q_heads + g * G + R % G;
       // split units write bf16 partial rows (normalised output) and fp32 LSE that
       // the merge kernel combines across the request's splits
@@ -611,7 +647,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         }
         tc_fence_after();
         const int key0 = j * kExtendKeys;
-        const bool diag = key0 + kExtendKeys - 1 > limit;  // some keys of this tile are masked for this row
+        // some keys of this tile are masked for this row: past its limit, or
+        // drafts that its tree may hide
+        const bool diag = key0 + kExtendKeys - 1 > limit || (TREE && key0 + kExtendKeys > draft0);
         // the request's last page inside this KV tile: zero the V rows past L
         // (done by the first tile that reads this V tile, before its PV)
         if ((ukv.dual || x == 0 || jr >= nA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
@@ -640,8 +678,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           tmem_ld32(lane_base + s_col + cc * 32 + 32, sr + 32);
           tmem_wait_ld();
           if (diag) {
-            mask32(sr, key0 + cc * 32, limit);
-            mask32(sr + 32, key0 + cc * 32 + 32, limit);
+            if constexpr (TREE) {
+              mask32_bits(sr, visible32(key0 + cc * 32, limit, draft0, tword));
+              mask32_bits(sr + 32, visible32(key0 + cc * 32 + 32, limit, draft0, tword));
+            } else {
+              mask32(sr, key0 + cc * 32, limit);
+              mask32(sr + 32, key0 + cc * 32 + 32, limit);
+            }
           }
         };
         // P of the tile against the reference; returns the tile's row sum
@@ -848,6 +891,7 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
   a.scale_log2 = sm_scale * kLog2e;
   a.out_32B = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
+  a.tree = active_tree(c);
   // Q as [tokens][heads][head_dim]: a box of 64 elements x G heads x 128/G
   // tokens is one 128-row tile column block, rows ordered (token, head) like
   // the tile's rows. The token extent only bounds the map; the kernel loads a
@@ -867,11 +911,10 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
     a.q_tma = 1;
     a.q_box_tokens = (int)box_tok;
   }
-  if (cudaFuncSetAttribute(extend_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-      cudaSuccess)
+  auto kernel = a.tree ? extend_tc_kernel<C, true> : extend_tc_kernel<C, false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return PKV_ERR_CUDA;
-  if (launch_pdl(extend_tc_kernel<C>, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, tq, a) !=
-      cudaSuccess)
+  if (launch_pdl(kernel, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, tq, a) != cudaSuccess)
     return PKV_ERR_CUDA;
   // requests whose rows fit one unit were split along their KV range
   return launch_split_merge(c, out, lse, kExtendUnitRows, true, st);

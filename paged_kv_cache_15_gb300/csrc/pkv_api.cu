@@ -1,9 +1,11 @@
 // Host side of the C ABI declared in include/pkv.h: argument checks, the
 // workspace layout, context lifetime, ForwardMode dispatch and launches.
+#include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
+#include <cmath>
 #include <new>
 
 #include "pkv_internal.cuh"
@@ -120,6 +122,16 @@ int get_encoder() {
       q != cudaDriverEntryPointSuccess || !fn)
     return PKV_ERR_CUDA;
   g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return PKV_OK;
+}
+
+// Masked scores become -inf before the scale multiplies them: the scales
+// must be positive (k_scale and v_scale matter only for E4M3 pools).
+int check_scales(const Ctx& c, float sm_scale, float k_scale, float v_scale) {
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return PKV_ERR_INVALID_ARG;
+  if (c.cfg.kv_dtype == PKV_KV_FP8_E4M3 &&
+      (!(k_scale > 0.f) || !std::isfinite(k_scale) || !(v_scale > 0.f) || !std::isfinite(v_scale)))
+    return PKV_ERR_INVALID_ARG;
   return PKV_OK;
 }
 
@@ -332,6 +344,8 @@ int pkv_forward_decode(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, cons
                        float k_scale, float v_scale, void* d_out, float* d_lse, void* stream) {
   int st = check_forward_args(ctx, d_q, d_k_pool, d_v_pool, d_out, d_lse);
   if (st != PKV_OK) return st;
+  st = check_scales(*ctx, sm_scale, k_scale, v_scale);
+  if (st != PKV_OK) return st;
   if (ctx->batch == 0) return PKV_OK;
   return launch_decode(*ctx, d_q, d_k_pool, d_v_pool, sm_scale, k_scale, v_scale, d_out, d_lse,
                        static_cast<cudaStream_t>(stream));
@@ -342,6 +356,8 @@ int pkv_forward_extend(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, cons
   (void)k_scale;
   (void)v_scale;
   int st = check_forward_args(ctx, d_q, d_k_pool, d_v_pool, d_out, d_lse);
+  if (st != PKV_OK) return st;
+  st = check_scales(*ctx, sm_scale, k_scale, v_scale);
   if (st != PKV_OK) return st;
   if (ctx->cfg.kv_dtype != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
   if (ctx->batch == 0) return PKV_OK;
@@ -359,6 +375,13 @@ int pkv_forward(pkv_ctx* ctx, int forward_mode, int spec_mode, const void* d_q, 
   if (path == PKV_PATH_DECODE)
     return pkv_forward_decode(ctx, d_q, d_k_pool, d_v_pool, sm_scale, k_scale, v_scale, d_out, d_lse, stream);
   return pkv_forward_extend(ctx, d_q, d_k_pool, d_v_pool, sm_scale, k_scale, v_scale, d_out, d_lse, stream);
+}
+
+int pkv_set_tree_mask(pkv_ctx* ctx, const uint64_t* d_tree_mask) {
+  if (!ctx) return PKV_ERR_INVALID_ARG;
+  if (d_tree_mask && (reinterpret_cast<uintptr_t>(d_tree_mask) & 7u) != 0) return PKV_ERR_INVALID_ARG;
+  ctx->tree = d_tree_mask;
+  return PKV_OK;
 }
 
 int pkv_get_device_error(pkv_ctx* ctx, int32_t* code, void* stream) {

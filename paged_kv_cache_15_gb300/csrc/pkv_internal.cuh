@@ -89,7 +89,13 @@ struct Ctx {
   int mode;
   bool qo_given;  // last build had explicit qo_lens
   int device;
+  const uint64_t* tree = nullptr;  // draft-tree mask words (pkv_set_tree_mask), or null
 };
+
+// The tree mask the next forward applies: only after a build in a verify mode.
+inline const uint64_t* active_tree(const Ctx& c) {
+  return (c.mode == PKV_MODE_TARGET_VERIFY || c.mode == PKV_MODE_DRAFT_EXTEND) ? c.tree : nullptr;
+}
 
 // Device-side view of the metadata in the workspace.
 struct Meta {

@@ -46,6 +46,11 @@ class DeviceBatch:
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty((W.total_q, W.num_q_heads), dtype=torch.float32, device=dev)
         self.mode = MODE_OF[W.mode]
+        # draft-tree mask words (uint64, carried as int64 bits)
+        self.tree = None
+        if W.tree_mask is not None:
+            self.tree = torch.from_numpy(W.tree_mask.view("int64").copy()).to(dev)
+            B.pkv_set_tree_mask(self.ctx, self.tree)
 
     @property
     def ctx(self):

@@ -12,7 +12,7 @@ import torch
 import oracle
 from paged_kv_cache_15_gb300 import binding as B
 from paged_kv_cache_15_gb300.runner import DeviceBatch, config_for
-from paged_kv_cache_15_gb300.workloads import make_workload, pool_bits, preset
+from paged_kv_cache_15_gb300.workloads import chain_tree_masks, make_workload, pool_bits, preset, random_tree_masks
 from tests._pipeline import oracle_meta, oracle_pools, oracle_reference, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -448,6 +448,111 @@ def test_extend_graph_replay():
     ref_o, ref_lse = oracle_reference(W)
     check_close(d.out.double().cpu().numpy(), ref_o, "o (graph)")
     check_close(d.lse.double().cpu().numpy(), ref_lse, "lse (graph)")
+
+
+@pytest.mark.parametrize("spec", ["prefill", "decode"])
+def test_draft_extend_mode_both_paths(spec):
+    """DRAFT_EXTEND is routed like TARGET_VERIFY (by the speculative attention
+    mode) and computes the same bottom-right causal attention over the drafts."""
+    W = make_workload("dx", "verify", 5, 16, 4, 128, [700, 0, 2100, 33, 1500], [3, 1, 4, 2, 4])
+    sm = B.PKV_SPEC_PREFILL if spec == "prefill" else B.PKV_SPEC_DECODE
+    assert B.pkv_select_backend(B.PKV_MODE_DRAFT_EXTEND, sm) == (B.PKV_PATH_EXTEND if spec == "prefill" else B.PKV_PATH_DECODE)
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    d.build_metadata(mode=B.PKV_MODE_DRAFT_EXTEND)
+    d.forward(sm, mode=B.PKV_MODE_DRAFT_EXTEND)
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    ref_o, ref_lse = oracle_reference(W)
+    check_close(d.out.double().cpu().numpy(), ref_o, "o")
+    check_close(d.lse.double().cpu().numpy(), ref_lse, "lse")
+
+
+def test_prefill_chunks_and_decode_rows_in_one_extend_call():
+    """A mixed batch on the extend path: prefill chunks of hundreds of tokens
+    next to one-token (decode) requests and short chunks, with and without a
+    cached prefix."""
+    W = make_workload("mix", "extend", 7, 32, 8, 128, [0, 900, 3000, 40, 0, 1200, 5000], [300, 1, 1, 77, 1, 2, 1])
+    full_check(W)
+
+
+# ------------------------------------------------------------------ draft trees
+def _tree_verify(name, bs, hq, hkv, d, max_drafts, seed, kv_dtype="bf16"):
+    rng = np.random.default_rng(seed)
+    W = make_workload(name, "verify", bs, hq, hkv, d, rng.integers(0, 1500, bs),
+                      rng.integers(1, max_drafts + 1, bs), kv_dtype=kv_dtype)
+    W.tree_mask = random_tree_masks(W.qo_lens, seed=seed)
+    return W
+
+
+@pytest.mark.parametrize("case", ["g16", "g4_d64", "g4_32_drafts", "g8_fp8"])
+@pytest.mark.parametrize("spec", ["prefill", "decode"])
+def test_tree_verify_parity(case, spec):
+    """Target verify with random draft trees (each draft sees the cached
+    prefix, its ancestors and itself) on both paths."""
+    if case == "g16":
+        W = _tree_verify("tv16", 6, 32, 2, 128, 8, 41)
+    elif case == "g4_d64":
+        W = _tree_verify("tv4", 5, 16, 4, 64, 8, 42)
+    elif case == "g4_32_drafts":
+        W = _tree_verify("tv32", 4, 16, 4, 128, 32, 43)
+    else:
+        if spec == "prefill":
+            pytest.skip("E4M3 pools run on the decode path only")
+        W = _tree_verify("tv8f", 4, 32, 4, 128, 16, 44, kv_dtype="fp8_e4m3")
+    full_check(W, spec_mode=B.PKV_SPEC_PREFILL if spec == "prefill" else B.PKV_SPEC_DECODE)
+
+
+@pytest.mark.parametrize("spec", ["prefill", "decode"])
+def test_chain_tree_matches_no_tree(spec):
+    """A chain-shaped tree gives the causal result of a batch without a mask."""
+    W = _tree_verify("tvc", 5, 32, 2, 128, 8, 45)
+    W.tree_mask = None
+    sm = B.PKV_SPEC_PREFILL if spec == "prefill" else B.PKV_SPEC_DECODE
+    plain = run_path(W, sm)
+    W.tree_mask = chain_tree_masks(W.qo_lens)
+    chain = run_path(W, sm)
+    assert torch.equal(plain.out, chain.out)
+    assert torch.equal(plain.lse, chain.lse)
+
+
+def test_tree_mask_ignored_by_extend_batches():
+    """The mask applies to verify batches only: an EXTEND batch stays causal."""
+    W = make_workload("tve", "extend", 3, 16, 4, 128, [300, 0, 1000], [40, 9, 3])
+    W.tree_mask = random_tree_masks(W.qo_lens, seed=46)
+    d = run_path(W)
+    W.tree_mask = None
+    ref_o, ref_lse = oracle_reference(W)
+    check_close(d.out.double().cpu().numpy(), ref_o, "o")
+    check_close(d.lse.double().cpu().numpy(), ref_lse, "lse")
+
+
+def test_tree_of_more_than_64_drafts_recorded():
+    W = make_workload("tv65", "verify", 2, 8, 2, 128, [100, 50], [65, 3])
+    W.tree_mask = np.concatenate([np.full(65, np.uint64(0xFFFFFFFFFFFFFFFF)), chain_tree_masks([3])])
+    d = DeviceBatch(W)
+    d.step(B.PKV_SPEC_PREFILL)
+    torch.cuda.synchronize()
+    assert d.device_error() == B.PKV_DEV_TREE_TOO_LONG
+    assert torch.isfinite(d.out.float()).all()
+
+
+def test_non_positive_scales_rejected():
+    W = preset("tiny_decode")
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    d.build_metadata()
+    for bad in (0.0, -0.125, float("nan"), float("inf")):
+        with pytest.raises(B.PkvError) as e:
+            B.pkv_forward(d.ctx, d.mode, B.PKV_SPEC_PREFILL, d.q, d.k_pool, d.v_pool, bad, d.out, d.lse)
+        assert e.value.status == B.PKV_ERR_INVALID_ARG
+    Wf = preset("long_fp8_decode", bs=2, len_scale=1 / 64)
+    df = DeviceBatch(Wf)
+    df.set_kv_buffer()
+    df.build_metadata()
+    with pytest.raises(B.PkvError):
+        B.pkv_forward(df.ctx, df.mode, B.PKV_SPEC_PREFILL, df.q, df.k_pool, df.v_pool, Wf.sm_scale, df.out,
+                      df.lse, 0.0, Wf.v_scale)
 
 
 def test_extend_mixed_split_and_unsplit_requests():
