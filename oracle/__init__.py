@@ -88,7 +88,7 @@ def _load():
         lib.oracle_lse_merge.restype = None
         lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]
         lib.oracle_attention.restype = ctypes.c_int
-        lib.oracle_attention.argtypes = [ctypes.c_int] * 6 + [vp, vp, vp, i32p, i32p, i32p, i32p, vp,
+        lib.oracle_attention.argtypes = [ctypes.c_int] * 6 + [vp, vp, vp, i32p, i32p, i32p, i32p, vp, vp,
                                                                ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                                                ctypes.c_int64, i32p, i32p, vp, vp, ctypes.c_int]
         lib.oracle_pool_bytes.restype = ctypes.c_int64
@@ -183,7 +183,7 @@ def lse_merge(o_parts, lse_parts):
 
 
 def attention(q, k_pool, v_pool, meta, num_q_heads, num_kv_heads, page_size, sm_scale, kv_dtype=KV_BF16,
-              k_scale=1.0, v_scale=1.0, rows=None, nthreads=None, tree_mask=None):
+              k_scale=1.0, v_scale=1.0, rows=None, nthreads=None, tree_mask=None, sinks=None):
     """fp64 attention over the paged pool.
 
     q: uint16 bf16 bits [T, Hq, D]; pools: uint16 / uint8 [slots, Hkv, D];
@@ -192,6 +192,8 @@ def attention(q, k_pool, v_pool, meta, num_q_heads, num_kv_heads, page_size, sm_
     pairs — returns o [n, D], lse [n]. tree_mask: None (chain drafts,
     bottom-right causal) or uint64 [T]: bit j of token t's word lets it see
     the j-th new token of its request (every cached key stays visible).
+    sinks: None or float [Hq], each head's sink logit (a key with that score
+    and a zero value vector).
     """
     lib = _load()
     q = np.ascontiguousarray(q, dtype=np.uint16)
@@ -219,8 +221,12 @@ def attention(q, k_pool, v_pool, meta, num_q_heads, num_kv_heads, page_size, sm_
     tm = None if tree_mask is None else np.ascontiguousarray(tree_mask, dtype=np.uint64)
     if tm is not None:
         assert tm.shape == (T,)
+    sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float64)
+    if sk is not None:
+        assert sk.shape == (hq,)
     st = lib.oracle_attention(bs, hq, num_kv_heads, d, page_size, int(kv_dtype), _ptr(q), _ptr(k_pool),
                               _ptr(v_pool), kvp_p, kvi_p, last_p, qoi_p, None if tm is None else _ptr(tm),
+                              None if sk is None else _ptr(sk),
                               float(sm_scale), float(k_scale),
                               float(v_scale), n_rows, rt_p, rh_p, _ptr(out_o), _ptr(out_lse), int(nthreads))
     if st != 0:

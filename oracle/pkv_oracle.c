@@ -28,7 +28,9 @@
  * rows of weights summing to one, extend == stacked decodes, the LSE-merge
  * identity, the full E4M3 code table, metadata closed forms; for tree masks,
  * brute force and torch SDPA with the same mask, and a chain-shaped tree
- * reproducing the causal result exactly.
+ * reproducing the causal result exactly; for sinks, -inf sinks reproducing
+ * the result without them exactly, torch SDPA with the sink as an extra key,
+ * and the uniform-score closed form.
  */
 #include <math.h>
 #include <pthread.h>
@@ -246,6 +248,7 @@ typedef struct {
   const int32_t* kv_last_page_len;
   const int32_t* qo_indptr;
   const uint64_t* tree_mask; /* NULL: chain drafts (bottom-right causal) */
+  const double* sinks;       /* NULL, or one sink logit per query head */
   double sm_scale, k_scale, v_scale;
   int64_t n_rows; /* number of (token, q-head) rows to compute */
   const int32_t* row_token; /* NULL: every row in token-major order */
@@ -278,7 +281,9 @@ static int kv_len_of(const attn_job* j, int b) {
  * set in tree_mask[t]: drafts are ordered with every ancestor before its
  * descendants, so bits above the row's own index are ignored. At most 64 new
  * tokens per request. GQA: query head h reads KV head h / (num_q_heads /
- * num_kv_heads). */
+ * num_kv_heads). With sinks, head h's sink logit joins the softmax as one
+ * more score whose value vector is zero: it adds to the normaliser (and the
+ * LSE) but not to o. */
 static int key_visible(const uint64_t* tree_mask, uint64_t word, int p, int prefix, int limit) {
   if (p > limit) return 0;
   if (!tree_mask || p < prefix) return 1;
@@ -303,8 +308,9 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
   int g = h / (j->num_q_heads / j->num_kv_heads);
   const uint16_t* qrow = j->q + ((int64_t)t * j->num_q_heads + h) * D;
   for (int d = 0; d < D; ++d) o[d] = 0.0;
+  double sink = j->sinks ? j->sinks[h] : -INFINITY;
   if (n_vis == 0) { /* no visible key: empty request (graph padding) or an empty mask row */
-    *lse = -INFINITY;
+    *lse = sink; /* the sink alone (-inf without one); o stays zero */
     return ORACLE_OK;
   }
   /* scores s_j = sm_scale * sum_d q_d k_jd over the visible keys */
@@ -319,8 +325,9 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
     scores[p] = j->sm_scale * dot;
     if (scores[p] > m) m = scores[p];
   }
-  /* softmax weights and weighted sum of V */
-  double z = 0.0;
+  if (sink > m) m = sink;
+  /* softmax weights (the sink's term in the normaliser) and weighted sum of V */
+  double z = sink > -INFINITY ? exp(sink - m) : 0.0;
   for (int p = 0; p <= limit; ++p)
     if (key_visible(j->tree_mask, word, p, prefix, limit)) z += exp(scores[p] - m);
   for (int p = 0; p <= limit; ++p) {
@@ -363,11 +370,12 @@ static void* attention_worker(void* arg) {
  * batch is computed (n_rows must equal qo_indptr[bs] * num_q_heads) and the
  * outputs are laid out [token][q_head][head_dim] / [token][q_head]. Rows are
  * independent; threads take them round-robin. tree_mask: NULL, or one word
- * per query token (see attention_row). */
+ * per query token; sinks: NULL, or one logit per query head (see
+ * attention_row). */
 int oracle_attention(int bs, int num_q_heads, int num_kv_heads, int head_dim, int page_size, int kv_dtype,
                      const uint16_t* q, const void* k_pool, const void* v_pool, const int32_t* kv_indptr,
                      const int32_t* kv_indices, const int32_t* kv_last_page_len, const int32_t* qo_indptr,
-                     const uint64_t* tree_mask, double sm_scale, double k_scale, double v_scale, int64_t n_rows, const int32_t* row_token,
+                     const uint64_t* tree_mask, const double* sinks, double sm_scale, double k_scale, double v_scale, int64_t n_rows, const int32_t* row_token,
                      const int32_t* row_head, double* out_o, double* out_lse, int nthreads) {
   if (bs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || page_size <= 0)
     return ORACLE_ERR_ARG;
@@ -389,6 +397,7 @@ int oracle_attention(int bs, int num_q_heads, int num_kv_heads, int head_dim, in
   job.kv_last_page_len = kv_last_page_len;
   job.qo_indptr = qo_indptr;
   job.tree_mask = tree_mask;
+  job.sinks = sinks;
   job.sm_scale = sm_scale;
   job.k_scale = k_scale;
   job.v_scale = v_scale;

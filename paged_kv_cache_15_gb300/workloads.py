@@ -69,6 +69,8 @@ class Workload:
     # uint64 [T], bit j of token t's word = it sees the j-th new token of its
     # request (every cached key stays visible)
     tree_mask: Optional[np.ndarray] = None
+    # attention sinks: None, or fp32 [Hq], each query head's sink logit
+    sinks: Optional[np.ndarray] = None
 
     @property
     def num_slots(self) -> int:
@@ -125,6 +127,13 @@ def random_tree_masks(qo_lens, seed: int = 5) -> np.ndarray:
             mask.append((1 << j) | (mask[parent] if parent >= 0 else 0))
         words.extend(mask)
     return np.array(words, dtype=np.uint64)
+
+
+def random_sinks(num_q_heads: int, seed: int = 6, lo: float = -2.0, hi: float = 4.0) -> np.ndarray:
+    """Per-head sink logits drawn uniformly from [lo, hi) (the scores of
+    N(0, 1) inputs scaled by 1/sqrt(D) sit around 0), stored as fp32."""
+    rng = np.random.default_rng(seed)
+    return rng.uniform(lo, hi, num_q_heads).astype(np.float32)
 
 
 def chain_tree_masks(qo_lens) -> np.ndarray:

@@ -32,7 +32,8 @@ def oracle_reference(W: Workload, rows=None, pools=None, nthreads=None):
     kv = oracle.KV_FP8_E4M3 if W.is_fp8 else oracle.KV_BF16
     return oracle.attention(bf16_bits(W.q), kp, vp, meta, W.num_q_heads, W.num_kv_heads, W.page_size,
                             W.sm_scale, kv_dtype=kv, k_scale=W.k_scale, v_scale=W.v_scale, rows=rows,
-                            nthreads=nthreads, tree_mask=W.tree_mask)
+                            nthreads=nthreads, tree_mask=W.tree_mask,
+                            sinks=None if W.sinks is None else W.sinks.astype(np.float64))
 
 
 def sample_rows(W: Workload, n: int, seed: int = 123):

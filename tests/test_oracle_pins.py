@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from paged_kv_cache_15_gb300.workloads import (Workload, bf16_bits, chain_tree_masks, make_workload, pool_bits,
-                                               preset, random_tree_masks)
+                                               preset, random_sinks, random_tree_masks)
 from tests._pipeline import oracle_meta, oracle_pools, oracle_reference
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -225,6 +225,73 @@ def test_p13_tree_of_more_than_64_drafts_rejected():
         oracle_reference(W)
     with pytest.raises(ValueError):
         random_tree_masks([65])
+
+
+# ---------------------------------------------------------------- P14 attention sinks
+def test_p14_minus_inf_sinks_change_nothing():
+    W = _tiny("extend", "bf16", seed_shift=8)
+    o0, l0 = oracle_reference(W)
+    W.sinks = np.full(W.num_q_heads, -np.inf, dtype=np.float32)
+    o1, l1 = oracle_reference(W)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+@pytest.mark.parametrize("mode", ["decode", "extend"])
+def test_p14_sinks_torch_sdpa_fp64(mode):
+    """The sink as one more key: zero key and value rows appended, and an
+    additive mask that gives that key head h's sink logit as its score."""
+    W = _tiny(mode, "bf16", seed_shift=9, hq=6, hkv=2)
+    W.sinks = random_sinks(W.num_q_heads, seed=3)
+    o, lse = oracle_reference(W)
+    q = torch.from_numpy(_q64(W))
+    G = W.num_q_heads // W.num_kv_heads
+    sink = torch.from_numpy(W.sinks.astype(np.float64))
+    qo_indptr = np.concatenate([[0], np.cumsum(W.qo_lens)])
+    for b, (K, V) in enumerate(_contiguous_kv(W)):
+        L, N = int(W.seq_lens[b]), int(W.qo_lens[b])
+        qb = q[qo_indptr[b]:qo_indptr[b + 1]].transpose(0, 1)  # [Hq, N, D]
+        Kt = torch.from_numpy(K).transpose(0, 1).repeat_interleave(G, dim=0)
+        Vt = torch.from_numpy(V).transpose(0, 1).repeat_interleave(G, dim=0)
+        Kt = torch.cat([Kt, torch.zeros(W.num_q_heads, 1, W.head_dim, dtype=Kt.dtype)], dim=1)
+        Vt = torch.cat([Vt, torch.zeros(W.num_q_heads, 1, W.head_dim, dtype=Vt.dtype)], dim=1)
+        vis = torch.arange(L)[None, :] <= (L - N + torch.arange(N))[:, None]  # [N, L]
+        add = torch.zeros(W.num_q_heads, N, L + 1, dtype=torch.float64)
+        add[:, :, :L] = torch.where(vis, 0.0, -math.inf)[None]
+        add[:, :, L] = sink[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qb, Kt, Vt, attn_mask=add, scale=W.sm_scale)
+        got = torch.from_numpy(o[qo_indptr[b]:qo_indptr[b + 1]]).transpose(0, 1)
+        assert torch.allclose(got, ref, atol=1e-12, rtol=0)
+        scores = (qb @ Kt.transpose(1, 2)) * W.sm_scale + add
+        ref_lse = torch.logsumexp(scores, dim=-1)
+        assert torch.allclose(torch.from_numpy(lse[qo_indptr[b]:qo_indptr[b + 1]]).T, ref_lse, atol=1e-12, rtol=0)
+
+
+def test_p14_sinks_uniform_scores_closed_form():
+    """q = 0: every visible score is 0, so o = (sum of v_j) / (n + e^sink) and
+    lse = ln(n + e^sink) with n the visible keys."""
+    W = _tiny("extend", "bf16", seed_shift=10)
+    W.q = torch.zeros_like(W.q)
+    W.sinks = random_sinks(W.num_q_heads, seed=4)
+    o, lse = oracle_reference(W)
+    G = W.num_q_heads // W.num_kv_heads
+    qo_indptr = np.concatenate([[0], np.cumsum(W.qo_lens)])
+    for b, (K, V) in enumerate(_contiguous_kv(W)):
+        L, N = int(W.seq_lens[b]), int(W.qo_lens[b])
+        for i in range(N):
+            n = L - N + i + 1
+            for h in range(W.num_q_heads):
+                e = math.exp(float(W.sinks[h]))
+                ref = V[:n, h // G].sum(axis=0) / (n + e)
+                assert np.allclose(o[qo_indptr[b] + i, h], ref, atol=1e-13, rtol=0)
+                assert abs(lse[qo_indptr[b] + i, h] - math.log(n + e)) < 1e-13
+
+
+def test_p14_sinks_empty_request():
+    W = make_workload("sk0", "decode", 2, 4, 2, 8, [0, 5], [1, 1], page_size=4)
+    W.seq_lens = np.array([0, 6], dtype=W.seq_lens.dtype)
+    W.sinks = random_sinks(4, seed=5)
+    o, lse = oracle_reference(W)
+    assert np.all(o[0] == 0.0) and np.allclose(lse[0], W.sinks.astype(np.float64), rtol=0, atol=0)
 
 
 # ---------------------------------------------------------------- P2 / P3 layout invariance
