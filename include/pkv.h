@@ -224,6 +224,21 @@ int pkv_forward(pkv_ctx* ctx, int forward_mode, int spec_mode, const void* d_q, 
  * so a captured graph replays with whatever the buffer holds then. */
 int pkv_set_tree_mask(pkv_ctx* ctx, const uint64_t* d_tree_mask);
 
+/* Attention sinks ("--attention-backend", section "The obvious fix, and why
+ * it fails": a model that uses them rules some backends out). The pages give
+ * no formula; this library's reading: d_sinks is a device fp32
+ * [num_q_heads] array, and head h's sink logit joins every softmax of that
+ * head as one more score whose value vector is zero:
+ *   o = sum_j exp(s_j) v_j / (sum_j exp(s_j) + exp(sink_h)),
+ *   lse = ln(sum_j exp(s_j) + exp(sink_h)),
+ * with s_j = sm_scale * q . k_j as above; a row with no visible key gives
+ * o = 0 and lse = sink_h. A -inf entry leaves its head unchanged. Applies to
+ * every forward of the context (both paths, all modes) until set again; NULL
+ * (the default) turns sinks off. The caller owns the buffer and keeps it
+ * alive while forwards that use it run; a captured graph replays with
+ * whatever it then holds. */
+int pkv_set_attention_sinks(pkv_ctx* ctx, const float* d_sinks);
+
 /* Synchronise `stream`, read the device error word into *code (PKV_DEV_*) and
  * clear it. Returns PKV_ERR_DEVICE when *code != PKV_DEV_OK. */
 int pkv_get_device_error(pkv_ctx* ctx, int32_t* code, void* stream);

@@ -30,7 +30,7 @@ PKV_KV_BF16, PKV_KV_FP8_E4M3 = 0, 1
 EXPORTS = ("pkv_status_string", "pkv_workspace_bytes", "pkv_pool_bytes", "pkv_create", "pkv_destroy",
            "pkv_select_backend", "pkv_build_metadata", "pkv_get_metadata", "pkv_set_kv_buffer",
            "pkv_forward_decode", "pkv_forward_extend", "pkv_forward", "pkv_get_device_error", "pkv_describe",
-           "pkv_forward_decode_static", "pkv_set_tree_mask")
+           "pkv_forward_decode_static", "pkv_set_tree_mask", "pkv_set_attention_sinks")
 
 
 class PkvError(RuntimeError):
@@ -79,6 +79,7 @@ def lib():
             "pkv_forward": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_float,
                                            ctypes.c_float, ctypes.c_float, vp, vp, vp]),
             "pkv_set_tree_mask": (ctypes.c_int, [vp, vp]),
+            "pkv_set_attention_sinks": (ctypes.c_int, [vp, vp]),
             "pkv_get_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), vp]),
             "pkv_describe": (ctypes.c_int, [vp, ctypes.c_char_p, sz]),
             "pkv_forward_decode_static": (ctypes.c_int, [cfgp, i32, vp, vp, i32, vp, vp, vp, ctypes.c_float,
@@ -193,6 +194,12 @@ def pkv_set_tree_mask(ctx, tree_mask) -> None:
     """Draft-tree mask words (uint64 device tensor, one per query token) for
     the verify forwards that follow, or None for chain drafts."""
     _check(lib().pkv_set_tree_mask(ctx, _ptr(tree_mask)), "pkv_set_tree_mask")
+
+
+def pkv_set_attention_sinks(ctx, sinks) -> None:
+    """Per-query-head sink logits (fp32 device tensor [num_q_heads]) for the
+    forwards that follow, or None to turn sinks off."""
+    _check(lib().pkv_set_attention_sinks(ctx, _ptr(sinks)), "pkv_set_attention_sinks")
 
 
 def pkv_get_device_error(ctx, stream=None) -> int:

@@ -89,6 +89,7 @@ struct DecodeArgs {
   float scale_log2;  // sm_scale * k_scale * log2(e)
   float v_scale;     // multiplies the output (E4M3 pools), 1 for bf16
   const uint64_t* tree;  // draft-tree mask word per query token, or null (chain drafts)
+  const float* sinks;    // sink logit per query head, or null
 };
 
 // Byte offset of (row, 16-byte chunk) inside a swizzled [rows][128 B] column block.
@@ -179,13 +180,19 @@ __device__ __forceinline__ void merge_row(const DecodeArgs& a, long long pbase, 
       V::fma(acc, __shfl_sync(0xffffffffu, w0, s0 + sp), x[sp]);
     }
   }
+  float lse = Z > 0.f ? M + __logf(Z) : -INFINITY;
+  if (a.sinks) {
+    const float f = sink_factor(lse, a.sinks[h]);
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc[j] *= f;
+  }
   uint16_t* dst = a.out + orow * D + lane * PER;
   if constexpr (PER == 4) {
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
   } else {
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
   }
-  if (a.lse && lane == 0) a.lse[orow] = Z > 0.f ? M + __logf(Z) : -INFINITY;
+  if (a.lse && lane == 0) a.lse[orow] = lse;
 }
 
 template <class C>
@@ -628,7 +635,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             float* lrow;
             out_row(r, orow, lrow);
             *reinterpret_cast<uint32_t*>(orow + 2 * c2) = 0u;
-            if (c2 == 0 && lrow) *lrow = -INFINITY;
+            // no key: the LSE is the sink's alone (final rows only)
+            if (c2 == 0 && lrow) *lrow = (direct && a.sinks) ? a.sinks[g * G + r % G] : -INFINITY;
           }
         }
       } else {
@@ -687,12 +695,14 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             acc.z += x.z * wgt[k];
             acc.w += x.w * wgt[k];
           }
+          float lse_r = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+          const float fs = (direct && a.sinks) ? sink_factor(lse_r, a.sinks[g * G + r % G]) : 1.f;
           uint16_t* orow;
           float* lrow;
           out_row(r, orow, lrow);
-          *reinterpret_cast<uint2*>(orow + c4 * 4) =
-              make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
-          if (c4 == 0 && lrow) *lrow = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+          *reinterpret_cast<uint2*>(orow + c4 * 4) = make_uint2(pack_bf16(acc.x * inv * fs, acc.y * inv * fs),
+                                                                pack_bf16(acc.z * inv * fs, acc.w * inv * fs));
+          if (c4 == 0 && lrow) *lrow = lse_r;
         }
         fence_proxy_async_smem();
         named_bar_sync(1, C::kConsumerWarps * 32);  // scratch reads done before the stage is refilled
@@ -966,8 +976,9 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           uint16_t* orow;
           float* lrow;
           out_row(r, orow, lrow);
-          const float inv = l > 0.f ? a.v_scale / l : 0.f;
-          const float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+          float inv = l > 0.f ? a.v_scale / l : 0.f;
+          float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+          if (direct && a.sinks) inv *= sink_factor(lse, a.sinks[g * G + r % G]);
 #pragma unroll
           for (int nt = 0; nt < C::kNT; ++nt) {
             const float x0 = o[nt][2 * half] * inv, x1 = o[nt][2 * half + 1] * inv;
@@ -1046,6 +1057,7 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.scale_log2 = sm_scale * (fp8 ? k_scale : 1.f) * kLog2e;
   a.v_scale = fp8 ? v_scale : 1.f;
   a.tree = active_tree(c);
+  a.sinks = c.sinks;
   cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
@@ -1139,6 +1151,7 @@ int launch_split_merge(Ctx& c, void* out, float* lse, int max_rows_per_head, boo
   a.scale_log2 = 0.f;
   a.v_scale = 1.f;
   a.tree = nullptr;
+  a.sinks = c.sinks;
   // one warp per (token, head) row, 8 warps per CTA, 3 CTAs per SM
   const long long rows = (long long)c.cfg.max_q_tokens * c.cfg.num_q_heads;
   const long long grid = std::min<long long>((rows + 7) / 8, (long long)c.num_sms * 3);

@@ -81,9 +81,10 @@ __device__ __forceinline__ void st_global_32B(void* p, const uint32_t* v) {
                : "memory");
 }
 
-// Visibility of the 32 keys key_base .. key_base + 31 for a row of a
-// draft-tree batch, one bit each: keys up to the row's limit, less the drafts
-// (keys from draft0 on) whose bit is clear in the row's tree word.
+// Visibility of the 32 keys key_base .. key_base + 31 for one row, one bit
+// each: keys up to the row's limit, less the drafts (keys from draft0 on)
+// whose bit is clear in the row's tree word (draft0 lies past every key when
+// no tree is set).
 __device__ __forceinline__ uint32_t visible32(int key_base, int limit, int draft0, uint64_t word) {
   const int n = limit - key_base + 1;  // keys within the limit
   const uint32_t v = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
@@ -213,11 +214,12 @@ struct ExtendArgs {
   int q_box_tokens;  // 128 / group
   int out_32B;       // out is 32-byte aligned: output rows are written with 32-byte stores
   const uint64_t* tree;  // draft-tree mask word per query token, or null (chain drafts)
+  const float* sinks;    // sink logit per query head, or null
 };
 
-// TREE: verify batches with draft-tree mask words (a separate instantiation,
-// so batches without a tree run the plain causal masking).
-template <class C, bool TREE>
+// EXTRAS: draft-tree mask words or attention sinks are in use (a separate
+// instantiation, so plain batches run the causal kernel without that code).
+template <class C, bool EXTRAS>
 __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                    const __grid_constant__ CUtensorMap tmap_v,
                                                                    const __grid_constant__ CUtensorMap tmap_q,
@@ -576,10 +578,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       // draft trees: the row's mask word clears the drafts outside its tree
       uint64_t tword = ~0ull;
       int draft0 = 0x3fffffff;  // first draft key (none without a tree)
-      if constexpr (TREE) {
-        tword = valid ? a.tree[q0 + R / G] : ~0ull;
-        draft0 = L - qo;
-        if (qo > 64 && r == 0 && x == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
+      if constexpr (EXTRAS) {
+        if (a.tree) {
+          tword = valid ? a.tree[q0 + R / G] : ~0ull;
+          draft0 = L - qo;
+          if (qo > 64 && r == 0 && x == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
+        }
       }
       const long long orow = (long long)(q0 + R / G) * a.num_q_heads + g * G + R % G;
       // split units write bf16 partial rows (normalised output) and fp32 LSE that
@@ -609,7 +613,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           } else {
             for (int c = 0; c < D; c += 8)
               *reinterpret_cast<uint4*>(a.out + orow * D + c) = make_uint4(0, 0, 0, 0);
-            if (a.lse) a.lse[orow] = -INFINITY;
+            // no key: the LSE is the sink's alone
+            if (a.lse) a.lse[orow] = (EXTRAS && a.sinks) ? a.sinks[g * G + R % G] : -INFINITY;
           }
         }
         jt += ukv.len();
@@ -649,7 +654,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         const int key0 = j * kExtendKeys;
         // some keys of this tile are masked for this row: past its limit, or
         // drafts that its tree may hide
-        const bool diag = key0 + kExtendKeys - 1 > limit || (TREE && key0 + kExtendKeys > draft0);
+        const bool diag = key0 + kExtendKeys - 1 > limit || (EXTRAS && key0 + kExtendKeys > draft0);
         // the request's last page inside this KV tile: zero the V rows past L
         // (done by the first tile that reads this V tile, before its PV)
         if ((ukv.dual || x == 0 || jr >= nA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
@@ -678,7 +683,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           tmem_ld32(lane_base + s_col + cc * 32 + 32, sr + 32);
           tmem_wait_ld();
           if (diag) {
-            if constexpr (TREE) {
+            if constexpr (EXTRAS) {
               mask32_bits(sr, visible32(key0 + cc * 32, limit, draft0, tword));
               mask32_bits(sr + 32, visible32(key0 + cc * 32 + 32, limit, draft0, tword));
             } else {
@@ -797,7 +802,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         l = l * wa + lb * wb;
         m_ref = m;
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float inv = l > 0.f ? 1.f / l : 0.f;
+      if constexpr (EXTRAS) {
+        // final rows of a model with sinks: the head's sink joins the normaliser
+        if (!split && valid && a.sinks) {
+          float lse_s = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+          inv *= sink_factor(lse_s, a.sinks[g * G + R % G]);
+        }
+      }
       wa *= inv;
       wb *= inv;
 #pragma unroll
@@ -851,7 +863,10 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         ++du;
       }
       if (valid) {
-        const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        float lse_v = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        if constexpr (EXTRAS) {
+          if (!split && a.sinks) (void)sink_factor(lse_v, a.sinks[g * G + R % G]);
+        }
         if (split)
           a.m.partial_lse[prow] = lse_v;
         else if (a.lse)
@@ -892,6 +907,7 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.scale_log2 = sm_scale * kLog2e;
   a.out_32B = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
   a.tree = active_tree(c);
+  a.sinks = c.sinks;
   // Q as [tokens][heads][head_dim]: a box of 64 elements x G heads x 128/G
   // tokens is one 128-row tile column block, rows ordered (token, head) like
   // the tile's rows. The token extent only bounds the map; the kernel loads a
@@ -911,7 +927,7 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
     a.q_tma = 1;
     a.q_box_tokens = (int)box_tok;
   }
-  auto kernel = a.tree ? extend_tc_kernel<C, true> : extend_tc_kernel<C, false>;
+  auto kernel = (a.tree || a.sinks) ? extend_tc_kernel<C, true> : extend_tc_kernel<C, false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (launch_pdl(kernel, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, tq, a) != cudaSuccess)

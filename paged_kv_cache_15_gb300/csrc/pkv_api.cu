@@ -384,6 +384,13 @@ int pkv_set_tree_mask(pkv_ctx* ctx, const uint64_t* d_tree_mask) {
   return PKV_OK;
 }
 
+int pkv_set_attention_sinks(pkv_ctx* ctx, const float* d_sinks) {
+  if (!ctx) return PKV_ERR_INVALID_ARG;
+  if (d_sinks && (reinterpret_cast<uintptr_t>(d_sinks) & 3u) != 0) return PKV_ERR_INVALID_ARG;
+  ctx->sinks = d_sinks;
+  return PKV_OK;
+}
+
 int pkv_get_device_error(pkv_ctx* ctx, int32_t* code, void* stream) {
   if (!ctx || !code) return PKV_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -90,6 +90,7 @@ struct Ctx {
   bool qo_given;  // last build had explicit qo_lens
   int device;
   const uint64_t* tree = nullptr;  // draft-tree mask words (pkv_set_tree_mask), or null
+  const float* sinks = nullptr;    // per-query-head sink logits (pkv_set_attention_sinks), or null
 };
 
 // The tree mask the next forward applies: only after a build in a verify mode.
@@ -332,6 +333,18 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
+}
+
+// Attention sink: the head's sink logit joins the softmax as a key with a zero
+// value vector. Given a finished row's natural-log LSE over its keys, returns
+// the factor that scales its output and moves lse to include the sink (a row
+// with no keys gets factor 0 and lse = sink).
+__device__ __forceinline__ float sink_factor(float& lse, float sink) {
+  const float mx = fmaxf(lse, sink);
+  if (mx == -INFINITY) return 1.f;  // no key and a -inf sink
+  const float a = expf(lse - mx), c = expf(sink - mx);
+  lse = mx + logf(a + c);
+  return a / (a + c);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -51,6 +51,11 @@ class DeviceBatch:
         if W.tree_mask is not None:
             self.tree = torch.from_numpy(W.tree_mask.view("int64").copy()).to(dev)
             B.pkv_set_tree_mask(self.ctx, self.tree)
+        # attention sinks (fp32 per query head)
+        self.sinks = None
+        if W.sinks is not None:
+            self.sinks = torch.from_numpy(W.sinks.astype("float32")).to(dev)
+            B.pkv_set_attention_sinks(self.ctx, self.sinks)
 
     @property
     def ctx(self):

@@ -12,7 +12,8 @@ import torch
 import oracle
 from paged_kv_cache_15_gb300 import binding as B
 from paged_kv_cache_15_gb300.runner import DeviceBatch, config_for
-from paged_kv_cache_15_gb300.workloads import chain_tree_masks, make_workload, pool_bits, preset, random_tree_masks
+from paged_kv_cache_15_gb300.workloads import (chain_tree_masks, make_workload, pool_bits, preset, random_sinks,
+                                               random_tree_masks)
 from tests._pipeline import oracle_meta, oracle_pools, oracle_reference, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -553,6 +554,48 @@ def test_non_positive_scales_rejected():
     with pytest.raises(B.PkvError):
         B.pkv_forward(df.ctx, df.mode, B.PKV_SPEC_PREFILL, df.q, df.k_pool, df.v_pool, Wf.sm_scale, df.out,
                       df.lse, 0.0, Wf.v_scale)
+
+
+# ------------------------------------------------------------------ attention sinks
+@pytest.mark.parametrize("case", ["decode", "decode_fp8", "decode_g16", "extend", "verify_prefill", "verify_decode",
+                                  "tree_verify"])
+def test_attention_sinks_parity(case):
+    """Each query head's sink logit joins its softmax as a zero-value key, on
+    single-split rows (the attention kernels apply it) and split rows (the
+    merge applies it)."""
+    spec = B.PKV_SPEC_PREFILL
+    if case == "decode":
+        W = preset("llama3_8b_decode", bs=8, len_scale=0.25)
+    elif case == "decode_fp8":
+        W = preset("long_fp8_decode", bs=3, len_scale=1 / 32)
+    elif case == "decode_g16":
+        W = make_workload("sk16", "decode", 5, 32, 2, 128, [0, 40, 700, 3000, 9], np.ones(5))
+    elif case == "extend":
+        W = make_workload("skx", "extend", 4, 16, 4, 128, [0, 300, 1200, 5], [200, 70, 1, 400])
+    elif case == "verify_prefill":
+        W = preset("spec_verify", bs=6, len_scale=0.1)
+    elif case == "verify_decode":
+        W = preset("spec_verify", bs=6, len_scale=0.1)
+        spec = B.PKV_SPEC_DECODE
+    else:
+        W = _tree_verify("sktv", 5, 32, 2, 128, 8, 47)
+    W.sinks = random_sinks(W.num_q_heads, seed=12)
+    full_check(W, spec_mode=spec)
+
+
+def test_sinks_on_padding_rows_and_minus_inf_sinks():
+    """A request without keys reports o = 0 and lse = the sink; -inf sinks
+    give bit for bit the result without sinks."""
+    W = make_workload("skp", "decode", 4, 8, 2, 64, [0, 37, 0, 211], np.ones(4))
+    W.seq_lens = np.array([0, 38, 0, 212], dtype=W.seq_lens.dtype)
+    W.sinks = random_sinks(W.num_q_heads, seed=13)
+    d = full_check(W)
+    assert torch.equal(d.lse[0].cpu(), torch.from_numpy(W.sinks))
+    W2 = preset("llama3_8b_decode", bs=6, len_scale=0.2)
+    plain = run_path(W2)
+    W2.sinks = np.full(W2.num_q_heads, -np.inf, dtype=np.float32)
+    neg = run_path(W2)
+    assert torch.equal(plain.out, neg.out) and torch.equal(plain.lse, neg.lse)
 
 
 def test_extend_mixed_split_and_unsplit_requests():
