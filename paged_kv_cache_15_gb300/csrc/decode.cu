@@ -195,7 +195,9 @@ __device__ __forceinline__ void merge_row(const DecodeArgs& a, long long pbase, 
   if (a.lse && lane == 0) a.lse[orow] = lse;
 }
 
-template <class C>
+// EXTRAS: draft-tree mask words or attention sinks are in use (a separate
+// instantiation, so plain batches run without that code).
+template <class C, bool EXTRAS>
 __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                      const __grid_constant__ CUtensorMap tmap_v,
                                                                      DecodeArgs a) {
@@ -213,6 +215,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
   volatile int* s_uq = reinterpret_cast<volatile int*>(uq_empty + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint64_t* const tree_words = EXTRAS ? a.tree : nullptr;
+  const float* const sinks = EXTRAS ? a.sinks : nullptr;
   int* plan = a.m.plan;
   pdl_launch_dependents();
 
@@ -363,16 +367,9 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
 #pragma unroll
         for (int e = 0; e < 2; ++e) lim[j][e] = prefix + min((8 * j + 2 * t4 + e) / G, qo - 1);
       // draft trees: a row's mask word clears the drafts outside its tree (the
-      // causal limit above still bounds it)
-      const bool tree = a.tree != nullptr;
-      uint64_t tw[RT][2];
-#pragma unroll
-      for (int j = 0; j < RT; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int r = 8 * j + 2 * t4 + e;
-          tw[j][e] = (tree && r < rows_valid) ? a.tree[q0 + r / G] : ~0ull;
-        }
+      // causal limit above still bounds it); the words are read only in the
+      // blocks that reach the drafts
+      const bool tree = tree_words != nullptr;
       if (tree && qo > 64 && lane == 0 && wk == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
 
       // Q^T fragments (B operand): column g8 of row tile j is query row 8j + g8
@@ -496,11 +493,14 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
 #pragma unroll
               for (int j = 0; j < RT; ++j)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int dj = abs0 + g8 + 8 * h - prefix;
+                for (int e = 0; e < 2; ++e) {
+                  const int r = 8 * j + 2 * t4 + e;
+                  const uint64_t tw = r < rows_valid ? tree_words[q0 + r / G] : ~0ull;
 #pragma unroll
-                  for (int e = 0; e < 2; ++e)
-                    if (dj >= 0 && !(dj < 64 && ((tw[j][e] >> dj) & 1ull))) s[j][2 * h + e] = -INFINITY;
+                  for (int h = 0; h < 2; ++h) {
+                    const int dj = abs0 + g8 + 8 * h - prefix;
+                    if (dj >= 0 && !(dj < 64 && ((tw >> dj) & 1ull))) s[j][2 * h + e] = -INFINITY;
+                  }
                 }
             }
             float al[RT][2];
@@ -636,7 +636,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             out_row(r, orow, lrow);
             *reinterpret_cast<uint32_t*>(orow + 2 * c2) = 0u;
             // no key: the LSE is the sink's alone (final rows only)
-            if (c2 == 0 && lrow) *lrow = (direct && a.sinks) ? a.sinks[g * G + r % G] : -INFINITY;
+            if (c2 == 0 && lrow) *lrow = (direct && sinks) ? sinks[g * G + r % G] : -INFINITY;
           }
         }
       } else {
@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             acc.w += x.w * wgt[k];
           }
           float lse_r = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
-          const float fs = (direct && a.sinks) ? sink_factor(lse_r, a.sinks[g * G + r % G]) : 1.f;
+          const float fs = (direct && sinks) ? sink_factor(lse_r, sinks[g * G + r % G]) : 1.f;
           uint16_t* orow;
           float* lrow;
           out_row(r, orow, lrow);
@@ -721,10 +721,9 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
       const int lim_b = prefix + min(rb / G, qo - 1);
       const long long qrow_a = ((long long)(q0 + ra / G) * a.num_q_heads + g * G + ra % G) * D;
       const long long qrow_b = ((long long)(q0 + rb / G) * a.num_q_heads + g * G + rb % G) * D;
-      // draft trees: each row's mask word clears the drafts outside its tree
-      const bool tree = a.tree != nullptr;
-      const uint64_t tw_a = (tree && va) ? a.tree[q0 + ra / G] : ~0ull;
-      const uint64_t tw_b = (tree && vb) ? a.tree[q0 + rb / G] : ~0ull;
+      // draft trees: each row's mask word clears the drafts outside its tree;
+      // the words are read only in the blocks that reach the drafts
+      const bool tree = tree_words != nullptr;
       if (tree && qo > 64 && lane == 0 && cw == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
 
       // Q fragments (A operand), D/16 k-steps x 4 registers
@@ -834,6 +833,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             if (tree && abs0 + 15 >= prefix) {
               // the block reaches the drafts: raw scores of drafts outside a
               // row's tree to -inf (the scale below is positive)
+              const uint64_t tw_a = va ? tree_words[q0 + ra / G] : ~0ull;
+              const uint64_t tw_b = vb ? tree_words[q0 + rb / G] : ~0ull;
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -978,7 +979,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           out_row(r, orow, lrow);
           float inv = l > 0.f ? a.v_scale / l : 0.f;
           float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
-          if (direct && a.sinks) inv *= sink_factor(lse, a.sinks[g * G + r % G]);
+          if (direct && sinks) inv *= sink_factor(lse, sinks[g * G + r % G]);
 #pragma unroll
           for (int nt = 0; nt < C::kNT; ++nt) {
             const float x0 = o[nt][2 * half] * inv, x1 = o[nt][2 * half + 1] * inv;
@@ -1058,11 +1059,10 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.v_scale = fp8 ? v_scale : 1.f;
   a.tree = active_tree(c);
   a.sinks = c.sinks;
-  cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
-  if (e != cudaSuccess) return PKV_ERR_CUDA;
-  if (launch_pdl(decode_splitkv_kernel<C>, dim3(c.decode_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, a) !=
-      cudaSuccess)
+  auto kernel = (a.tree || a.sinks) ? decode_splitkv_kernel<C, true> : decode_splitkv_kernel<C, false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (launch_pdl(kernel, dim3(c.decode_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, a) != cudaSuccess)
     return PKV_ERR_CUDA;
   return launch_split_merge(c, out, lse, c.cfg.max_qo_len * a.group, false, st);
 }
