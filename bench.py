@@ -43,15 +43,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (profiles/), valid only while the kernel source is unchanged.
 NCU_TRAFFIC = {
-    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "7978a7b619b91bfc", "bytes_per_launch": 1386582528,
+    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1386555136,
                                              "source": "profiles/decode_splitkv_llama3_8b_decode.md"},
-    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "7978a7b619b91bfc", "bytes_per_launch": 1509188864,
+    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1504556032,
                                             "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("decode_splitkv", "spec_verify"): {"src_sha": "7978a7b619b91bfc", "bytes_per_launch": 601608704,
+    ("decode_splitkv", "spec_verify"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 601473024,
                                         "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("extend_tc", "prefix_extend"): {"src_sha": "fd7d32f9906cdca2", "bytes_per_launch": 1050398464,
+    ("extend_tc", "prefix_extend"): {"src_sha": "6e52fe7fd3947dc0", "bytes_per_launch": 927089920,
                                      "source": "profiles/extend_tc_prefix_extend.md"},
-    ("extend_tc", "spec_verify"): {"src_sha": "fd7d32f9906cdca2", "bytes_per_launch": 599987712,
+    ("extend_tc", "spec_verify"): {"src_sha": "6e52fe7fd3947dc0", "bytes_per_launch": 599929344,
                                    "source": "profiles/dram_traffic_fp8_and_verify.md"},
 }
 
