@@ -215,10 +215,12 @@ struct ExtendArgs {
   int out_32B;       // out is 32-byte aligned: output rows are written with 32-byte stores
   const uint64_t* tree;  // draft-tree mask word per query token, or null (chain drafts)
   const float* sinks;    // sink logit per query head, or null
+  float v_scale;         // multiplies every written row (E4M3 pools; 1 otherwise), EXTRAS only
 };
 
-// EXTRAS: draft-tree mask words or attention sinks are in use (a separate
-// instantiation, so plain batches run the causal kernel without that code).
+// EXTRAS: draft-tree mask words, attention sinks or an E4M3 pool's value scale
+// are in use (a separate instantiation, so plain batches run the causal
+// kernel without that code).
 template <class C, bool EXTRAS>
 __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                    const __grid_constant__ CUtensorMap tmap_v,
@@ -804,6 +806,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       }
       float inv = l > 0.f ? 1.f / l : 0.f;
       if constexpr (EXTRAS) {
+        inv *= a.v_scale;
         // final rows of a model with sinks: the head's sink joins the normaliser
         if (!split && valid && a.sinks) {
           float lse_s = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
@@ -884,12 +887,73 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   }
 }
 
+// E4M3 pools on the extend path: the codes of the batch's pages, in
+// kv_indices order, widened to bf16 (exact: every E4M3 value is a bf16
+// value) into a compact copy whose page i is the batch's i-th page, plus the
+// identity page list idx[i] = i through which the extend kernel reads it.
+// One thread widens 16 codes (one 16-byte vector) of K and of V.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
+  const uint32_t h = e4m3x2_to_f16x2(v);
+  float lo, hi;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h & 0xffffu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h >> 16)));
+  return pack_bf16(lo, hi);
+}
+
+__global__ void __launch_bounds__(256) fp8_stage_kernel(const uint8_t* __restrict__ kp, const uint8_t* __restrict__ vp,
+                                                        uint16_t* __restrict__ sk, uint16_t* __restrict__ sv,
+                                                        int* __restrict__ idx, const int* __restrict__ kv_indices,
+                                                        const int* __restrict__ plan, int page_elems) {
+  pdl_launch_dependents();
+  pdl_wait();  // the page list comes from the metadata build before this launch
+  const int np = plan[kTotalPages];
+  const int vec = page_elems / 16;
+  const long long n = (long long)np * vec;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int pi = (int)(i / vec), w = (int)(i % vec);
+    const long long src = (long long)kv_indices[pi] * page_elems + (long long)w * 16;
+    const long long dst = (long long)pi * page_elems + (long long)w * 16;
+    const uint4 k = *reinterpret_cast<const uint4*>(kp + src);
+    const uint4 v = *reinterpret_cast<const uint4*>(vp + src);
+    const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
+    uint32_t ko[8], vo[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      ko[2 * j] = e4m3x2_to_bf16x2((uint16_t)(kw[j] & 0xffffu));
+      ko[2 * j + 1] = e4m3x2_to_bf16x2((uint16_t)(kw[j] >> 16));
+      vo[2 * j] = e4m3x2_to_bf16x2((uint16_t)(vw[j] & 0xffffu));
+      vo[2 * j + 1] = e4m3x2_to_bf16x2((uint16_t)(vw[j] >> 16));
+    }
+    *reinterpret_cast<uint4*>(sk + dst) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+    *reinterpret_cast<uint4*>(sk + dst + 8) = make_uint4(ko[4], ko[5], ko[6], ko[7]);
+    *reinterpret_cast<uint4*>(sv + dst) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+    *reinterpret_cast<uint4*>(sv + dst + 8) = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+    if (w == 0) idx[pi] = pi;
+  }
+}
+
 template <class C>
-int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, void* out, float* lse,
-               cudaStream_t st) {
+int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+               float v_scale, void* out, float* lse, cudaStream_t st) {
   CUtensorMap tk, tv;
   const uint64_t inner = (uint64_t)c.cfg.num_kv_heads * C::D;
-  const uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
+  uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
+  const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
+  if (fp8) {
+    // widen the batch's E4M3 pages into the workspace copy and read that
+    if (!c.lay.has_stage) return PKV_ERR_UNSUPPORTED;
+    uint16_t* sk = reinterpret_cast<uint16_t*>(c.ws + c.lay.stage_k);
+    uint16_t* sv = reinterpret_cast<uint16_t*>(c.ws + c.lay.stage_v);
+    int* idx = reinterpret_cast<int*>(c.ws + c.lay.stage_idx);
+    const int page_elems = c.cfg.page_size * c.cfg.num_kv_heads * C::D;
+    if (launch_pdl(fp8_stage_kernel, dim3((unsigned)(c.num_sms * 4)), dim3(256), 0, st,
+                   static_cast<const uint8_t*>(k_pool), static_cast<const uint8_t*>(v_pool), sk, sv, idx,
+                   make_meta(c).kv_indices, static_cast<const int*>(make_meta(c).plan), page_elems) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    k_pool = sk;
+    v_pool = sv;
+    slots = (uint64_t)c.cfg.max_pages_total * c.cfg.page_size;
+  }
   if (encode_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(k_pool), inner, slots, inner * 2, 64,
                      kPageSize, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
@@ -904,7 +968,9 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.num_q_heads = c.cfg.num_q_heads;
   a.num_kv_heads = c.cfg.num_kv_heads;
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
-  a.scale_log2 = sm_scale * kLog2e;
+  a.scale_log2 = sm_scale * (fp8 ? k_scale : 1.f) * kLog2e;
+  a.v_scale = fp8 ? v_scale : 1.f;
+  if (fp8) a.m.kv_indices = reinterpret_cast<const int*>(c.ws + c.lay.stage_idx);
   a.out_32B = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
   a.tree = active_tree(c);
   a.sinks = c.sinks;
@@ -927,7 +993,7 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
     a.q_tma = 1;
     a.q_box_tokens = (int)box_tok;
   }
-  auto kernel = (a.tree || a.sinks) ? extend_tc_kernel<C, true> : extend_tc_kernel<C, false>;
+  auto kernel = (a.tree || a.sinks || fp8) ? extend_tc_kernel<C, true> : extend_tc_kernel<C, false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (launch_pdl(kernel, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, tq, a) != cudaSuccess)
@@ -938,10 +1004,12 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
 
 }  // namespace
 
-int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, void* out,
-                  float* lse, cudaStream_t st) {
-  if (c.cfg.head_dim == 128) return run_extend<ExtCfg<128, 3, 2>>(c, q, k_pool, v_pool, sm_scale, out, lse, st);
-  if (c.cfg.head_dim == 64) return run_extend<ExtCfg<64, 4, 4>>(c, q, k_pool, v_pool, sm_scale, out, lse, st);
+int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+                  float v_scale, void* out, float* lse, cudaStream_t st) {
+  if (c.cfg.head_dim == 128)
+    return run_extend<ExtCfg<128, 3, 2>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st);
+  if (c.cfg.head_dim == 64)
+    return run_extend<ExtCfg<64, 4, 4>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st);
   return PKV_ERR_UNSUPPORTED;
 }
 

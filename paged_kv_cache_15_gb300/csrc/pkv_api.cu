@@ -61,7 +61,7 @@ void grid_sizes(const pkv_config& cfg, int num_sms, int* decode_ctas, int* exten
   if (*extend_ctas < 1) *extend_ctas = 1;
 }
 
-Layout make_layout(const pkv_config& cfg, int num_sms) {
+Layout make_layout(const pkv_config& cfg, int num_sms, bool with_stage) {
   Layout L;
   int dctas, ectas;
   grid_sizes(cfg, num_sms, &dctas, &ectas);
@@ -94,6 +94,14 @@ Layout make_layout(const pkv_config& cfg, int num_sms) {
   L.extend_tiles = take(sizeof(ExtendTile) * (size_t)L.max_extend_tiles);
   L.partial_o = take(sizeof(uint16_t) * (size_t)cap * cfg.num_q_heads * cfg.head_dim);
   L.partial_lse = take(sizeof(float) * (size_t)cap * cfg.num_q_heads);
+  L.has_stage = with_stage && cfg.kv_dtype == PKV_KV_FP8_E4M3;
+  L.stage_k = L.stage_v = L.stage_idx = 0;
+  if (L.has_stage) {
+    const size_t page_bytes = (size_t)cfg.page_size * cfg.num_kv_heads * cfg.head_dim * sizeof(uint16_t);
+    L.stage_k = take(page_bytes * (size_t)cfg.max_pages_total);
+    L.stage_v = take(page_bytes * (size_t)cfg.max_pages_total);
+    L.stage_idx = take(sizeof(int) * (size_t)cfg.max_pages_total);
+  }
   L.total = off;
   return L;
 }
@@ -194,7 +202,7 @@ int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint
 int static_config_ok(const pkv_config* cfg) { return check_config(cfg); }
 
 size_t static_layout_bytes(const pkv_config& cfg, int num_sms, Layout* lay) {
-  *lay = make_layout(cfg, num_sms);
+  *lay = make_layout(cfg, num_sms, false);  // decode only: no extend staging
   return lay->total;
 }
 
@@ -235,7 +243,7 @@ int pkv_workspace_bytes(const pkv_config* cfg, size_t* bytes_out) {
   if (!bytes_out) return PKV_ERR_INVALID_ARG;
   int dev, sms;
   if (device_sms(&dev, &sms) != PKV_OK) return PKV_ERR_CUDA;
-  *bytes_out = make_layout(*cfg, sms).total;
+  *bytes_out = make_layout(*cfg, sms, true).total;
   return PKV_OK;
 }
 
@@ -256,7 +264,7 @@ int pkv_create(const pkv_config* cfg, void* d_workspace, size_t workspace_bytes,
   if (reinterpret_cast<uintptr_t>(d_workspace) & 255) return PKV_ERR_INVALID_ARG;
   int dev, sms;
   if (device_sms(&dev, &sms) != PKV_OK) return PKV_ERR_CUDA;
-  Layout lay = make_layout(*cfg, sms);
+  Layout lay = make_layout(*cfg, sms, true);
   if (workspace_bytes < lay.total) return PKV_ERR_CAPACITY;
   if (get_encoder() != PKV_OK) return PKV_ERR_CUDA;
   pkv_ctx* c = new (std::nothrow) pkv_ctx();
@@ -353,15 +361,13 @@ int pkv_forward_decode(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, cons
 
 int pkv_forward_extend(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, const void* d_v_pool, float sm_scale,
                        float k_scale, float v_scale, void* d_out, float* d_lse, void* stream) {
-  (void)k_scale;
-  (void)v_scale;
   int st = check_forward_args(ctx, d_q, d_k_pool, d_v_pool, d_out, d_lse);
   if (st != PKV_OK) return st;
   st = check_scales(*ctx, sm_scale, k_scale, v_scale);
   if (st != PKV_OK) return st;
-  if (ctx->cfg.kv_dtype != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
   if (ctx->batch == 0) return PKV_OK;
-  return launch_extend(*ctx, d_q, d_k_pool, d_v_pool, sm_scale, d_out, d_lse, static_cast<cudaStream_t>(stream));
+  return launch_extend(*ctx, d_q, d_k_pool, d_v_pool, sm_scale, k_scale, v_scale, d_out, d_lse,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int pkv_forward(pkv_ctx* ctx, int forward_mode, int spec_mode, const void* d_q, const void* d_k_pool,

@@ -75,6 +75,11 @@ struct ExtendTile {
 struct Layout {
   size_t plan, kv_indptr, kv_indices, kv_last_page_len, qo_indptr, kv_len, n_splits, ext_splits, partial_indptr,
       token_req, decode_items, extend_tiles, partial_o, partial_lse, total;
+  // E4M3 pools on the extend path: bf16 copies of the codes of the batch's
+  // pages (K and V, max_pages_total pages each) and the identity page list
+  // that reads them; absent (has_stage false) for bf16 pools
+  size_t stage_k, stage_v, stage_idx;
+  bool has_stage;
   int max_decode_items, max_extend_tiles, partial_rows_cap;
 };
 
@@ -125,8 +130,8 @@ int launch_set_kv_buffer(Ctx& c, void* k_pool, void* v_pool, const int32_t* loc,
                          int n, float k_inv, float v_inv, cudaStream_t st);
 int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
                   float v_scale, void* out, float* lse, cudaStream_t st);
-int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, void* out,
-                  float* lse, cudaStream_t st);
+int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+                  float v_scale, void* out, float* lse, cudaStream_t st);
 // LSE merge of split partials for requests whose rows per KV head are at most
 // max_rows_per_head (the decode path: its largest tile; the extend path: 256,
 // the requests it split).

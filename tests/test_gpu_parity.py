@@ -412,14 +412,26 @@ def test_extend_nan_unused_slots_never_read():
     assert torch.isfinite(d.out.float()).all() and torch.isfinite(d.lse).all()
 
 
-def test_extend_fp8_pool_unsupported():
-    W = make_workload("e8", "extend", 1, 8, 2, 128, [10], [20], kv_dtype="fp8_e4m3")
-    d = DeviceBatch(W)
-    d.set_kv_buffer()
-    d.build_metadata()
-    with pytest.raises(B.PkvError) as ei:
-        d.forward()
-    assert ei.value.status == B.PKV_ERR_UNSUPPORTED
+@pytest.mark.parametrize("case", ["small", "g16", "long_prefix", "verify_prefill", "with_sinks"])
+def test_extend_fp8_pool(case):
+    """E4M3 pools on the extend path: the batch's pages are widened into a
+    bf16 copy of the codes, k_scale goes into the score scale and v_scale
+    into the output; every row against the oracle's exact E4M3 decoding."""
+    spec = B.PKV_SPEC_PREFILL
+    if case == "small":
+        W = make_workload("e8", "extend", 3, 8, 2, 128, [10, 0, 300], [20, 130, 7], kv_dtype="fp8_e4m3")
+    elif case == "g16":
+        W = make_workload("e8g", "extend", 3, 32, 2, 128, [500, 33, 0], [64, 1, 200], kv_dtype="fp8_e4m3")
+    elif case == "long_prefix":
+        W = make_workload("e8l", "extend", 2, 32, 8, 128, [6000, 2500], [300, 45], kv_dtype="fp8_e4m3")
+    elif case == "verify_prefill":
+        rng = np.random.default_rng(48)
+        W = make_workload("e8v", "verify", 6, 64, 4, 128, rng.integers(100, 3000, 6), rng.integers(4, 9, 6),
+                          kv_dtype="fp8_e4m3")
+    else:
+        W = make_workload("e8s", "extend", 3, 16, 4, 128, [700, 0, 90], [50, 300, 1], kv_dtype="fp8_e4m3")
+        W.sinks = random_sinks(W.num_q_heads, seed=14)
+    full_check(W, spec_mode=spec)
 
 
 def test_full_size_extend_sampled():
@@ -498,8 +510,6 @@ def test_tree_verify_parity(case, spec):
     elif case == "g4_32_drafts":
         W = _tree_verify("tv32", 4, 16, 4, 128, 32, 43)
     else:
-        if spec == "prefill":
-            pytest.skip("E4M3 pools run on the decode path only")
         W = _tree_verify("tv8f", 4, 32, 4, 128, 16, 44, kv_dtype="fp8_e4m3")
     full_check(W, spec_mode=B.PKV_SPEC_PREFILL if spec == "prefill" else B.PKV_SPEC_DECODE)
 
