@@ -215,12 +215,10 @@ struct ExtendArgs {
   int out_32B;       // out is 32-byte aligned: output rows are written with 32-byte stores
   const uint64_t* tree;  // draft-tree mask word per query token, or null (chain drafts)
   const float* sinks;    // sink logit per query head, or null
-  float v_scale;         // multiplies every written row (E4M3 pools; 1 otherwise), EXTRAS only
 };
 
-// EXTRAS: draft-tree mask words, attention sinks or an E4M3 pool's value scale
-// are in use (a separate instantiation, so plain batches run the causal
-// kernel without that code).
+// EXTRAS: draft-tree mask words or attention sinks are in use (a separate
+// instantiation, so plain batches run the causal kernel without that code).
 template <class C, bool EXTRAS>
 __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                    const __grid_constant__ CUtensorMap tmap_v,
@@ -806,7 +804,6 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       }
       float inv = l > 0.f ? 1.f / l : 0.f;
       if constexpr (EXTRAS) {
-        inv *= a.v_scale;
         // final rows of a model with sinks: the head's sink joins the normaliser
         if (!split && valid && a.sinks) {
           float lse_s = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
@@ -887,23 +884,24 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   }
 }
 
-// E4M3 pools on the extend path: the codes of the batch's pages, in
-// kv_indices order, widened to bf16 (exact: every E4M3 value is a bf16
-// value) into a compact copy whose page i is the batch's i-th page, plus the
-// identity page list idx[i] = i through which the extend kernel reads it.
-// One thread widens 16 codes (one 16-byte vector) of K and of V.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
-  const uint32_t h = e4m3x2_to_f16x2(v);
+// E4M3 pools on the extend path: the batch's pages, in kv_indices order,
+// dequantised (code * scale, rounded once to bf16) into a compact copy whose
+// page i is the batch's i-th page, plus the identity page list idx[i] = i
+// through which the extend kernel reads it. One thread converts 16 codes
+// (one 16-byte vector) of K and of V.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint16_t v, float scale) {
+  const uint32_t h = e4m3x2_to_f16x2(v);  // exact
   float lo, hi;
   asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h & 0xffffu)));
   asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h >> 16)));
-  return pack_bf16(lo, hi);
+  return pack_bf16(lo * scale, hi * scale);
 }
 
 __global__ void __launch_bounds__(256) fp8_stage_kernel(const uint8_t* __restrict__ kp, const uint8_t* __restrict__ vp,
                                                         uint16_t* __restrict__ sk, uint16_t* __restrict__ sv,
                                                         int* __restrict__ idx, const int* __restrict__ kv_indices,
-                                                        const int* __restrict__ plan, int page_elems) {
+                                                        const int* __restrict__ plan, int page_elems, float k_scale,
+                                                        float v_scale) {
   pdl_launch_dependents();
   pdl_wait();  // the page list comes from the metadata build before this launch
   const int np = plan[kTotalPages];
@@ -919,10 +917,10 @@ __global__ void __launch_bounds__(256) fp8_stage_kernel(const uint8_t* __restric
     uint32_t ko[8], vo[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      ko[2 * j] = e4m3x2_to_bf16x2((uint16_t)(kw[j] & 0xffffu));
-      ko[2 * j + 1] = e4m3x2_to_bf16x2((uint16_t)(kw[j] >> 16));
-      vo[2 * j] = e4m3x2_to_bf16x2((uint16_t)(vw[j] & 0xffffu));
-      vo[2 * j + 1] = e4m3x2_to_bf16x2((uint16_t)(vw[j] >> 16));
+      ko[2 * j] = e4m3x2_to_bf16x2_scaled((uint16_t)(kw[j] & 0xffffu), k_scale);
+      ko[2 * j + 1] = e4m3x2_to_bf16x2_scaled((uint16_t)(kw[j] >> 16), k_scale);
+      vo[2 * j] = e4m3x2_to_bf16x2_scaled((uint16_t)(vw[j] & 0xffffu), v_scale);
+      vo[2 * j + 1] = e4m3x2_to_bf16x2_scaled((uint16_t)(vw[j] >> 16), v_scale);
     }
     *reinterpret_cast<uint4*>(sk + dst) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
     *reinterpret_cast<uint4*>(sk + dst + 8) = make_uint4(ko[4], ko[5], ko[6], ko[7]);
@@ -948,7 +946,8 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
     const int page_elems = c.cfg.page_size * c.cfg.num_kv_heads * C::D;
     if (launch_pdl(fp8_stage_kernel, dim3((unsigned)(c.num_sms * 4)), dim3(256), 0, st,
                    static_cast<const uint8_t*>(k_pool), static_cast<const uint8_t*>(v_pool), sk, sv, idx,
-                   make_meta(c).kv_indices, static_cast<const int*>(make_meta(c).plan), page_elems) != cudaSuccess)
+                   make_meta(c).kv_indices, static_cast<const int*>(make_meta(c).plan), page_elems, k_scale,
+                   v_scale) != cudaSuccess)
       return PKV_ERR_CUDA;
     k_pool = sk;
     v_pool = sv;
@@ -968,8 +967,8 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.num_q_heads = c.cfg.num_q_heads;
   a.num_kv_heads = c.cfg.num_kv_heads;
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
-  a.scale_log2 = sm_scale * (fp8 ? k_scale : 1.f) * kLog2e;
-  a.v_scale = fp8 ? v_scale : 1.f;
+  // an E4M3 pool's scales are already in the dequantised copy
+  a.scale_log2 = sm_scale * kLog2e;
   if (fp8) a.m.kv_indices = reinterpret_cast<const int*>(c.ws + c.lay.stage_idx);
   a.out_32B = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
   a.tree = active_tree(c);
@@ -993,7 +992,7 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
     a.q_tma = 1;
     a.q_box_tokens = (int)box_tok;
   }
-  auto kernel = (a.tree || a.sinks || fp8) ? extend_tc_kernel<C, true> : extend_tc_kernel<C, false>;
+  auto kernel = (a.tree || a.sinks) ? extend_tc_kernel<C, true> : extend_tc_kernel<C, false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (launch_pdl(kernel, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, tq, a) != cudaSuccess)
