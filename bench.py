@@ -49,9 +49,9 @@ NCU_TRAFFIC = {
                                             "source": "profiles/dram_traffic_fp8_and_verify.md"},
     ("decode_splitkv", "spec_verify"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 601473024,
                                         "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("extend_tc", "prefix_extend"): {"src_sha": "6e52fe7fd3947dc0", "bytes_per_launch": 927089920,
+    ("extend_tc", "prefix_extend"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 967569664,
                                      "source": "profiles/extend_tc_prefix_extend.md"},
-    ("extend_tc", "spec_verify"): {"src_sha": "6e52fe7fd3947dc0", "bytes_per_launch": 599929344,
+    ("extend_tc", "spec_verify"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 599880704,
                                    "source": "profiles/dram_traffic_fp8_and_verify.md"},
 }
 
