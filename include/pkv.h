@@ -96,8 +96,8 @@ typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
  * metadata buffer in the workspace, so captured graphs can be replayed.
  * Supported: head_dim 64 or 128; page_size 16; num_q_heads a multiple of
  * num_kv_heads with a group size num_q_heads / num_kv_heads of at most 16;
- * FP8 KV on the decode path only (forward_extend with an FP8 pool returns
- * PKV_ERR_UNSUPPORTED). */
+ * E4M3 (FP8) pools with head_dim 128 on both paths (head_dim 64 with an
+ * E4M3 pool returns PKV_ERR_UNSUPPORTED). */
 typedef struct {
   int32_t num_q_heads;
   int32_t num_kv_heads;
