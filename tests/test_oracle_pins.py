@@ -568,3 +568,26 @@ def test_select_path_truth_table():
     for m, s, p in rows:
         assert oracle.select_path(m, s) == p
     assert oracle.select_path(7, 0) == -1 and oracle.select_path(0, 5) == -1
+
+
+def test_random_tree_masks_are_trees():
+    """The seeded draft trees are valid inputs: each word holds its own bit,
+    no later draft, and its parent's word (a tree laid out parents first)."""
+    qo = [1, 5, 17, 64, 8]
+    words = random_tree_masks(qo, seed=21)
+    assert words.dtype == np.uint64 and words.shape == (sum(qo),)
+    off = 0
+    branched = False
+    for n in qo:
+        w = [int(x) for x in words[off:off + n]]
+        for i in range(n):
+            assert (w[i] >> i) & 1
+            assert w[i] >> (i + 1) == 0
+            below = w[i] & ((1 << i) - 1)
+            if below:
+                parent = below.bit_length() - 1  # the highest set bit below i is the parent
+                assert w[parent] == below
+            branched |= w[i] != (1 << (i + 1)) - 1
+        off += n
+    assert branched
+    assert np.array_equal(chain_tree_masks([3]), np.array([1, 3, 7], dtype=np.uint64))
