@@ -290,7 +290,7 @@ static int key_visible(const uint64_t* tree_mask, uint64_t word, int p, int pref
   return (int)((word >> (p - prefix)) & 1u);
 }
 
-static int attention_row(const attn_job* j, int t, int h, double* scores, double* o, double* lse) {
+static int attention_row(const attn_job* j, int t, int h, double* scores, double* qd, double* o, double* lse) {
   int D = j->head_dim;
   int b = 0;
   while (b < j->bs && j->qo_indptr[b + 1] <= t) ++b;
@@ -307,6 +307,7 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
   for (int p = 0; p <= limit; ++p) n_vis += key_visible(j->tree_mask, word, p, prefix, limit);
   int g = h / (j->num_q_heads / j->num_kv_heads);
   const uint16_t* qrow = j->q + ((int64_t)t * j->num_q_heads + h) * D;
+  for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_decode(qrow[d]); /* the row's query, widened once */
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   double sink = j->sinks ? j->sinks[h] : -INFINITY;
   if (n_vis == 0) { /* no visible key: empty request (graph padding) or an empty mask row */
@@ -321,7 +322,7 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
     int64_t slot = (int64_t)page * j->page_size + p % j->page_size;
     int64_t base = (slot * j->num_kv_heads + g) * D;
     double dot = 0.0;
-    for (int d = 0; d < D; ++d) dot += oracle_bf16_decode(qrow[d]) * kv_value(j->k_pool, j->kv_dtype, base + d, j->k_scale);
+    for (int d = 0; d < D; ++d) dot += qd[d] * kv_value(j->k_pool, j->kv_dtype, base + d, j->k_scale);
     scores[p] = j->sm_scale * dot;
     if (scores[p] > m) m = scores[p];
   }
@@ -346,7 +347,10 @@ static void* attention_worker(void* arg) {
   attn_worker* w = (attn_worker*)arg;
   attn_job* j = w->job;
   double* scores = (double*)malloc(sizeof(double) * (size_t)(j->max_kv_len > 0 ? j->max_kv_len : 1));
-  if (!scores) {
+  double* qd = (double*)malloc(sizeof(double) * (size_t)j->head_dim);
+  if (!scores || !qd) {
+    free(scores);
+    free(qd);
     w->status = ORACLE_ERR_NOMEM;
     return NULL;
   }
@@ -359,10 +363,11 @@ static void* attention_worker(void* arg) {
       t = (int)(r / j->num_q_heads);
       h = (int)(r % j->num_q_heads);
     }
-    int st = attention_row(j, t, h, scores, j->out_o + r * j->head_dim, j->out_lse + r);
+    int st = attention_row(j, t, h, scores, qd, j->out_o + r * j->head_dim, j->out_lse + r);
     if (st != ORACLE_OK) w->status = st;
   }
   free(scores);
+  free(qd);
   return NULL;
 }
 
