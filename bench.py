@@ -40,19 +40,15 @@ METRIC = "paged decode KV GB/s (% HBM peak); extend TFLOP/s (% bf16 peak); µs/c
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM traffic per launch of the dominant kernel from one ncu capture
-# (profiles/), valid only while the kernel source is unchanged.
+# DRAM traffic per launch of the dominant kernel from one ncu capture of the
+# workload (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the
+# kernel's source file is unchanged (src_sha: first 16 hex digits of its sha256).
 NCU_TRAFFIC = {
-    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1386555136,
-                                             "source": "profiles/decode_splitkv_llama3_8b_decode.md"},
-    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1504556032,
-                                            "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("decode_splitkv", "spec_verify"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 601473024,
-                                        "source": "profiles/dram_traffic_fp8_and_verify.md"},
-    ("extend_tc", "prefix_extend"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 967569664,
-                                     "source": "profiles/extend_tc_prefix_extend.md"},
-    ("extend_tc", "spec_verify"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 599880704,
-                                   "source": "profiles/dram_traffic_fp8_and_verify.md"},
+    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1386555136},
+    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1504556032},
+    ("decode_splitkv", "spec_verify"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 601473024},
+    ("extend_tc", "prefix_extend"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 967569664},
+    ("extend_tc", "spec_verify"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 599880704},
 }
 
 
@@ -175,7 +171,9 @@ def metric_value(W, work, seconds):
 
 
 def oracle_sample(W, budget_s=15.0):
-    """Time the fp64 oracle on whole requests of W until about budget_s of CPU work."""
+    """Time the fp64 oracle on a bounded sample of W: whole requests (every
+    query head) for decode and verify, blocks of query tokens (every head) for
+    extend, until about budget_s of wall time on all host cores."""
     sys.path.insert(0, ROOT)
     import oracle
     from tests._pipeline import oracle_pools
@@ -187,29 +185,48 @@ def oracle_sample(W, budget_s=15.0):
     qbits = bf16_bits(W.q)
     nthreads = os.cpu_count() or 1
     kv = oracle.KV_FP8_E4M3 if W.is_fp8 else oracle.KV_BF16
-    done_kv = done_pairs = 0
-    t0 = time.perf_counter()
-    n_req = 0
     esz = 1 if W.is_fp8 else 2
+    block = 8 if W.mode == "extend" else 1 << 30  # tokens per oracle call
+    done_kv = done_pairs = done_tok = 0
+    reqs = set()
+    t0 = time.perf_counter()
     for b in range(W.bs):
-        rows = [(t, h) for t in range(qo_indptr[b], qo_indptr[b + 1]) for h in range(W.num_q_heads)]
-        if not rows:
-            continue
-        oracle.attention(qbits, kp, vp, meta, W.num_q_heads, W.num_kv_heads, W.page_size, W.sm_scale, kv_dtype=kv,
-                         k_scale=W.k_scale, v_scale=W.v_scale, rows=np.array(rows), nthreads=nthreads)
+        q0, q1 = int(qo_indptr[b]), int(qo_indptr[b + 1])
         L, N = int(W.seq_lens[b]), int(W.qo_lens[b])
-        done_kv += L * W.num_kv_heads * W.head_dim * esz * 2
-        done_pairs += N * (L - N) + N * (N + 1) // 2
-        n_req += 1
+        for t_lo in range(q0, q1, min(block, max(q1 - q0, 1))):
+            t_hi = min(q1, t_lo + block)
+            rows = np.array([(t, h) for t in range(t_lo, t_hi) for h in range(W.num_q_heads)], dtype=np.int32)
+            oracle.attention(qbits, kp, vp, meta, W.num_q_heads, W.num_kv_heads, W.page_size, W.sm_scale,
+                             kv_dtype=kv, k_scale=W.k_scale, v_scale=W.v_scale, rows=rows, nthreads=nthreads)
+            # token i of the request sees L - N + i + 1 keys
+            done_pairs += sum(L - N + (t - q0) + 1 for t in range(t_lo, t_hi))
+            done_tok += t_hi - t_lo
+            reqs.add(b)
+            if t_hi == q1:
+                done_kv += L * W.num_kv_heads * W.head_dim * esz * 2
+            if time.perf_counter() - t0 > budget_s:
+                break
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
     if W.mode == "extend":
         val, unit = 4 * W.head_dim * W.num_q_heads * done_pairs / dt / 1e12, "TFLOP/s"
+        what = f"{done_tok} of {W.total_q} query tokens in {len(reqs)} of {W.bs} requests"
     else:
         val, unit = done_kv / dt / 1e9, "GB/s"
+        what = f"{len(reqs)} of {W.bs} requests"
     return {"value": val, "unit": unit, "cores": nthreads, "kind": "oracle",
-            "sample": f"{n_req} of {W.bs} requests (all query heads), {dt:.1f} s, fp64 C oracle"}, dt
+            "sample": f"{what} (all query heads), {dt:.1f} s, fp64 C oracle"}, dt
+
+
+def config_of(W, spec_mode, world):
+    """The workload as the JSON line names it (both arms print the same keys)."""
+    return {"workload": W.name, "batch": W.bs, "num_q_heads": W.num_q_heads, "num_kv_heads": W.num_kv_heads,
+            "head_dim": W.head_dim, "page_size": W.page_size, "kv_dtype": W.kv_dtype, "mode": W.mode,
+            "spec_mode": spec_mode, "total_kv_tokens": int(W.seq_lens.sum()), "total_q_rows": W.total_q,
+            "l2": "inputs larger than L2 (K+V pools "
+                  f"{2 * W.k_pool.numel() * W.k_pool.element_size() / 1e9:.2f} GB)",
+            "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args, W, rank, world):
@@ -227,9 +244,7 @@ def run_reference(args, W, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": cpu["unit"], "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": W.name, "batch": W.bs, "num_q_heads": W.num_q_heads,
-                       "num_kv_heads": W.num_kv_heads, "head_dim": W.head_dim, "page_size": W.page_size,
-                       "kv_dtype": W.kv_dtype},
+            "config": config_of(W, args.spec_mode, world),
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": cpu["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -320,8 +335,9 @@ def timed_steps(d, spec, steps, world):
     return step_s, fwd_s
 
 
-def secondary(name, spec_name, local, steps, world):
-    """Short measurement of another workload (no e2e / CPU baseline)."""
+def secondary(name, spec_name, local, steps, world, cpu_budget):
+    """Short measurement of another workload (no e2e), with the oracle timed
+    beside it on a bounded sample (rank 0 of a single-GPU run only)."""
     from paged_kv_cache_15_gb300 import binding as B
     from paged_kv_cache_15_gb300.runner import DeviceBatch
     from paged_kv_cache_15_gb300.workloads import preset
@@ -347,9 +363,11 @@ def secondary(name, spec_name, local, steps, world):
            "graph_step_us": graph_step_us(d, step, steps, torch.cuda.current_stream()),
            "roofline_frac": roof["frac"], "achieved": roof["achieved"], "achieved_unit": roof["unit"],
            "kernel": roof["kernel"], "path": "decode" if roof["kernel"] == "decode_splitkv" else "extend",
-           "steps": steps}
+           "steps": steps, "cpu_baseline": None}
     del d
     torch.cuda.empty_cache()
+    if world == 1 and cpu_budget > 0:
+        out["cpu_baseline"], _ = oracle_sample(W, budget_s=cpu_budget)
     return out
 
 
@@ -427,12 +445,13 @@ def run_ours(args, W, rank, world, local):
     # --- the other named workloads of the metric, short runs
     others = {}
     if not args.no_secondary:
-        for name, sp in (("tiny_decode", "prefill"), ("prefix_extend", "prefill"), ("spec_verify", "decode"),
-                         ("spec_verify", "prefill"), ("long_fp8_decode", "prefill")):
+        for name, sp in (("tiny_decode", "prefill"), ("prefix_extend", "prefill"), ("prefix_extend_fp8", "prefill"),
+                         ("spec_verify", "decode"), ("spec_verify", "prefill"), ("long_fp8_decode", "prefill")):
             if name == W.name and sp == args.spec_mode:
                 continue
             key = name if name != "spec_verify" else f"spec_verify/{sp}_path"
-            others[key] = secondary(name, sp, local, args.secondary_steps, world)
+            others[key] = secondary(name, sp, local, args.secondary_steps, world,
+                                    0.0 if args.no_cpu_baseline else args.secondary_cpu_budget)
 
     if rank != 0:
         return
@@ -447,13 +466,7 @@ def run_ours(args, W, rank, world, local):
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8_e4m3 kv / bf16 q" if W.is_fp8 else "bf16",
             "data": "synthetic",
-            "config": {"workload": W.name, "batch": W.bs, "num_q_heads": W.num_q_heads,
-                       "num_kv_heads": W.num_kv_heads, "head_dim": W.head_dim, "page_size": W.page_size,
-                       "kv_dtype": W.kv_dtype, "mode": W.mode, "spec_mode": args.spec_mode,
-                       "total_kv_tokens": int(W.seq_lens.sum()), "total_q_rows": W.total_q,
-                       "l2": "inputs larger than L2 (K+V pools "
-                             f"{2 * W.k_pool.numel() * W.k_pool.element_size() / 1e9:.2f} GB)",
-                       "parallelism": f"replicas x{world}"},
+            "config": config_of(W, args.spec_mode, world),
             "us_per_call": fwd_s * 1e6,
             "step_us": step_s * 1e6,
             "graph_step_us": graph_us,
@@ -482,6 +495,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-secondary", action="store_true", help="skip the short runs of the other workloads")
     ap.add_argument("--secondary-steps", type=int, default=30)
+    ap.add_argument("--secondary-cpu-budget", type=float, default=6.0,
+                    help="seconds of oracle time beside each of the other workloads")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     from paged_kv_cache_15_gb300.workloads import preset

@@ -65,7 +65,7 @@ extern "C" {
 
 /* Device error word values (pkv_get_device_error). */
 #define PKV_DEV_OK 0
-#define PKV_DEV_BAD_LENGTH 1   /* seq_len < 0, qo_len < 0 or qo_len > seq_len */
+#define PKV_DEV_BAD_LENGTH 1   /* seq_len < 0, qo_len < 0, qo_len > seq_len, or ceil(seq_len / page_size) > page_table_stride */
 #define PKV_DEV_BAD_PAGE 2     /* page id outside [0, num_pages) */
 #define PKV_DEV_CAPACITY 3     /* total pages / query rows beyond the configured capacity */
 #define PKV_DEV_BAD_SLOT 4     /* set_kv_buffer loc outside [0, num_pages * page_size) */
@@ -152,7 +152,11 @@ int pkv_select_backend(int forward_mode, int spec_mode);
  * page_table_stride entries. forward_mode selects nothing here (both paths'
  * plans are built); it is checked for validity, and IDLE (or batch == 0)
  * builds an empty plan. Errors: INVALID_ARG, CAPACITY (batch > max_batch),
- * CUDA. Data errors are recorded on the device. */
+ * CUDA. Data errors are recorded on the device: a request with negative
+ * lengths, more query rows than keys, or more pages than one page-table row
+ * holds (ceil(seq_len / page_size) > page_table_stride) records
+ * PKV_DEV_BAD_LENGTH and is treated as empty (output 0, LSE -inf); its row of
+ * the page table is not read. */
 int pkv_build_metadata(pkv_ctx* ctx, int forward_mode, int32_t batch, const int32_t* d_seq_lens,
                        const int32_t* d_qo_lens, const int32_t* d_page_table, int32_t page_table_stride,
                        void* stream);
@@ -273,6 +277,8 @@ int pkv_describe(pkv_ctx* ctx, char* buf, size_t n);
  *     PKV_ERR_CAPACITY and launches nothing.
  *   - d_error (device int32, nullable) receives the device error word of this
  *     call (PKV_DEV_*), written on `stream` after the kernels.
+ *   - The array used is the one of the CURRENT device (cudaGetDevice), so
+ *     `stream` must belong to the current device.
  *   - The first call on each device looks up the array's device address; make
  *     that first call before any stream capture on that device.
  *   - Every call on a device shares the one array, and it keeps the previous

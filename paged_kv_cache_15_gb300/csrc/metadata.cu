@@ -80,10 +80,14 @@ struct MetaArgs {
   int max_tiles;
 };
 
+// A request's lengths as given, validated: negative lengths, more query rows
+// than keys, and a KV length whose pages do not fit one page-table row (the
+// gather would read past the row, into the next request's or past the table)
+// mark it bad, and a bad request is treated as empty.
 __device__ __forceinline__ void raw_lengths(const MetaArgs& a, int b, int& L, int& qo, bool& bad) {
   L = a.seq_lens[b];
   qo = a.qo_lens ? a.qo_lens[b] : 1;
-  bad = (L < 0) || (qo < 0) || (L > 0 && qo > L);
+  bad = (L < 0) || (qo < 0) || (L > 0 && qo > L) || (L > 0 && (L - 1) / kPageSize >= a.stride);
   if (bad) {
     L = 0;
     qo = qo < 0 ? 0 : qo;
@@ -106,12 +110,15 @@ __device__ __forceinline__ void lengths(const MetaArgs& a, int b, int& L, int& q
   }
 }
 
+// pages of a validated length (no overflow near INT_MAX)
+__device__ __forceinline__ int pages_of(int L) { return L > 0 ? (L - 1) / kPageSize + 1 : 0; }
+
 __device__ __forceinline__ int kv_tiles_of(int np) { return (np + kPagesPerKvTile - 1) / kPagesPerKvTile; }
 
 __device__ __forceinline__ ReqInfo req_info(const MetaArgs& a, int b, int chunk, int ext_ct) {
   ReqInfo r;
   lengths(a, b, r.L, r.qo, r.bad);
-  r.np = (r.L + kPageSize - 1) / kPageSize;
+  r.np = pages_of(r.L);
   r.nsplit = r.np > 0 ? (r.np + chunk - 1) / chunk : 1;
   r.prow = r.nsplit > 1 ? r.nsplit * r.qo : 0;
   r.qtiles = (r.qo * a.group + kExtendUnitRows - 1) / kExtendUnitRows;
@@ -218,7 +225,7 @@ __device__ int extend_split_tiles(const MetaArgs& a, int chunk, const Sums& tot)
     int L, qo;
     bool bad;
     lengths(a, b, L, qo, bad);
-    const int np = (L + kPageSize - 1) / kPageSize;
+    const int np = pages_of(L);
     const int qt = (qo * a.group + kExtendUnitRows - 1) / kExtendUnitRows;
     if (qt == 1 && np > chunk)
       split_units += (kv_tiles_of(np) + ct - 1) / ct;
@@ -292,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
     bool bad;
     raw_lengths(a, b, L, qo, bad);
     if (b < kLenCache) s_len_cache[b] = make_int2(L, bad ? (int)((unsigned)qo | 0x80000000u) : qo);
-    long long np = (L + kPageSize - 1) / kPageSize;
+    long long np = pages_of(L);
     s.np += np;
     s.qo += qo;
     s.npqo += np * qo;

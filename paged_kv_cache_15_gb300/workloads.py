@@ -230,12 +230,23 @@ def _randint(gen, lo, hi, n):
 # --------------------------------------------------------------------------
 
 PRESETS = ("tiny_decode", "llama3_8b_decode", "prefix_extend", "spec_verify", "long_fp8_decode")
+# E4M3 pools on the prefix-cached extend case: the same lengths and values,
+# with the cached prefix quantised on the host and the new tokens quantised by
+# set_kv_buffer
+VARIANTS = ("prefix_extend_fp8",)
 
 
-def preset(name: str, bs: Optional[int] = None, len_scale: float = 1.0) -> Workload:
+def preset(name: str, bs: Optional[int] = None, len_scale: float = 1.0, page_size: int = 16,
+           kv_dtype: Optional[str] = None) -> Workload:
     """The five cases at full size (defaults), or with fewer requests / shorter
-    lengths (``len_scale`` multiplies every length bound) for quick parity runs."""
+    lengths (``len_scale`` multiplies every length bound) for quick parity runs.
+    ``page_size`` and ``kv_dtype`` override the case's page size (16) and pool
+    element type; the lengths, pages and values are drawn the same way."""
     g = torch.Generator().manual_seed(0)
+    ps = page_size
+
+    def kvd(default):
+        return kv_dtype if kv_dtype is not None else default
 
     def lens(lo, hi, n):
         lo2 = max(1, int(round(lo * len_scale)))
@@ -248,23 +259,28 @@ def preset(name: str, bs: Optional[int] = None, len_scale: float = 1.0) -> Workl
         if bs is not None:
             L = L[:bs]
         n = L.shape[0]
-        return make_workload(name, "decode", n, 8, 2, 64, L - 1, np.ones(n), num_pages=128)
+        # a 128-page pool of 16-token pages (2,048 slots), the same slots at other page sizes
+        return make_workload(name, "decode", n, 8, 2, 64, L - 1, np.ones(n), page_size=ps,
+                             num_pages=max(128 * 16 // ps, 1 + int(((L + ps - 1) // ps).sum())),
+                             kv_dtype=kvd("bf16"))
     if name == "llama3_8b_decode":
         n = 64 if bs is None else bs
         L = lens(1024, 8192, n)
-        return make_workload(name, "decode", n, 32, 8, 128, L - 1, np.ones(n))
-    if name == "prefix_extend":
+        return make_workload(name, "decode", n, 32, 8, 128, L - 1, np.ones(n), page_size=ps, kv_dtype=kvd("bf16"))
+    if name in ("prefix_extend", "prefix_extend_fp8"):
         n = 8 if bs is None else bs
         P = _randint(g, 0, int(round(4096 * len_scale)), n)
         N = lens(128, 2048, n)
-        return make_workload(name, "extend", n, 32, 8, 128, P, N)
+        dt = kvd("fp8_e4m3" if name == "prefix_extend_fp8" else "bf16")
+        return make_workload(name, "extend", n, 32, 8, 128, P, N, page_size=ps, kv_dtype=dt)
     if name == "spec_verify":
         n = 32 if bs is None else bs
         ctx = lens(2048, 16384, n)
         N = _randint(g, 4, 8, n)
-        return make_workload(name, "verify", n, 64, 4, 128, ctx, N)
+        return make_workload(name, "verify", n, 64, 4, 128, ctx, N, page_size=ps, kv_dtype=kvd("bf16"))
     if name == "long_fp8_decode":
         n = 8 if bs is None else bs
         L = lens(32768, 131072, n)
-        return make_workload(name, "decode", n, 32, 8, 128, L - 1, np.ones(n), kv_dtype="fp8_e4m3")
+        return make_workload(name, "decode", n, 32, 8, 128, L - 1, np.ones(n), page_size=ps,
+                             kv_dtype=kvd("fp8_e4m3"))
     raise KeyError(name)

@@ -34,21 +34,3 @@ def oracle_reference(W: Workload, rows=None, pools=None, nthreads=None):
                             W.sm_scale, kv_dtype=kv, k_scale=W.k_scale, v_scale=W.v_scale, rows=rows,
                             nthreads=nthreads, tree_mask=W.tree_mask,
                             sinks=None if W.sinks is None else W.sinks.astype(np.float64))
-
-
-def sample_rows(W: Workload, n: int, seed: int = 123):
-    """A seeded sample of (token, head) rows that always includes the first and
-    last token of every request (the causal diagonal ends)."""
-    rng = np.random.default_rng(seed)
-    T = W.total_q
-    qo_indptr = np.concatenate([[0], np.cumsum(W.qo_lens)])
-    toks = set()
-    for b in range(W.bs):
-        if W.qo_lens[b]:
-            toks.add(int(qo_indptr[b]))
-            toks.add(int(qo_indptr[b + 1] - 1))
-    toks = sorted(toks)
-    rows = [(t, int(rng.integers(0, W.num_q_heads))) for t in toks]
-    rest = max(0, n - len(rows))
-    rows += [(int(rng.integers(0, T)), int(rng.integers(0, W.num_q_heads))) for _ in range(rest)]
-    return np.array(rows, dtype=np.int32)

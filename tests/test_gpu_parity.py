@@ -14,7 +14,7 @@ from paged_kv_cache_15_gb300 import binding as B
 from paged_kv_cache_15_gb300.runner import DeviceBatch, config_for
 from paged_kv_cache_15_gb300.workloads import (chain_tree_masks, make_workload, pool_bits, preset, random_sinks,
                                                random_tree_masks)
-from tests._pipeline import oracle_meta, oracle_pools, oracle_reference, sample_rows
+from tests._pipeline import oracle_meta, oracle_pools, oracle_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -55,18 +55,6 @@ def full_check(W, spec_mode=B.PKV_SPEC_PREFILL):
     ref_o, ref_lse = oracle_reference(W)
     check_close(d.out.double().cpu().numpy(), ref_o, "o")
     check_close(d.lse.double().cpu().numpy(), ref_lse, "lse")
-    return d
-
-
-def sampled_check(W, n_rows=96, spec_mode=B.PKV_SPEC_PREFILL):
-    d = run_path(W, spec_mode)
-    rows = sample_rows(W, n_rows)
-    ref_o, ref_lse = oracle_reference(W, rows=rows)
-    out = d.out.double().cpu().numpy()
-    lse = d.lse.double().cpu().numpy()
-    check_close(out[rows[:, 0], rows[:, 1]], ref_o, "o (sampled)")
-    check_close(lse[rows[:, 0], rows[:, 1]], ref_lse, "lse (sampled)")
-    assert np.isfinite(out).all() and np.isfinite(lse).all()
     return d
 
 
@@ -240,14 +228,41 @@ def test_verify_decode_path_fp8():
     full_check(W, spec_mode=B.PKV_SPEC_DECODE)
 
 
-# ------------------------------------------------------------------ full sizes, sampled rows
+# ------------------------------------------------------------------ full sizes, every row
+FULL_PRESETS = ["tiny_decode", "llama3_8b_decode", "prefix_extend", "prefix_extend_fp8", "spec_verify",
+                "long_fp8_decode"]
+
+
+@pytest.mark.parametrize("name", FULL_PRESETS)
+def test_full_size_metadata_and_pools_bit_exact(name):
+    """Every named case at its full size: the pools after set_kv_buffer (every
+    byte, untouched NaN slots included) and the metadata, bit for bit."""
+    W = preset(name)
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    d.build_metadata()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    kp, vp = oracle_pools(W)
+    assert np.array_equal(pool_bits(d.k_pool.cpu()), kp)
+    assert np.array_equal(pool_bits(d.v_pool.cpu()), vp)
+    del kp, vp
+    ref = oracle_meta(W)
+    p_indptr, p_indices, p_last, p_qo = B.pkv_get_metadata(d.ctx)
+    n_pages = int(ref["kv_indptr"][-1])
+    assert np.array_equal(workspace_ints(d, p_indptr, W.bs + 1), ref["kv_indptr"])
+    assert np.array_equal(workspace_ints(d, p_indices, n_pages), ref["kv_indices"])
+    assert np.array_equal(workspace_ints(d, p_last, W.bs), ref["kv_last_page_len"])
+    assert np.array_equal(workspace_ints(d, p_qo, W.bs + 1), ref["qo_indptr"])
+
+
 @pytest.mark.parametrize("name", ["llama3_8b_decode", "long_fp8_decode"])
-def test_full_size_decode_sampled(name):
-    sampled_check(preset(name))
+def test_full_size_decode_every_row(name):
+    full_check(preset(name))
 
 
-def test_full_size_verify_decode_path_sampled():
-    sampled_check(preset("spec_verify"), spec_mode=B.PKV_SPEC_DECODE)
+def test_full_size_verify_decode_path_every_row():
+    full_check(preset("spec_verify"), spec_mode=B.PKV_SPEC_DECODE)
 
 
 # ------------------------------------------------------------------ device-side data errors
@@ -260,6 +275,31 @@ def test_bad_page_id_recorded_without_fault():
     d.forward()
     assert d.device_error() == B.PKV_DEV_BAD_PAGE
     assert d.device_error() == 0  # reading clears the word
+
+
+def test_page_table_row_shorter_than_a_request_recorded():
+    """A request with more pages than one page-table row holds is recorded as
+    a bad length and treated as empty, and its gather never runs past its row.
+    Two spare rows follow the batch's rows, so a gather that ignored the
+    stride would still read inside this allocation (pages that hold other
+    requests' keys, or the NaN sentinel page) and show up in the output."""
+    W = preset("tiny_decode")  # 3, 7, 14 and 19 pages
+    stride = 10
+    d = DeviceBatch(W)
+    table = torch.zeros((W.bs + 2, stride), dtype=torch.int32, device=d.page_table.device)
+    table[:W.bs] = d.page_table[:, :stride]
+    table[W.bs:] = d.page_table[:2, :stride]
+    d.page_table = table[:W.bs]
+    d.step()
+    torch.cuda.synchronize()
+    assert d.device_error() == B.PKV_DEV_BAD_LENGTH
+    out = d.out.double().cpu().numpy()
+    lse = d.lse.double().cpu().numpy()
+    assert np.all(out[2:] == 0) and np.all(np.isneginf(lse[2:]))
+    W.seq_lens = np.array([W.seq_lens[0], W.seq_lens[1], 0, 0], dtype=W.seq_lens.dtype)
+    ref_o, ref_lse = oracle_reference(W)
+    check_close(out, ref_o, "o")
+    check_close(lse, ref_lse, "lse")
 
 
 def test_capacity_overflow_recorded():
@@ -434,12 +474,16 @@ def test_extend_fp8_pool(case):
     full_check(W, spec_mode=spec)
 
 
-def test_full_size_extend_sampled():
-    sampled_check(preset("prefix_extend"), n_rows=48)
+@pytest.mark.parametrize("name", ["prefix_extend", "prefix_extend_fp8"])
+def test_full_size_extend_every_row(name):
+    """The prefix-cached extend case at full size (about 296k rows), bf16 and
+    E4M3 pools (the new tokens quantised by set_kv_buffer), every row against
+    the oracle."""
+    full_check(preset(name))
 
 
-def test_full_size_verify_prefill_path_sampled():
-    sampled_check(preset("spec_verify"), spec_mode=B.PKV_SPEC_PREFILL)
+def test_full_size_verify_prefill_path_every_row():
+    full_check(preset("spec_verify"), spec_mode=B.PKV_SPEC_PREFILL)
 
 
 def test_extend_graph_replay():
