@@ -46,9 +46,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 NCU_TRAFFIC = {
     ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1386555136},
     ("decode_splitkv", "long_fp8_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1504556032},
-    ("decode_splitkv", "spec_verify"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 601473024},
     ("extend_tc", "prefix_extend"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 967569664},
-    ("extend_tc", "spec_verify"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 599880704},
+    ("extend_tc", "spec_verify/prefill_path"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 599880704},
 }
 
 
@@ -286,10 +285,14 @@ def roofline_of(W, work, fwd_s, spec, B):
         achieved = work["bytes"] / fwd_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} HBM copy"}
-    key = "extend_tc" if on_extend else "decode_splitkv"
-    tr = NCU_TRAFFIC.get((key, W.name))
+    # the verify shapes run on the tcgen05 tile kernel on both paths (over the
+    # decode plan on the decode path)
+    on_tc = on_extend or W.mode == "verify"
+    key = "extend_tc" if on_tc else "decode_splitkv"
+    name = W.name if W.mode != "verify" else f"{W.name}/{'prefill' if on_extend else 'decode'}_path"
+    tr = NCU_TRAFFIC.get((key, name))
     roof["traffic"] = None
-    if tr and tr["src_sha"] == src_sha("extend.cu" if on_extend else "decode.cu"):
+    if tr and tr["src_sha"] == src_sha("extend.cu" if on_tc else "decode.cu"):
         roof["traffic"] = tr["bytes_per_launch"]
     roof["kernel"] = key
     roof["timed"] = ("forward call (attention kernel plus the split merge kernel), CUDA events on the "
@@ -362,7 +365,8 @@ def secondary(name, spec_name, local, steps, world, cpu_budget):
     out = {"metric_value": value * world, "unit": unit, "us_per_call": fwd_s * 1e6, "step_us": step_s * 1e6,
            "graph_step_us": graph_step_us(d, step, steps, torch.cuda.current_stream()),
            "roofline_frac": roof["frac"], "achieved": roof["achieved"], "achieved_unit": roof["unit"],
-           "kernel": roof["kernel"], "path": "decode" if roof["kernel"] == "decode_splitkv" else "extend",
+           "kernel": roof["kernel"], "path": spec_name if W.mode == "verify" else
+           ("decode" if W.mode == "decode" else "extend"),
            "steps": steps, "cpu_baseline": None}
     del d
     torch.cuda.empty_cache()

@@ -20,8 +20,12 @@
 //     S^T = K Q^T with 16 keys along the MMA's M and the rows along N in one or
 //     two 8-row tiles, then O^T += V^T P^T, P^T reaching the B operand through
 //     an in-register 8x8 transpose (movmatrix). Four key warps split each
-//     stage's keys and combine through shared memory. The verify shapes (up to
-//     128 rows) use query-major 16-row tiles, one per row warp.
+//     stage's keys and combine through shared memory.
+//   * Verify shapes (target verify on the decode path: more than 16 and up to
+//     128 query rows per KV head) are a dense contraction of a full 128-row
+//     tile against every key, so they run on the 5th-generation tensor cores:
+//     the tcgen05 tile kernel of extend.cu walks this path's plan (the same
+//     split items, the same merge below).
 //   * Each unit ends with its normalised output and LSE. A request with one split
 //     writes the final bf16 output directly; otherwise the unit writes a bf16
 //     partial row and an fp32 LSE, and the merge kernel (one warp per
@@ -45,21 +49,20 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D_, bool FP8_, int WR_, int WK_, int KPW_, int STAGES_, int RT_ = 0>
+template <int D_, bool FP8_, int WK_, int KPW_, int STAGES_, int RT_>
 struct DecodeCfg {
   static constexpr int D = D_;
   static constexpr bool FP8 = FP8_;
-  // RT > 0: key-major tile (keys along the MMA's M, RT tiles of 8 query rows
-  // along N), one row warp; RT == 0: query-major tile, WR row warps
+  // key-major tile: keys along the MMA's M, RT tiles of 8 query rows along N
   static constexpr int RT = RT_;
-  static constexpr int WR = WR_;  // row warps (16 rows each)
+  static constexpr int WR = 1;    // one row position (the rows are the MMA's N)
   static constexpr int WK = WK_;  // key warps (split each stage's keys)
   static constexpr int KPW = KPW_;  // keys per key-warp per stage (multiple of 16)
   static constexpr int STAGES = STAGES_;
   static constexpr int kConsumerWarps = WR * WK;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
   static constexpr int kMinBlocks = kThreads <= 160 ? 2 : 1;  // two CTAs per SM hide latency for the decode shapes
-  static constexpr int kRows = RT > 0 ? 8 * RT : 16 * WR;
+  static constexpr int kRows = 8 * RT;
   static constexpr int kStageKeys = WK * KPW;
   static constexpr int kStagePages = kStageKeys / kPageSize;
   static constexpr int kElem = FP8 ? 1 : 2;
@@ -67,7 +70,6 @@ struct DecodeCfg {
   static constexpr int kColBlocks = kRowBytes / 128;
   static constexpr int kTileBytes = kStageKeys * kRowBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kNT = D / 8;  // n-tiles of the output
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kMlOffset = kBarOffset + 2 * STAGES * 8;
   static constexpr int kAbortOffset = kMlOffset + WK * 16 * 2 * 4;
@@ -76,8 +78,7 @@ struct DecodeCfg {
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
   static_assert(KPW % 16 == 0 && kStageKeys % kPageSize == 0, "stage must hold whole pages");
   static_assert(!(WK > 1) || (WK * 16 * D * 4 <= kStageBytes), "merge scratch must fit in one stage");
-  static_assert(RT == 0 || (WR == 1 && WK > 1 && RT <= 2), "key-major tiles: one row warp, key warps combined");
-  static_assert(RT > 0 || WK == 1, "query-major tiles: each warp holds all keys of a stage");
+  static_assert(WK > 1 && RT >= 1 && RT <= 2, "key-major tiles: one or two 8-row tiles, key warps combined");
 };
 
 struct DecodeArgs {
@@ -99,16 +100,6 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// Output column of accumulator element e (0/1) of n-tile nt for quad lane q.
-template <bool FP8>
-__device__ __forceinline__ int ocol(int nt, int q, int e) {
-  if constexpr (FP8) {
-    return (nt >> 1) * 16 + 4 * q + 2 * e + (nt & 1);
-  } else {
-    return nt * 8 + 2 * q + e;
-  }
-}
 
 // Combine the nsplit partial rows of one (token, query head) row:
 //   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s.
@@ -312,9 +303,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
 
   // -------------------------------------------------------------- consumers
   const int cw = warp;  // consumer warp
-  const int wr = cw / C::WK, wk = cw % C::WK;
-  const int qd = lane & 3;   // quad lane
-  const int rq = lane >> 2;  // row within the 8-row half
+  const int wk = cw % C::WK;  // key warp
   const int G = a.group;
   int slot = 0;
   uint32_t phase = 0;
@@ -343,13 +332,13 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
     const int np_req = a.m.kv_indptr[b + 1] - a.m.kv_indptr[b];
     const int rows_valid = qo * G;
     const bool skip = rows_valid > C::kRows;  // tile too small: recorded, pipeline still drained
-    if (skip && lane == 0 && wr == 0 && wk == 0) record_error(plan, PKV_DEV_QO_TOO_LONG, b);
+    if (skip && lane == 0 && wk == 0) record_error(plan, PKV_DEV_QO_TOO_LONG, b);
     const int key_begin = it.p0 * kPageSize;
     const int key_end = min(it.p1 * kPageSize, L);
     const int npages = it.p1 - it.p0;
     const int nst = (npages + C::kStagePages - 1) / C::kStagePages;
 
-    if constexpr (C::RT > 0) {
+    {
       // ---------------------------------------------- key-major tile (decode)
       // S^T = K Q^T with the stage's keys along the MMA's M (16 per block) and
       // the unit's query rows along N (RT tiles of 8), then O^T += V^T P^T with
@@ -712,289 +701,6 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           phase ^= 1;
         }
       }
-    } else {
-      // rows of this thread: ra = wr*16 + rq, rb = ra + 8 -> (token i, head-in-group)
-      const int ra = wr * 16 + rq, rb = ra + 8;
-      const bool va = ra < rows_valid, vb = rb < rows_valid;
-      const int prefix = L - qo;
-      const int lim_a = prefix + min(ra / G, qo - 1);
-      const int lim_b = prefix + min(rb / G, qo - 1);
-      const long long qrow_a = ((long long)(q0 + ra / G) * a.num_q_heads + g * G + ra % G) * D;
-      const long long qrow_b = ((long long)(q0 + rb / G) * a.num_q_heads + g * G + rb % G) * D;
-      // draft trees: each row's mask word clears the drafts outside its tree;
-      // the words are read only in the blocks that reach the drafts
-      const bool tree = tree_words != nullptr;
-      if (tree && qo > 64 && lane == 0 && cw == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
-
-      // Q fragments (A operand), D/16 k-steps x 4 registers
-      uint32_t qf[D / 16][4];
-      if constexpr (!C::FP8) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int c0 = kk * 16 + 2 * qd;
-          qf[kk][0] = va ? *reinterpret_cast<const uint32_t*>(a.q + qrow_a + c0) : 0u;
-          qf[kk][1] = vb ? *reinterpret_cast<const uint32_t*>(a.q + qrow_b + c0) : 0u;
-          qf[kk][2] = va ? *reinterpret_cast<const uint32_t*>(a.q + qrow_a + c0 + 8) : 0u;
-          qf[kk][3] = vb ? *reinterpret_cast<const uint32_t*>(a.q + qrow_b + c0 + 8) : 0u;
-        }
-      } else {
-        // permuted contraction order matching the 8-byte K loads below:
-        // k-step 2p  : logical k {2q,2q+1} <- D 32p+8q+{0,1}, {2q+8,2q+9} <- D 32p+8q+{2,3}
-        // k-step 2p+1: logical k {2q,2q+1} <- D 32p+8q+{4,5}, {2q+8,2q+9} <- D 32p+8q+{6,7}
-#pragma unroll
-        for (int p = 0; p < D / 32; ++p) {
-          const int c0 = p * 32 + 8 * qd;
-          uint4 xa = va ? *reinterpret_cast<const uint4*>(a.q + qrow_a + c0) : make_uint4(0, 0, 0, 0);
-          uint4 xb = vb ? *reinterpret_cast<const uint4*>(a.q + qrow_b + c0) : make_uint4(0, 0, 0, 0);
-          qf[2 * p][0] = pack_f16(bf16lo(xa.x), bf16hi(xa.x));
-          qf[2 * p][1] = pack_f16(bf16lo(xb.x), bf16hi(xb.x));
-          qf[2 * p][2] = pack_f16(bf16lo(xa.y), bf16hi(xa.y));
-          qf[2 * p][3] = pack_f16(bf16lo(xb.y), bf16hi(xb.y));
-          qf[2 * p + 1][0] = pack_f16(bf16lo(xa.z), bf16hi(xa.z));
-          qf[2 * p + 1][1] = pack_f16(bf16lo(xb.z), bf16hi(xb.z));
-          qf[2 * p + 1][2] = pack_f16(bf16lo(xa.w), bf16hi(xa.w));
-          qf[2 * p + 1][3] = pack_f16(bf16lo(xb.w), bf16hi(xb.w));
-        }
-      }
-
-      float o[C::kNT][4];
-#pragma unroll
-      for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-      float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-      for (int st = 0; st < nst; ++st) {
-        // a failed wait keeps this warp on the common control flow (so every
-        // named barrier still sees all consumer warps); the loop-top vote ends it
-        if (!aborted && !mbar_wait_ab(&full[slot], phase, plan, s_abort)) {
-          *s_abort = 1;
-          aborted = true;
-        }
-        const uint32_t kbase = smem_u32(smem + slot * C::kStageBytes);
-        const uint32_t vbase = kbase + C::kTileBytes;
-        const int stage_key0 = key_begin + st * C::kStageKeys;
-        // last page of the request with a partial fill: zero the V rows past L
-        const bool tail = (it.p1 == np_req) && (st == nst - 1) && (L % kPageSize) != 0;
-        if (tail) {
-          const int r0 = L - stage_key0;
-          const int r1 = min(C::kStagePages, npages - st * C::kStagePages) * kPageSize;
-          uint8_t* vb8 = smem + slot * C::kStageBytes + C::kTileBytes;
-          const int n16 = (r1 - r0) * C::kColBlocks * 8;
-          for (int i = cw * 32 + lane; i < n16; i += C::kConsumerWarps * 32) {
-            const int row = r0 + i / (C::kColBlocks * 8);
-            const int rest = i % (C::kColBlocks * 8);
-            const int cb = rest / 8, ch = rest % 8;
-            *reinterpret_cast<uint4*>(vb8 + cb * C::kStageKeys * 128 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(1, C::kConsumerWarps * 32);
-        }
-
-        // a row-warp whose 16 rows are all padding (fewer drafts than the tile
-        // holds) still takes part in the stage protocol but computes nothing
-        if (!skip && (C::WR == 1 || wr * 16 < rows_valid)) {
-#pragma unroll
-          for (int kb = 0; kb < C::KPW / 16; ++kb) {
-            const int kr0 = wk * C::KPW + kb * 16;  // first stage row of this 16-key block
-            const int abs0 = stage_key0 + kr0;
-            if (abs0 >= key_end) break;
-            // ---- S = Q K^T for 16 keys (two n-tiles of 8) ----
-            float s[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-            if constexpr (!C::FP8) {
-              const int key = kr0 + (lane & 7) + ((lane >> 4) << 3);
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const int chunk = 2 * kk + ((lane >> 3) & 1);
-                const uint32_t addr = kbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
-                uint32_t b00, b01, b10, b11;
-                ldsm_x4(addr, b00, b01, b10, b11);
-                mma_bf16(s[0], qf[kk], b00, b01);
-                mma_bf16(s[1], qf[kk], b10, b11);
-              }
-            } else {
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) {
-                const int key = kr0 + nt * 8 + rq;
-#pragma unroll
-                for (int p = 0; p < D / 32; ++p) {
-                  const int byte = p * 32 + 8 * qd;
-                  const uint32_t addr = kbase + swz(key, byte >> 4) + (byte & 15);
-                  uint32_t x0, x1;
-                  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x0), "=r"(x1) : "r"(addr));
-                  mma_f16(s[nt], qf[2 * p], e4m3x2_to_f16x2((uint16_t)(x0 & 0xffff)),
-                          e4m3x2_to_f16x2((uint16_t)(x0 >> 16)));
-                  mma_f16(s[nt], qf[2 * p + 1], e4m3x2_to_f16x2((uint16_t)(x1 & 0xffff)),
-                          e4m3x2_to_f16x2((uint16_t)(x1 >> 16)));
-                }
-              }
-            }
-            // ---- mask, online softmax (log2 domain) ----
-            if (tree && abs0 + 15 >= prefix) {
-              // the block reaches the drafts: raw scores of drafts outside a
-              // row's tree to -inf (the scale below is positive)
-              const uint64_t tw_a = va ? tree_words[q0 + ra / G] : ~0ull;
-              const uint64_t tw_b = vb ? tree_words[q0 + rb / G] : ~0ull;
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const int dj = abs0 + nt * 8 + 2 * qd + e - prefix;
-                  if (dj >= 0 && !(dj < 64 && ((tw_a >> dj) & 1ull))) s[nt][e] = -INFINITY;
-                  if (dj >= 0 && !(dj < 64 && ((tw_b >> dj) & 1ull))) s[nt][2 + e] = -INFINITY;
-                }
-            }
-            float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int kp = abs0 + nt * 8 + 2 * qd + e;
-                const bool ok = kp < key_end;
-                s[nt][e] = (ok && kp <= lim_a) ? s[nt][e] * a.scale_log2 : -INFINITY;
-                s[nt][2 + e] = (ok && kp <= lim_b) ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
-                mx_a = fmaxf(mx_a, s[nt][e]);
-                mx_b = fmaxf(mx_b, s[nt][2 + e]);
-              }
-            }
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-            const float ref_a = mn_a == -INFINITY ? 0.f : mn_a;
-            const float ref_b = mn_b == -INFINITY ? 0.f : mn_b;
-            const float al_a = fast_exp2(m_a - ref_a), al_b = fast_exp2(m_b - ref_b);
-            m_a = mn_a;
-            m_b = mn_b;
-            float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                s[nt][e] = fast_exp2(s[nt][e] - ref_a);
-                s[nt][2 + e] = fast_exp2(s[nt][2 + e] - ref_b);
-                ps_a += s[nt][e];
-                ps_b += s[nt][2 + e];
-              }
-            }
-            l_a = l_a * al_a + ps_a;
-            l_b = l_b * al_b + ps_b;
-            if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {
-#pragma unroll
-              for (int nt = 0; nt < C::kNT; ++nt) {
-                o[nt][0] *= al_a;
-                o[nt][1] *= al_a;
-                o[nt][2] *= al_b;
-                o[nt][3] *= al_b;
-              }
-            }
-            // ---- O += P V ----
-            uint32_t pf[4];
-            if constexpr (!C::FP8) {
-              pf[0] = pack_bf16(s[0][0], s[0][1]);
-              pf[1] = pack_bf16(s[0][2], s[0][3]);
-              pf[2] = pack_bf16(s[1][0], s[1][1]);
-              pf[3] = pack_bf16(s[1][2], s[1][3]);
-              const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-              for (int jj = 0; jj < D / 16; ++jj) {
-                const int chunk = 2 * jj + (lane >> 4);
-                const uint32_t addr = vbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
-                uint32_t b0e, b1e, b0o, b1o;
-                ldsm_x4_t(addr, b0e, b1e, b0o, b1o);
-                mma_bf16(o[2 * jj], pf, b0e, b1e);
-                mma_bf16(o[2 * jj + 1], pf, b0o, b1o);
-              }
-            } else {
-              pf[0] = pack_f16(s[0][0], s[0][1]);
-              pf[1] = pack_f16(s[0][2], s[0][3]);
-              pf[2] = pack_f16(s[1][0], s[1][1]);
-              pf[3] = pack_f16(s[1][2], s[1][3]);
-              const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-              for (int jp = 0; jp < D / 32; ++jp) {
-                // 16-byte chunks 2jp (D 32jp..+15) and 2jp+1 (D 32jp+16..+31)
-                const int chunk = 2 * jp + (lane >> 4);
-                const uint32_t addr = vbase + swz(key, chunk);
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4_t(addr, r0, r1, r2, r3);
-                // r0: keys 0-7 / chunk 2jp, r1: keys 8-15 / chunk 2jp, r2, r3: chunk 2jp+1.
-                // bytes of r: V[2q][2c], V[2q][2c+1], V[2q+1][2c], V[2q+1][2c+1]
-                const uint32_t e0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0020));
-                const uint32_t o0 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r0, 0, 0x0031));
-                const uint32_t e1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0020));
-                const uint32_t o1 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r1, 0, 0x0031));
-                const uint32_t e2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0020));
-                const uint32_t o2 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r2, 0, 0x0031));
-                const uint32_t e3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0020));
-                const uint32_t o3 = e4m3x2_to_f16x2((uint16_t)__byte_perm(r3, 0, 0x0031));
-                mma_f16(o[4 * jp + 0], pf, e0, e1);
-                mma_f16(o[4 * jp + 1], pf, o0, o1);
-                mma_f16(o[4 * jp + 2], pf, e2, e3);
-                mma_f16(o[4 * jp + 3], pf, o2, o3);
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (++slot == C::STAGES) {
-          slot = 0;
-          phase ^= 1;
-        }
-      }
-      // ---------------------------------------------------------- epilogue
-      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-
-      const bool direct = nsplit == 1;
-      const int split = it.split;
-      // destination row of row r: the output, or (split units) a bf16 partial
-      // row of the same layout plus its LSE
-      auto out_row = [&](int r, uint16_t*& orow, float*& lrow) {
-        const int i = r / G, h = g * G + r % G;
-        const long long t = q0 + i;
-        if (direct) {
-          orow = a.out + (t * a.num_q_heads + h) * D;
-          lrow = a.lse ? a.lse + t * a.num_q_heads + h : nullptr;
-        } else {
-          const long long pr = (long long)a.m.partial_indptr[b] + (long long)split * qo + i;
-          orow = a.m.partial_o + (pr * a.num_q_heads + h) * D;
-          lrow = a.m.partial_lse + pr * a.num_q_heads + h;
-        }
-      };
-
-      if (!skip) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int r = half ? rb : ra;
-          const bool v = half ? vb : va;
-          const float m = half ? m_b : m_a, l = half ? l_b : l_a;
-          if (!v) continue;
-          uint16_t* orow;
-          float* lrow;
-          out_row(r, orow, lrow);
-          float inv = l > 0.f ? a.v_scale / l : 0.f;
-          float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
-          if (direct && sinks) inv *= sink_factor(lse, sinks[g * G + r % G]);
-#pragma unroll
-          for (int nt = 0; nt < C::kNT; ++nt) {
-            const float x0 = o[nt][2 * half] * inv, x1 = o[nt][2 * half + 1] * inv;
-            const int c0 = ocol<C::FP8>(nt, qd, 0), c1 = ocol<C::FP8>(nt, qd, 1);
-            if constexpr (!C::FP8) {
-              *reinterpret_cast<uint32_t*>(orow + c0) = pack_bf16(x0, x1);
-            } else {
-              uint32_t pk = pack_bf16(x0, x1);
-              orow[c0] = (uint16_t)(pk & 0xffff);
-              orow[c1] = (uint16_t)(pk >> 16);
-            }
-          }
-          if (qd == 0 && lrow) *lrow = lse;
-        }
-      }
     }
 
   }
@@ -1067,24 +773,14 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   return launch_split_merge(c, out, lse, c.cfg.max_qo_len * a.group, false, st);
 }
 
-// Tile shapes: decode packs one 16-row tile per unit and splits each stage's
-// keys over four warps; the verify shape gives each of up to eight warps its
-// own 16 rows and all keys of a stage.
-using DecBf16D128_1 = DecodeCfg<128, false, 1, 4, 16, 3, 1>;
-using DecBf16D128_2 = DecodeCfg<128, false, 1, 4, 16, 3, 2>;
-using DecBf16D64_1 = DecodeCfg<64, false, 1, 4, 16, 4, 1>;
-using DecBf16D64_2 = DecodeCfg<64, false, 1, 4, 16, 4, 2>;
-using DecFp8D128_1 = DecodeCfg<128, true, 1, 4, 32, 3, 1>;
-using DecFp8D128_2 = DecodeCfg<128, true, 1, 4, 32, 3, 2>;
-using VerBf16D128_2 = DecodeCfg<128, false, 2, 1, 64, 3>;
-using VerBf16D128_4 = DecodeCfg<128, false, 4, 1, 64, 3>;
-using VerBf16D128_8 = DecodeCfg<128, false, 8, 1, 64, 3>;
-using VerBf16D64_2 = DecodeCfg<64, false, 2, 1, 64, 4>;
-using VerBf16D64_4 = DecodeCfg<64, false, 4, 1, 64, 4>;
-using VerBf16D64_8 = DecodeCfg<64, false, 8, 1, 64, 4>;
-using VerFp8D128_2 = DecodeCfg<128, true, 2, 1, 128, 3>;
-using VerFp8D128_4 = DecodeCfg<128, true, 4, 1, 128, 3>;
-using VerFp8D128_8 = DecodeCfg<128, true, 8, 1, 128, 3>;
+// Tile shapes: one or two 8-row key-major tiles per unit; four key warps
+// split each stage's keys.
+using DecBf16D128_1 = DecodeCfg<128, false, 4, 16, 3, 1>;
+using DecBf16D128_2 = DecodeCfg<128, false, 4, 16, 3, 2>;
+using DecBf16D64_1 = DecodeCfg<64, false, 4, 16, 4, 1>;
+using DecBf16D64_2 = DecodeCfg<64, false, 4, 16, 4, 2>;
+using DecFp8D128_1 = DecodeCfg<128, true, 4, 32, 3, 1>;
+using DecFp8D128_2 = DecodeCfg<128, true, 4, 32, 3, 2>;
 
 }  // namespace
 
@@ -1098,7 +794,12 @@ int decode_row_warps(const pkv_config& cfg) {
   return 0;
 }
 
+// Pages per pipeline stage of the decode kernel; the metadata rounds the
+// decode plan's chunks to whole stages. The verify shapes run on the tcgen05
+// tile kernel, whose KV tiles are 128 keys (8 pages): their chunks are whole
+// tiles.
 int decode_stage_pages(const pkv_config& cfg) {
+  if (decode_row_warps(cfg) > 1) return kExtendKeys / kPageSize;
   return cfg.kv_dtype == PKV_KV_FP8_E4M3 ? 8 : 4;
 }
 
@@ -1106,34 +807,22 @@ int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool,
                   float v_scale, void* out, float* lse, cudaStream_t st) {
   const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
   const int D = c.cfg.head_dim;
-  const int wr = decode_row_warps(c.cfg);
+  // verify shapes (more than 16 rows per KV head): the tcgen05 tile kernel
+  // over this path's plan
+  if (decode_row_warps(c.cfg) > 1)
+    return launch_decode_tc(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st);
   // decode shapes (at most 16 rows): key-major tiles of one or two 8-row tiles
   const bool rt1 = c.cfg.max_qo_len * (c.cfg.num_q_heads / c.cfg.num_kv_heads) <= 8;
 #define PKV_RUN(CFG) return run_decode<CFG>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st)
   if (!fp8 && D == 128) {
-    if (wr == 1) {
-      if (rt1) PKV_RUN(DecBf16D128_1);
-      PKV_RUN(DecBf16D128_2);
-    }
-    if (wr == 2) PKV_RUN(VerBf16D128_2);
-    if (wr == 4) PKV_RUN(VerBf16D128_4);
-    if (wr == 8) PKV_RUN(VerBf16D128_8);
+    if (rt1) PKV_RUN(DecBf16D128_1);
+    PKV_RUN(DecBf16D128_2);
   } else if (!fp8 && D == 64) {
-    if (wr == 1) {
-      if (rt1) PKV_RUN(DecBf16D64_1);
-      PKV_RUN(DecBf16D64_2);
-    }
-    if (wr == 2) PKV_RUN(VerBf16D64_2);
-    if (wr == 4) PKV_RUN(VerBf16D64_4);
-    if (wr == 8) PKV_RUN(VerBf16D64_8);
+    if (rt1) PKV_RUN(DecBf16D64_1);
+    PKV_RUN(DecBf16D64_2);
   } else if (fp8 && D == 128) {
-    if (wr == 1) {
-      if (rt1) PKV_RUN(DecFp8D128_1);
-      PKV_RUN(DecFp8D128_2);
-    }
-    if (wr == 2) PKV_RUN(VerFp8D128_2);
-    if (wr == 4) PKV_RUN(VerFp8D128_4);
-    if (wr == 8) PKV_RUN(VerFp8D128_8);
+    if (rt1) PKV_RUN(DecFp8D128_1);
+    PKV_RUN(DecFp8D128_2);
   }
 #undef PKV_RUN
   return PKV_ERR_UNSUPPORTED;

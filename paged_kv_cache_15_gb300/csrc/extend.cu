@@ -215,7 +215,33 @@ struct ExtendArgs {
   int out_32B;       // out is 32-byte aligned: output rows are written with 32-byte stores
   const uint64_t* tree;  // draft-tree mask word per query token, or null (chain drafts)
   const float* sinks;    // sink logit per query head, or null
+  // 1: the units are the decode plan's (request, split) items, the decode
+  // path's verify shapes (at most 128 rows per KV head); 0: the extend plan
+  int dplan;
 };
+
+// Work unit idx of the plan the kernel runs. A decode-plan item (request b,
+// split s, pages [p0, p1)) becomes a dual unit: its rows (every query token
+// of the request times the group's heads) fit one 128-row tile, both tiles
+// hold them and take half of the item's KV tiles each. The decode plan's
+// chunks are whole 128-key tiles on these shapes, so [p0, p1) maps onto KV
+// tiles exactly; a request cut into several items writes partial rows that
+// the decode path's merge combines.
+__device__ __forceinline__ ExtendTile load_unit(const ExtendArgs& a, int idx) {
+  if (!a.dplan) return a.m.extend_tiles[idx];
+  constexpr int kPagesPerTile = kExtendKeys / kPageSize;
+  const DecodeItem it = a.m.decode_items[idx];
+  ExtendTile u;
+  u.b = it.b;
+  u.row0 = 0;
+  u.kv_a = (a.m.kv_len[it.b] + kExtendKeys - 1) / kExtendKeys;  // the last row sees every key
+  u.kv_b = 0;
+  u.split = a.m.n_splits[it.b] > 1 ? it.split : -1;
+  u.kv0 = it.p0 / kPagesPerTile;
+  u.kv1 = (it.p1 + kPagesPerTile - 1) / kPagesPerTile;
+  u.dual = 1;
+  return u;
+}
 
 // EXTRAS: draft-tree mask words or attention sinks are in use (a separate
 // instantiation, so plain batches run the causal kernel without that code).
@@ -288,7 +314,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   // step stored are only read after the preceding grid has finished
   pdl_wait();
 
-  const int n_units = plan[kExtendTiles] * a.num_kv_heads;
+  const int n_units = plan[a.dplan ? kDecodeItems : kExtendTiles] * a.num_kv_heads;
   const int G = a.group;
   const uint32_t smem_base = smem_u32(smem);
   const int total_q = plan[kTotalQ];
@@ -322,7 +348,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     uint32_t qtcount[2] = {0, 0};  // of those, written by the softmax warps (phase of q_written)
     bool stop = false;
     for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
-      const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
+      const ExtendTile u = load_unit(a, w / a.num_kv_heads);
       const int g = w % a.num_kv_heads;
       const UnitKV ukv = unit_kv(u);
       const int np = a.m.kv_indptr[u.b + 1] - a.m.kv_indptr[u.b];
@@ -458,7 +484,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       if (last) umma_commit_warp(&pv_done[x]);
     };
     for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
-      const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
+      const ExtendTile u = load_unit(a, w / a.num_kv_heads);
       const UnitKV ukv = unit_kv(u);
       const int n[2] = {ukv.n0, ukv.n1};
       const int nT = ukv.steps();
@@ -559,7 +585,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     uint32_t ucount = 0;  // units with work for this tile (phase of pv_done)
     uint32_t du = 0;      // dual units with work (phase of b_done / a_read)
     for (int w = blockIdx.x; w < n_units && !*s_abort; w += gridDim.x) {
-      const ExtendTile u = a.m.extend_tiles[w / a.num_kv_heads];
+      const ExtendTile u = load_unit(a, w / a.num_kv_heads);
       const int g = w % a.num_kv_heads;
       const UnitKV ukv = unit_kv(u);
       const int kb = ukv.start(x);  // this tile's KV tiles: [kb, kb + nX)
@@ -573,6 +599,10 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       const int np = a.m.kv_indptr[b + 1] - a.m.kv_indptr[b];
       const int R = u.row0 + (ukv.dual ? 0 : x * kExtendRows) + r;  // a dual unit's tiles hold the same rows
       const bool valid = R < qo * G;
+      // a decode-plan unit holds one 128-row tile of rows (the configuration
+      // bounds max_qo_len * group); the rows of a longer request past the
+      // tile are recorded and left unwritten
+      if (a.dplan && qo * G > kExtendRows && r == 0 && x == 0) record_error(plan, PKV_DEV_QO_TOO_LONG, b);
       const int tok = min(R / G, qo - 1);
       const int limit = L - qo + tok;
       // draft trees: the row's mask word clears the drafts outside its tree
@@ -932,7 +962,7 @@ __global__ void __launch_bounds__(256) fp8_stage_kernel(const uint8_t* __restric
 
 template <class C>
 int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
-               float v_scale, void* out, float* lse, cudaStream_t st) {
+               float v_scale, void* out, float* lse, cudaStream_t st, bool dplan) {
   CUtensorMap tk, tv;
   const uint64_t inner = (uint64_t)c.cfg.num_kv_heads * C::D;
   uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
@@ -973,6 +1003,7 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.out_32B = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
   a.tree = active_tree(c);
   a.sinks = c.sinks;
+  a.dplan = dplan ? 1 : 0;
   // Q as [tokens][heads][head_dim]: a box of 64 elements x G heads x 128/G
   // tokens is one 128-row tile column block, rows ordered (token, head) like
   // the tile's rows. The token extent only bounds the map; the kernel loads a
@@ -997,19 +1028,32 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
     return PKV_ERR_CUDA;
   if (launch_pdl(kernel, dim3(c.extend_ctas), dim3(C::kThreads), C::kSmemBytes, st, tk, tv, tq, a) != cudaSuccess)
     return PKV_ERR_CUDA;
-  // requests whose rows fit one unit were split along their KV range
+  // the decode plan's split requests are merged by the decode path's merge
+  // (its split counts); on the extend path, the requests whose rows fit one
+  // unit were split along their KV range
+  if (dplan) return launch_split_merge(c, out, lse, c.cfg.max_qo_len * a.group, false, st);
   return launch_split_merge(c, out, lse, kExtendUnitRows, true, st);
+}
+
+int run_tc(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+           float v_scale, void* out, float* lse, cudaStream_t st, bool dplan) {
+  if (c.cfg.head_dim == 128)
+    return run_extend<ExtCfg<128, 3, 2>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
+  if (c.cfg.head_dim == 64)
+    return run_extend<ExtCfg<64, 4, 4>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
+  return PKV_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
 int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
                   float v_scale, void* out, float* lse, cudaStream_t st) {
-  if (c.cfg.head_dim == 128)
-    return run_extend<ExtCfg<128, 3, 2>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st);
-  if (c.cfg.head_dim == 64)
-    return run_extend<ExtCfg<64, 4, 4>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st);
-  return PKV_ERR_UNSUPPORTED;
+  return run_tc(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, false);
+}
+
+int launch_decode_tc(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+                     float v_scale, void* out, float* lse, cudaStream_t st) {
+  return run_tc(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, true);
 }
 
 }  // namespace pkv

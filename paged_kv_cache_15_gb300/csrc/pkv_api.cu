@@ -417,12 +417,20 @@ int pkv_describe(pkv_ctx* ctx, char* buf, size_t n) {
   if (!ctx || !buf || n == 0) return PKV_ERR_INVALID_ARG;
   const pkv_config& c = ctx->cfg;
   const int group = c.num_q_heads / c.num_kv_heads;
+  const int rows = c.max_qo_len * group;
+  char dec[160];
+  if (decode_row_warps(c) > 1)
+    snprintf(dec, sizeof dec, "split-KV on tcgen05 %dx%d tiles (verify shapes, up to %d rows/unit), grid %d",
+             kExtendRows, kExtendKeys, rows, ctx->extend_ctas);
+  else
+    snprintf(dec, sizeof dec, "split-KV TMA+mma.sync key-major, up to %d rows/unit, %d pages/stage, grid %d",
+             rows <= 8 ? 8 : 16, decode_stage_pages(c), ctx->decode_ctas);
   snprintf(buf, n,
-           "pkv sm_103a: heads %d/%d (group %d) head_dim %d page_size %d kv %s pool_pages %d | decode: split-KV "
-           "TMA+mma.sync, %d rows/unit, %d pages/stage, grid %d | extend: tcgen05 %dx%d tiles, grid %d | SMs %d",
+           "pkv sm_103a: heads %d/%d (group %d) head_dim %d page_size %d kv %s pool_pages %d | decode: %s | "
+           "extend: tcgen05 %dx%d tiles, grid %d | SMs %d",
            c.num_q_heads, c.num_kv_heads, group, c.head_dim, c.page_size,
-           c.kv_dtype == PKV_KV_FP8_E4M3 ? "fp8_e4m3" : "bf16", c.num_pages, 16 * decode_row_warps(c),
-           decode_stage_pages(c), ctx->decode_ctas, kExtendRows, kExtendKeys, ctx->extend_ctas, ctx->num_sms);
+           c.kv_dtype == PKV_KV_FP8_E4M3 ? "fp8_e4m3" : "bf16", c.num_pages, dec, kExtendRows, kExtendKeys,
+           ctx->extend_ctas, ctx->num_sms);
   return PKV_OK;
 }
 

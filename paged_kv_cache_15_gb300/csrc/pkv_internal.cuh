@@ -132,6 +132,11 @@ int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool,
                   float v_scale, void* out, float* lse, cudaStream_t st);
 int launch_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
                   float v_scale, void* out, float* lse, cudaStream_t st);
+// The decode path's verify shapes (more than 16 query rows per KV head): the
+// tcgen05 tile kernel of the extend path, run over the decode plan's split-KV
+// items and merged by the decode path's merge.
+int launch_decode_tc(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
+                     float v_scale, void* out, float* lse, cudaStream_t st);
 // LSE merge of split partials for requests whose rows per KV head are at most
 // max_rows_per_head (the decode path: its largest tile; the extend path: 256,
 // the requests it split).

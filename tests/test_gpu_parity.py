@@ -222,6 +222,33 @@ def test_verify_decode_path_parity(bs, len_scale):
     full_check(W, spec_mode=B.PKV_SPEC_DECODE)
 
 
+@pytest.mark.parametrize("case", ["rows128_g8", "one_token_rows", "ragged_tiles", "d64_g16"])
+def test_verify_decode_path_tensor_core_tiles(case):
+    """The decode path's verify shapes run on 128-row tcgen05 tiles over the
+    decode plan's split items: a full tile (16 drafts x group 8), one-token
+    requests on a configuration sized for drafts (16 valid rows of 128),
+    lengths that end anywhere inside a 128-key tile and splits of many
+    lengths, and head_dim 64."""
+    cfg = None
+    if case == "rows128_g8":
+        W = make_workload("vt128", "verify", 4, 32, 4, 128, [3000, 17, 900, 6100], [16, 16, 9, 16])
+    elif case == "one_token_rows":
+        W = make_workload("vt1", "verify", 6, 64, 4, 128, [5000, 300, 0, 2047, 129, 12000], np.ones(6))
+        cfg = config_for(W, max_qo_len=8)
+    elif case == "ragged_tiles":
+        W = make_workload("vtr", "verify", 5, 64, 4, 128, [2045, 126, 16380, 3999, 257], [4, 8, 5, 7, 6])
+    else:
+        W = make_workload("vt64", "verify", 4, 32, 2, 64, [700, 4000, 33, 9000], [8, 3, 8, 5])
+    d = DeviceBatch(W, cfg=cfg)
+    d.step(B.PKV_SPEC_DECODE)
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    assert "tcgen05" in B.pkv_describe(d.ctx).split("| decode:")[1].split("|")[0]
+    ref_o, ref_lse = oracle_reference(W)
+    check_close(d.out.double().cpu().numpy(), ref_o, "o")
+    check_close(d.lse.double().cpu().numpy(), ref_lse, "lse")
+
+
 def test_verify_decode_path_fp8():
     W = make_workload("vf8", "verify", 5, 32, 8, 128, [100, 2000, 517, 33, 4096], [4, 8, 5, 7, 6],
                       kv_dtype="fp8_e4m3")
