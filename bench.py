@@ -338,13 +338,13 @@ def timed_steps(d, spec, steps, world):
     return step_s, fwd_s
 
 
-def secondary(name, spec_name, local, steps, world, cpu_budget):
+def secondary(name, spec_name, local, steps, world, cpu_budget, page_size=16):
     """Short measurement of another workload (no e2e), with the oracle timed
     beside it on a bounded sample (rank 0 of a single-GPU run only)."""
     from paged_kv_cache_15_gb300 import binding as B
     from paged_kv_cache_15_gb300.runner import DeviceBatch
     from paged_kv_cache_15_gb300.workloads import preset
-    W = preset(name)
+    W = preset(name, page_size=page_size)
     spec = B.PKV_SPEC_DECODE if spec_name == "decode" else B.PKV_SPEC_PREFILL
     d = DeviceBatch(W, device=f"cuda:{local}")
 
@@ -367,7 +367,7 @@ def secondary(name, spec_name, local, steps, world, cpu_budget):
            "roofline_frac": roof["frac"], "achieved": roof["achieved"], "achieved_unit": roof["unit"],
            "kernel": roof["kernel"], "path": spec_name if W.mode == "verify" else
            ("decode" if W.mode == "decode" else "extend"),
-           "steps": steps, "cpu_baseline": None}
+           "steps": steps, "page_size": W.page_size, "cpu_baseline": None}
     del d
     torch.cuda.empty_cache()
     if world == 1 and cpu_budget > 0:
@@ -449,13 +449,17 @@ def run_ours(args, W, rank, world, local):
     # --- the other named workloads of the metric, short runs
     others = {}
     if not args.no_secondary:
-        for name, sp in (("tiny_decode", "prefill"), ("prefix_extend", "prefill"), ("prefix_extend_fp8", "prefill"),
-                         ("spec_verify", "decode"), ("spec_verify", "prefill"), ("long_fp8_decode", "prefill")):
-            if name == W.name and sp == args.spec_mode:
+        for name, sp, ps in (("tiny_decode", "prefill", 16), ("prefix_extend", "prefill", 16),
+                             ("prefix_extend_fp8", "prefill", 16), ("spec_verify", "decode", 16),
+                             ("spec_verify", "prefill", 16), ("long_fp8_decode", "prefill", 16),
+                             ("llama3_8b_decode", "prefill", 128)):
+            if name == W.name and sp == args.spec_mode and ps == W.page_size:
                 continue
             key = name if name != "spec_verify" else f"spec_verify/{sp}_path"
+            if ps != 16:
+                key += f"/page_size_{ps}"
             others[key] = secondary(name, sp, local, args.secondary_steps, world,
-                                    0.0 if args.no_cpu_baseline else args.secondary_cpu_budget)
+                                    0.0 if args.no_cpu_baseline else args.secondary_cpu_budget, page_size=ps)
 
     if rank != 0:
         return
@@ -494,6 +498,7 @@ def main():
     ap.add_argument("--workload", default="llama3_8b_decode")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--spec-mode", default="prefill", choices=["prefill", "decode"])
+    ap.add_argument("--page-size", type=int, default=16, choices=[16, 128])
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
@@ -504,7 +509,7 @@ def main():
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     from paged_kv_cache_15_gb300.workloads import preset
-    W = preset(args.workload)
+    W = preset(args.workload, page_size=args.page_size)
     if args.impl == "reference":
         run_reference(args, W, rank, world)
     else:

@@ -94,10 +94,13 @@ typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
 /* ---- configuration --------------------------------------------------------
  * Fixed for the life of a context; every capacity bounds a fixed-size
  * metadata buffer in the workspace, so captured graphs can be replayed.
- * Supported: head_dim 64 or 128; page_size 16; num_q_heads a multiple of
- * num_kv_heads with a group size num_q_heads / num_kv_heads of at most 16;
- * E4M3 (FP8) pools with head_dim 128 on both paths (head_dim 64 with an
- * E4M3 pool returns PKV_ERR_UNSUPPORTED). */
+ * Supported: head_dim 64 or 128; page_size 16 or 128 (the 16-token page of
+ * the configs the library is tuned on, and the 128-token page that
+ * "--attention-backend", section "The obvious fix, and why it fails", names
+ * as fa4's native page size); num_q_heads a multiple of num_kv_heads with a
+ * group size num_q_heads / num_kv_heads of at most 16; E4M3 (FP8) pools with
+ * head_dim 128 on both paths (head_dim 64 with an E4M3 pool returns
+ * PKV_ERR_UNSUPPORTED). */
 typedef struct {
   int32_t num_q_heads;
   int32_t num_kv_heads;

@@ -64,7 +64,7 @@ struct DecodeCfg {
   static constexpr int kMinBlocks = kThreads <= 160 ? 2 : 1;  // two CTAs per SM hide latency for the decode shapes
   static constexpr int kRows = 8 * RT;
   static constexpr int kStageKeys = WK * KPW;
-  static constexpr int kStagePages = kStageKeys / kPageSize;
+  static constexpr int kStagePages = kStageKeys / kSegSlots;
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;
   static constexpr int kColBlocks = kRowBytes / 128;
@@ -76,7 +76,7 @@ struct DecodeCfg {
   static constexpr int kUnitQOffset = kAbortOffset + 16;  // unit queue: 2 full + 2 empty barriers, 2 ids
   static constexpr int kSmemBytes = kUnitQOffset + 40 + 1024;  // + alignment slack
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
-  static_assert(KPW % 16 == 0 && kStageKeys % kPageSize == 0, "stage must hold whole pages");
+  static_assert(KPW % 16 == 0 && kStageKeys % kSegSlots == 0, "stage must hold whole pages");
   static_assert(!(WK > 1) || (WK * 16 * D * 4 <= kStageBytes), "merge scratch must fit in one stage");
   static_assert(WK > 1 && RT >= 1 && RT <= 2, "key-major tiles: one or two 8-row tiles, key warps combined");
 };
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
         const int claimed = n_units > (int)gridDim.x ? (int)gridDim.x + atomicAdd(&plan[kDecodeNext], 1) : n_units;
         const DecodeItem it = a.m.decode_items[w / a.num_kv_heads];
         const int g = w % a.num_kv_heads;
-        const int base = a.m.kv_indptr[it.b] + it.p0;
+        const int base = a.m.seg_indptr[it.b] + it.p0;
         const int npages = it.p1 - it.p0;
         const int nst = (npages + C::kStagePages - 1) / C::kStagePages;
         for (int st = 0; st < nst; ++st) {
@@ -273,17 +273,17 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             break;
           }
           const int np = min(C::kStagePages, npages - st * C::kStagePages);
-          mbar_arrive_expect_tx(&full[slot], (uint32_t)(np * kPageSize * C::kRowBytes * 2));
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(np * kSegSlots * C::kRowBytes * 2));
           uint8_t* kdst = smem + slot * C::kStageBytes;
           uint8_t* vdst = kdst + C::kTileBytes;
           for (int p = 0; p < np; ++p) {
-            const int page = a.m.kv_indices[base + st * C::kStagePages + p];
+            const int page = a.m.seg_indices[base + st * C::kStagePages + p];
 #pragma unroll
             for (int cb = 0; cb < C::kColBlocks; ++cb) {
               const int x = g * D + cb * (128 / C::kElem);
-              const int off = cb * C::kStageKeys * 128 + p * kPageSize * 128;
-              tma_load_2d_hint(kdst + off, &tmap_k, x, page * kPageSize, &full[slot], pol);
-              tma_load_2d_hint(vdst + off, &tmap_v, x, page * kPageSize, &full[slot], pol);
+              const int off = cb * C::kStageKeys * 128 + p * kSegSlots * 128;
+              tma_load_2d_hint(kdst + off, &tmap_k, x, page * kSegSlots, &full[slot], pol);
+              tma_load_2d_hint(vdst + off, &tmap_v, x, page * kSegSlots, &full[slot], pol);
             }
           }
           armed |= 1u << slot;
@@ -329,12 +329,12 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
     const int q0 = a.m.qo_indptr[b];
     const int qo = a.m.qo_indptr[b + 1] - q0;
     const int nsplit = a.m.n_splits[b];
-    const int np_req = a.m.kv_indptr[b + 1] - a.m.kv_indptr[b];
+    const int np_req = a.m.seg_indptr[b + 1] - a.m.seg_indptr[b];
     const int rows_valid = qo * G;
     const bool skip = rows_valid > C::kRows;  // tile too small: recorded, pipeline still drained
     if (skip && lane == 0 && wk == 0) record_error(plan, PKV_DEV_QO_TOO_LONG, b);
-    const int key_begin = it.p0 * kPageSize;
-    const int key_end = min(it.p1 * kPageSize, L);
+    const int key_begin = it.p0 * kSegSlots;
+    const int key_end = min(it.p1 * kSegSlots, L);
     const int npages = it.p1 - it.p0;
     const int nst = (npages + C::kStagePages - 1) / C::kStagePages;
 
@@ -413,10 +413,10 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
         const uint32_t vbase = kbase + C::kTileBytes;
         const int stage_key0 = key_begin + st * C::kStageKeys;
         // last page of the request with a partial fill: zero the V rows past L
-        const bool tail = (it.p1 == np_req) && (st == nst - 1) && (L % kPageSize) != 0;
+        const bool tail = (it.p1 == np_req) && (st == nst - 1) && (L % kSegSlots) != 0;
         if (tail) {
           const int r0 = L - stage_key0;
-          const int r1 = min(C::kStagePages, npages - st * C::kStagePages) * kPageSize;
+          const int r1 = min(C::kStagePages, npages - st * C::kStagePages) * kSegSlots;
           uint8_t* vb8 = smem + slot * C::kStageBytes + C::kTileBytes;
           const int n16 = (r1 - r0) * C::kColBlocks * 8;
           for (int i = cw * 32 + lane; i < n16; i += C::kConsumerWarps * 32) {
@@ -746,10 +746,10 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   const uint64_t inner = (uint64_t)c.cfg.num_kv_heads * C::D;
   const uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
   const uint32_t box_inner = 128 / C::kElem;
-  if (encode_tmap_2d(&tk, dt, const_cast<void*>(k_pool), inner, slots, inner * C::kElem, box_inner, kPageSize,
+  if (encode_tmap_2d(&tk, dt, const_cast<void*>(k_pool), inner, slots, inner * C::kElem, box_inner, kSegSlots,
                      CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
-  if (encode_tmap_2d(&tv, dt, const_cast<void*>(v_pool), inner, slots, inner * C::kElem, box_inner, kPageSize,
+  if (encode_tmap_2d(&tv, dt, const_cast<void*>(v_pool), inner, slots, inner * C::kElem, box_inner, kSegSlots,
                      CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
   DecodeArgs a;
@@ -799,7 +799,7 @@ int decode_row_warps(const pkv_config& cfg) {
 // tile kernel, whose KV tiles are 128 keys (8 pages): their chunks are whole
 // tiles.
 int decode_stage_pages(const pkv_config& cfg) {
-  if (decode_row_warps(cfg) > 1) return kExtendKeys / kPageSize;
+  if (decode_row_warps(cfg) > 1) return kExtendKeys / kSegSlots;
   return cfg.kv_dtype == PKV_KV_FP8_E4M3 ? 8 : 4;
 }
 

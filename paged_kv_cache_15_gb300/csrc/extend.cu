@@ -229,7 +229,7 @@ struct ExtendArgs {
 // the decode path's merge combines.
 __device__ __forceinline__ ExtendTile load_unit(const ExtendArgs& a, int idx) {
   if (!a.dplan) return a.m.extend_tiles[idx];
-  constexpr int kPagesPerTile = kExtendKeys / kPageSize;
+  constexpr int kPagesPerTile = kExtendKeys / kSegSlots;
   const DecodeItem it = a.m.decode_items[idx];
   ExtendTile u;
   u.b = it.b;
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
                                                                    ExtendArgs a) {
   constexpr int D = C::D;
   constexpr int NK = C::NK, NV = C::NV;
-  constexpr int kPagesPerTile = kExtendKeys / kPageSize;
+  constexpr int kPagesPerTile = kExtendKeys / kSegSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
@@ -351,8 +351,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       const ExtendTile u = load_unit(a, w / a.num_kv_heads);
       const int g = w % a.num_kv_heads;
       const UnitKV ukv = unit_kv(u);
-      const int np = a.m.kv_indptr[u.b + 1] - a.m.kv_indptr[u.b];
-      const int page_base = a.m.kv_indptr[u.b];
+      const int np = a.m.seg_indptr[u.b + 1] - a.m.seg_indptr[u.b];
+      const int page_base = a.m.seg_indptr[u.b];
       if (!is_v) {
         // the unit's Q tiles, each once the previous unit's last QK on it has
         // finished: by TMA (a box of 128/G tokens x the group's G heads), or
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         const int e = e0 + (lane >> 3), p = lane & 7;
         if (e >= len) return 0;
         const int jj = seq_tile(e);
-        return p < np - jj * kPagesPerTile ? __ldg(a.m.kv_indices + page_base + jj * kPagesPerTile + p) : 0;
+        return p < np - jj * kPagesPerTile ? __ldg(a.m.seg_indices + page_base + jj * kPagesPerTile + p) : 0;
       };
       int grp = load_group(0);
       int grp_next = load_group(4);
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           break;
         }
         const bool leader = elect_one();
-        if (leader) mbar_arrive_expect_tx(&full[st], (uint32_t)(npg * kPageSize * D * 2));
+        if (leader) mbar_arrive_expect_tx(&full[st], (uint32_t)(npg * kSegSlots * D * 2));
         uint8_t* dst = smem + ring_off + st * C::kTileBytes;
 #pragma unroll
         for (int p = 0; p < kPagesPerTile; ++p) {
@@ -425,8 +425,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           if (p < npg && leader) {
 #pragma unroll
             for (int cb = 0; cb < C::kColBlocks; ++cb)
-              tma_load_2d_hint(dst + cb * (kExtendKeys * 128) + p * (kPageSize * 128), tmap, g * D + cb * 64,
-                               pg * kPageSize, &full[st], pol);
+              tma_load_2d_hint(dst + cb * (kExtendKeys * 128) + p * (kSegSlots * 128), tmap, g * D + cb * 64,
+                               pg * kSegSlots, &full[st], pol);
           }
         }
         armed |= 1u << st;
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       const int q0 = a.m.qo_indptr[b];
       const int qo = a.m.qo_indptr[b + 1] - q0;
       const int L = a.m.kv_len[b];
-      const int np = a.m.kv_indptr[b + 1] - a.m.kv_indptr[b];
+      const int np = a.m.seg_indptr[b + 1] - a.m.seg_indptr[b];
       const int R = u.row0 + (ukv.dual ? 0 : x * kExtendRows) + r;  // a dual unit's tiles hold the same rows
       const bool valid = R < qo * G;
       // a decode-plan unit holds one 128-row tile of rows (the configuration
@@ -687,14 +687,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         const bool diag = key0 + kExtendKeys - 1 > limit || (EXTRAS && key0 + kExtendKeys > draft0);
         // the request's last page inside this KV tile: zero the V rows past L
         // (done by the first tile that reads this V tile, before its PV)
-        if ((ukv.dual || x == 0 || jr >= nA) && np <= (j + 1) * kPagesPerTile && (L % kPageSize) != 0) {
+        if ((ukv.dual || x == 0 || jr >= nA) && np <= (j + 1) * kPagesPerTile && (L % kSegSlots) != 0) {
           const int vs = jj % NV;
           if (!mbar_wait_warp(&v_full[vs], (jj / NV) & 1, plan, s_abort)) {
             aborted = true;
             break;
           }
           const int r0 = L - j * kExtendKeys;
-          const int r1 = (np - j * kPagesPerTile) * kPageSize;
+          const int r1 = (np - j * kPagesPerTile) * kSegSlots;
           uint8_t* vt = smem + C::kVOff + vs * C::kTileBytes;
           const int n16 = (r1 - r0) * C::kColBlocks * 8;
           for (int i = r; i < n16; i += 128) {
@@ -914,11 +914,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   }
 }
 
-// E4M3 pools on the extend path: the batch's pages, in kv_indices order,
-// dequantised (code * scale, rounded once to bf16) into a compact copy whose
-// page i is the batch's i-th page, plus the identity page list idx[i] = i
-// through which the extend kernel reads it. One thread converts 16 codes
-// (one 16-byte vector) of K and of V.
+// E4M3 pools on the extend path: the batch's 16-slot segments, in
+// seg_indices order, dequantised (code * scale, rounded once to bf16) into a
+// compact copy whose segment i is the batch's i-th segment, plus the identity
+// list idx[i] = i through which the extend kernel reads it. One thread
+// converts 16 codes (one 16-byte vector) of K and of V.
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint16_t v, float scale) {
   const uint32_t h = e4m3x2_to_f16x2(v);  // exact
   float lo, hi;
@@ -929,18 +929,18 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint16_t v, float sc
 
 __global__ void __launch_bounds__(256) fp8_stage_kernel(const uint8_t* __restrict__ kp, const uint8_t* __restrict__ vp,
                                                         uint16_t* __restrict__ sk, uint16_t* __restrict__ sv,
-                                                        int* __restrict__ idx, const int* __restrict__ kv_indices,
-                                                        const int* __restrict__ plan, int page_elems, float k_scale,
+                                                        int* __restrict__ idx, const int* __restrict__ seg_indices,
+                                                        const int* __restrict__ plan, int seg_elems, float k_scale,
                                                         float v_scale) {
   pdl_launch_dependents();
-  pdl_wait();  // the page list comes from the metadata build before this launch
-  const int np = plan[kTotalPages];
-  const int vec = page_elems / 16;
+  pdl_wait();  // the segment list comes from the metadata build before this launch
+  const int np = plan[kTotalSegs];
+  const int vec = seg_elems / 16;
   const long long n = (long long)np * vec;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const int pi = (int)(i / vec), w = (int)(i % vec);
-    const long long src = (long long)kv_indices[pi] * page_elems + (long long)w * 16;
-    const long long dst = (long long)pi * page_elems + (long long)w * 16;
+    const long long src = (long long)seg_indices[pi] * seg_elems + (long long)w * 16;
+    const long long dst = (long long)pi * seg_elems + (long long)w * 16;
     const uint4 k = *reinterpret_cast<const uint4*>(kp + src);
     const uint4 v = *reinterpret_cast<const uint4*>(vp + src);
     const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
@@ -968,26 +968,26 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
   const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
   if (fp8) {
-    // widen the batch's E4M3 pages into the workspace copy and read that
+    // widen the batch's E4M3 segments into the workspace copy and read that
     if (!c.lay.has_stage) return PKV_ERR_UNSUPPORTED;
     uint16_t* sk = reinterpret_cast<uint16_t*>(c.ws + c.lay.stage_k);
     uint16_t* sv = reinterpret_cast<uint16_t*>(c.ws + c.lay.stage_v);
     int* idx = reinterpret_cast<int*>(c.ws + c.lay.stage_idx);
-    const int page_elems = c.cfg.page_size * c.cfg.num_kv_heads * C::D;
+    const int seg_elems = kSegSlots * c.cfg.num_kv_heads * C::D;
     if (launch_pdl(fp8_stage_kernel, dim3((unsigned)(c.num_sms * 4)), dim3(256), 0, st,
                    static_cast<const uint8_t*>(k_pool), static_cast<const uint8_t*>(v_pool), sk, sv, idx,
-                   make_meta(c).kv_indices, static_cast<const int*>(make_meta(c).plan), page_elems, k_scale,
+                   make_meta(c).seg_indices, static_cast<const int*>(make_meta(c).plan), seg_elems, k_scale,
                    v_scale) != cudaSuccess)
       return PKV_ERR_CUDA;
     k_pool = sk;
     v_pool = sv;
-    slots = (uint64_t)c.cfg.max_pages_total * c.cfg.page_size;
+    slots = (uint64_t)c.cfg.max_pages_total * (c.cfg.page_size / kSegSlots) * kSegSlots;
   }
   if (encode_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(k_pool), inner, slots, inner * 2, 64,
-                     kPageSize, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+                     kSegSlots, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
   if (encode_tmap_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(v_pool), inner, slots, inner * 2, 64,
-                     kPageSize, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+                     kSegSlots, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
   ExtendArgs a;
   a.m = make_meta(c);
@@ -999,7 +999,7 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
   // an E4M3 pool's scales are already in the dequantised copy
   a.scale_log2 = sm_scale * kLog2e;
-  if (fp8) a.m.kv_indices = reinterpret_cast<const int*>(c.ws + c.lay.stage_idx);
+  if (fp8) a.m.seg_indices = reinterpret_cast<const int*>(c.ws + c.lay.stage_idx);
   a.out_32B = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
   a.tree = active_tree(c);
   a.sinks = c.sinks;

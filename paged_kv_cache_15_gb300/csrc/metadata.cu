@@ -8,7 +8,10 @@
 //   kv_indices          = page_table[b, 0 : pages_b] concatenated over b
 //   kv_last_page_len[b] = L_b - (pages_b - 1) * page_size   (0 when L_b == 0)
 //   qo_indptr[b+1]      = qo_indptr[b] + qo_len_b
-// and two work lists:
+// the same lists over 16-slot segments when a page holds several (128-token
+// pages: segment k of a request is segment k % 8 of its page k / 8, id
+// page * 8 + k % 8), which is what the attention kernels gather; and two work
+// lists, counted in segments:
 //   decode path: (request, split, page range) items; every request's pages are
 //     cut into chunks of chunk_pages, with chunk_pages chosen so the number of
 //     (item, KV head) units fills the persistent grid a few times over and the
@@ -29,12 +32,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxCtas = 64;
-constexpr int kPagesPerKvTile = kExtendKeys / kPageSize;
+constexpr int kPagesPerKvTile = kExtendKeys / kSegSlots;
 
 struct ReqInfo {
   int L;       // KV length used (0 if the request's lengths were invalid)
   int qo;      // query rows
-  int np;      // pages
+  int np;      // 16-slot segments
+  int npg;     // pages
   int nsplit;  // decode splits
   int esplit;  // extend KV splits (1 unless the rows fit one unit and the range is cut)
   int prow;    // partial-output rows (0 when the request has a single split)
@@ -43,7 +47,8 @@ struct ReqInfo {
 };
 
 struct Sums {
-  long long np, qo, ns, pr, qt, npqo;
+  long long np, qo, ns, pr, qt, npqo;  // np: segments
+  long long npg;                       // pages
   long long et;  // KV tiles of the requests whose rows fit one extend unit
   int maxqo, splitd, splite;
   int maxnp;  // pages of the longest request
@@ -54,6 +59,8 @@ struct MetaArgs {
   int* kv_indptr;
   int* kv_indices;
   int* kv_last_page_len;
+  int* seg_indptr;   // aliases kv_indptr when a page is one segment
+  int* seg_indices;  // aliases kv_indices when a page is one segment
   int* qo_indptr;
   int* kv_len;
   int* n_splits;
@@ -68,9 +75,15 @@ struct MetaArgs {
   int stride;
   int bs;
   int num_pages;
+  int page_size;     // tokens per page: 16 or 128
+  int seg_per_page;  // page_size / 16
   int group;  // num_q_heads / num_kv_heads
   int num_kv_heads;
-  int stage_pages;  // the decode kernel's pages per pipeline stage
+  int stage_pages;  // the decode kernel's segments per pipeline stage
+  // the decode path runs on the tcgen05 tile kernel (verify shapes): its
+  // splits are equal shares of whole 128-key tiles, sized like the extend
+  // path's KV splits
+  int dec_tc;
   int units_target;      // decode work units to aim for
   int ext_grid;          // CTAs of the extend kernel (units are dealt to them by a fixed stride)
   int partial_cap;
@@ -87,7 +100,7 @@ struct MetaArgs {
 __device__ __forceinline__ void raw_lengths(const MetaArgs& a, int b, int& L, int& qo, bool& bad) {
   L = a.seq_lens[b];
   qo = a.qo_lens ? a.qo_lens[b] : 1;
-  bad = (L < 0) || (qo < 0) || (L > 0 && qo > L) || (L > 0 && (L - 1) / kPageSize >= a.stride);
+  bad = (L < 0) || (qo < 0) || (L > 0 && qo > L) || (L > 0 && (L - 1) / a.page_size >= a.stride);
   if (bad) {
     L = 0;
     qo = qo < 0 ? 0 : qo;
@@ -110,16 +123,23 @@ __device__ __forceinline__ void lengths(const MetaArgs& a, int b, int& L, int& q
   }
 }
 
-// pages of a validated length (no overflow near INT_MAX)
-__device__ __forceinline__ int pages_of(int L) { return L > 0 ? (L - 1) / kPageSize + 1 : 0; }
+// segments and pages of a validated length (no overflow near INT_MAX)
+__device__ __forceinline__ int segs_of(int L) { return L > 0 ? (L - 1) / kSegSlots + 1 : 0; }
+__device__ __forceinline__ int pages_of(const MetaArgs& a, int L) { return L > 0 ? (L - 1) / a.page_size + 1 : 0; }
 
 __device__ __forceinline__ int kv_tiles_of(int np) { return (np + kPagesPerKvTile - 1) / kPagesPerKvTile; }
 
 __device__ __forceinline__ ReqInfo req_info(const MetaArgs& a, int b, int chunk, int ext_ct) {
   ReqInfo r;
   lengths(a, b, r.L, r.qo, r.bad);
-  r.np = pages_of(r.L);
-  r.nsplit = r.np > 0 ? (r.np + chunk - 1) / chunk : 1;
+  r.np = segs_of(r.L);
+  r.npg = pages_of(a, r.L);
+  if (a.dec_tc) {
+    const int tiles = kv_tiles_of(r.np);
+    r.nsplit = tiles > ext_ct ? (tiles + ext_ct - 1) / ext_ct : 1;
+  } else {
+    r.nsplit = r.np > 0 ? (r.np + chunk - 1) / chunk : 1;
+  }
   r.prow = r.nsplit > 1 ? r.nsplit * r.qo : 0;
   r.qtiles = (r.qo * a.group + kExtendUnitRows - 1) / kExtendUnitRows;
   // rows that fit one extend unit: cut the KV range into equal splits of at
@@ -143,7 +163,7 @@ __device__ __forceinline__ int warp_max(int v) {
 
 // Block-wide sum of a Sums record (result valid in every thread).
 __device__ Sums block_sum(Sums s) {
-  __shared__ long long red[7][kThreads / 32];
+  __shared__ long long red[8][kThreads / 32];
   __shared__ int redm[kThreads / 32], redd[kThreads / 32], rede[kThreads / 32], redp[kThreads / 32];
   int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   s.np = warp_sum(s.np);
@@ -153,6 +173,7 @@ __device__ Sums block_sum(Sums s) {
   s.qt = warp_sum(s.qt);
   s.npqo = warp_sum(s.npqo);
   s.et = warp_sum(s.et);
+  s.npg = warp_sum(s.npg);
   s.maxqo = warp_max(s.maxqo);
   s.maxnp = warp_max(s.maxnp);
   s.splitd = warp_sum(s.splitd);
@@ -166,13 +187,14 @@ __device__ Sums block_sum(Sums s) {
     red[4][w] = s.qt;
     red[5][w] = s.npqo;
     red[6][w] = s.et;
+    red[7][w] = s.npg;
     redm[w] = s.maxqo;
     redp[w] = s.maxnp;
     redd[w] = s.splitd;
     rede[w] = s.splite;
   }
   __syncthreads();
-  Sums t{0, 0, 0, 0, 0, 0, 0, 0, 0};
+  Sums t{};
   for (int i = 0; i < kThreads / 32; ++i) {
     t.splitd += redd[i];
     t.splite += rede[i];
@@ -183,6 +205,7 @@ __device__ Sums block_sum(Sums s) {
     t.qt += red[4][i];
     t.npqo += red[5][i];
     t.et += red[6][i];
+    t.npg += red[7][i];
     t.maxqo = max(t.maxqo, redm[i]);
     t.maxnp = max(t.maxnp, redp[i]);
   }
@@ -225,7 +248,7 @@ __device__ int extend_split_tiles(const MetaArgs& a, int chunk, const Sums& tot)
     int L, qo;
     bool bad;
     lengths(a, b, L, qo, bad);
-    const int np = pages_of(L);
+    const int np = segs_of(L);
     const int qt = (qo * a.group + kExtendUnitRows - 1) / kExtendUnitRows;
     if (qt == 1 && np > chunk)
       split_units += (kv_tiles_of(np) + ct - 1) / ct;
@@ -253,15 +276,16 @@ __device__ int extend_split_tiles(const MetaArgs& a, int chunk, const Sums& tot)
   return ct_lo + (kExtCandidates - 1 - (int)(best % kExtCandidates));
 }
 
-// Exclusive block scan of five ints; returns this thread's prefix and the tile total.
-struct Scan5 {
-  int v[5];
+// Exclusive block scan of six ints; returns this thread's prefix and the tile total.
+constexpr int kScanN = 6;
+struct ScanV {
+  int v[kScanN];
 };
-__device__ Scan5 block_exclusive_scan(const Scan5& x, Scan5& total) {
-  __shared__ int part[5][kThreads / 32];
+__device__ ScanV block_exclusive_scan(const ScanV& x, ScanV& total) {
+  __shared__ int part[kScanN][kThreads / 32];
   int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  Scan5 inc = x;
-  for (int k = 0; k < 5; ++k) {
+  ScanV inc = x;
+  for (int k = 0; k < kScanN; ++k) {
     for (int o = 1; o < 32; o <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, inc.v[k], o);
       if (l >= o) inc.v[k] += y;
@@ -269,10 +293,10 @@ __device__ Scan5 block_exclusive_scan(const Scan5& x, Scan5& total) {
   }
   __syncthreads();
   if (l == 31)
-    for (int k = 0; k < 5; ++k) part[k][w] = inc.v[k];
+    for (int k = 0; k < kScanN; ++k) part[k][w] = inc.v[k];
   __syncthreads();
-  Scan5 ex;
-  for (int k = 0; k < 5; ++k) {
+  ScanV ex;
+  for (int k = 0; k < kScanN; ++k) {
     int before = 0, all = 0;
     for (int i = 0; i < kThreads / 32; ++i) {
       if (i < w) before += part[k][i];
@@ -293,14 +317,15 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   // grid has finished
   pdl_wait();
   // ---- 1. batch totals (identical in every CTA) ----
-  Sums s{0, 0, 0, 0, 0, 0, 0, 0, 0};
+  Sums s{};
   for (int b = threadIdx.x; b < a.bs; b += kThreads) {
     int L, qo;
     bool bad;
     raw_lengths(a, b, L, qo, bad);
     if (b < kLenCache) s_len_cache[b] = make_int2(L, bad ? (int)((unsigned)qo | 0x80000000u) : qo);
-    long long np = pages_of(L);
+    long long np = segs_of(L);
     s.np += np;
+    s.npg += pages_of(a, L);
     s.qo += qo;
     s.npqo += np * qo;
     s.maxqo = max(s.maxqo, qo);
@@ -308,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
     if (qo > 0 && (long long)qo * a.group <= kExtendUnitRows) s.et += kv_tiles_of((int)np);
   }
   Sums tot = block_sum(s);
-  bool over = tot.np > a.max_pages_total || tot.qo > a.max_q_tokens || tot.qo >= a.partial_cap;
+  bool over = tot.npg > a.max_pages_total || tot.qo > a.max_q_tokens || tot.qo >= a.partial_cap;
 
   // decode split size: fill the grid, never finer than the minimum chunk, and
   // keep sum over split requests of nsplit*qo below the partial buffer
@@ -329,9 +354,9 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
 
   if (over) {
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-      record_error(a.plan, PKV_DEV_CAPACITY, (int)tot.np);
+      record_error(a.plan, PKV_DEV_CAPACITY, (int)tot.npg);
       a.plan[kBatch] = 0;
-      a.plan[kTotalPages] = 0;
+      a.plan[kTotalSegs] = 0;
       a.plan[kTotalQ] = 0;
       a.plan[kDecodeItems] = 0;
       a.plan[kExtendTiles] = 0;
@@ -348,10 +373,11 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   // ---- 2. this CTA's request range and the prefix before it ----
   int per = (a.bs + gridDim.x - 1) / gridDim.x;
   int b0 = min(a.bs, (int)blockIdx.x * per), b1 = min(a.bs, b0 + per);
-  Sums pre{0, 0, 0, 0, 0, 0, 0, 0, 0};
+  Sums pre{};
   for (int b = threadIdx.x; b < b0; b += kThreads) {
     ReqInfo r = req_info(a, b, ichunk, ext_ct);
     pre.np += r.np;
+    pre.npg += r.npg;
     pre.qo += r.qo;
     pre.ns += r.nsplit;
     pre.pr += r.prow;
@@ -359,7 +385,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   }
   Sums base = block_sum(pre);
   // totals of the scanned quantities over the whole batch (for the plan words)
-  Sums all{0, 0, 0, 0, 0, 0, 0, 0, 0};
+  Sums all{};
   if (blockIdx.x == 0) {
     for (int b = threadIdx.x; b < a.bs; b += kThreads) {
       ReqInfo r = req_info(a, b, ichunk, ext_ct);
@@ -373,37 +399,41 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   }
 
   // ---- 3. scan the range tile by tile; per-element writes spread over the CTA ----
-  Scan5 carry{{(int)base.np, (int)base.qo, (int)base.ns, (int)base.pr, (int)base.qt}};
-  enum { kNp, kPBase, kQo, kQBase, kNs, kSBase, kQt, kTBase, kL, kEs, kInfo };
+  ScanV carry{{(int)base.np, (int)base.qo, (int)base.ns, (int)base.pr, (int)base.qt, (int)base.npg}};
+  enum { kNp, kPBase, kQo, kQBase, kNs, kSBase, kQt, kTBase, kL, kEs, kGBase, kInfo };
   __shared__ int s_info[kThreads][kInfo];
+  const bool segs = a.seg_per_page > 1;  // segment lists of their own (else they are the page lists)
   for (int t0 = b0; t0 < b1; t0 += kThreads) {
     const int b = t0 + threadIdx.x;
-    ReqInfo r{0, 0, 0, 0, 1, 0, 0, false};
+    ReqInfo r{0, 0, 0, 0, 0, 1, 0, 0, false};
     const bool live = b < b1;
     if (live) r = req_info(a, b, ichunk, ext_ct);
-    Scan5 x{{r.np, r.qo, r.nsplit, r.prow, r.qtiles}};
-    if (!live) x = Scan5{{0, 0, 0, 0, 0}};
-    Scan5 tile_tot;
-    Scan5 ex = block_exclusive_scan(x, tile_tot);
+    ScanV x{{r.np, r.qo, r.nsplit, r.prow, r.qtiles, r.npg}};
+    if (!live) x = ScanV{};
+    ScanV tile_tot;
+    ScanV ex = block_exclusive_scan(x, tile_tot);
     const int p_np = carry.v[0] + ex.v[0], p_qo = carry.v[1] + ex.v[1], p_ns = carry.v[2] + ex.v[2];
-    const int p_pr = carry.v[3] + ex.v[3], p_qt = carry.v[4] + ex.v[4];
+    const int p_pr = carry.v[3] + ex.v[3], p_qt = carry.v[4] + ex.v[4], p_pg = carry.v[5] + ex.v[5];
     if (live) {
       if (r.bad) record_error(a.plan, PKV_DEV_BAD_LENGTH, b);
-      a.kv_indptr[b] = p_np;
+      a.kv_indptr[b] = p_pg;
+      if (segs) a.seg_indptr[b] = p_np;
       a.qo_indptr[b] = p_qo;
       a.partial_indptr[b] = p_pr;
       a.kv_len[b] = r.L;
       a.n_splits[b] = r.nsplit;
       a.ext_splits[b] = r.esplit;
-      a.kv_last_page_len[b] = r.np > 0 ? r.L - (r.np - 1) * kPageSize : 0;
+      a.kv_last_page_len[b] = r.npg > 0 ? r.L - (r.npg - 1) * a.page_size : 0;
       if (b == a.bs - 1) {
-        a.kv_indptr[a.bs] = p_np + r.np;
+        a.kv_indptr[a.bs] = p_pg + r.npg;
+        if (segs) a.seg_indptr[a.bs] = p_np + r.np;
         a.qo_indptr[a.bs] = p_qo + r.qo;
         a.partial_indptr[a.bs] = p_pr + r.prow;
       }
       int* inf = s_info[threadIdx.x];
       inf[kNp] = r.np;
       inf[kPBase] = p_np;
+      inf[kGBase] = p_pg;
       inf[kQo] = r.qo;
       inf[kQBase] = p_qo;
       inf[kNs] = r.nsplit;
@@ -421,21 +451,33 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
       const int np = inf[kNp], pbase = inf[kPBase], qo = inf[kQo], qbase = inf[kQBase];
       const int ns = inf[kNs], sbase = inf[kSBase], qt = inf[kQt], tbase = inf[kTBase], L = inf[kL];
       const int* __restrict__ row = a.page_table + (long long)bb * a.stride;
-      for (int p = threadIdx.x; p < np; p += kThreads) {
+      // segment k is segment k % R of page k / R (R = segments per page); the
+      // page list takes each page once
+      const int R = a.seg_per_page, gbase = inf[kGBase];
+      for (int k = threadIdx.x; k < np; k += kThreads) {
+        const int p = k / R, sub = k - p * R;
         int page = row[p];
         if (page < 0 || page >= a.num_pages) {
           record_error(a.plan, PKV_DEV_BAD_PAGE, bb);
           page = 0;
         }
-        a.kv_indices[pbase + p] = page;
+        if (sub == 0) a.kv_indices[gbase + p] = page;
+        if (segs) a.seg_indices[pbase + k] = page * R + sub;
       }
       for (int sp = threadIdx.x; sp < ns; sp += kThreads) {
         if (sbase + sp < a.max_items) {
           DecodeItem it;
           it.b = bb;
           it.split = sp;
-          it.p0 = sp * ichunk;
-          it.p1 = min(np, (sp + 1) * ichunk);
+          if (a.dec_tc) {
+            // equal shares of the request's 128-key tiles
+            const int tiles = kv_tiles_of(np);
+            it.p0 = (int)((long long)sp * tiles / ns) * kPagesPerKvTile;
+            it.p1 = min(np, (int)((long long)(sp + 1) * tiles / ns) * kPagesPerKvTile);
+          } else {
+            it.p0 = sp * ichunk;
+            it.p1 = min(np, (sp + 1) * ichunk);
+          }
           a.items[sbase + sp] = it;
         }
       }
@@ -466,20 +508,21 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
       }
       for (int i = threadIdx.x; i < qo; i += kThreads) a.token_req[qbase + i] = bb;
     }
-    for (int k = 0; k < 5; ++k) carry.v[k] += tile_tot.v[k];
+    for (int k = 0; k < kScanN; ++k) carry.v[k] += tile_tot.v[k];
     __syncthreads();
   }
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (a.bs == 0) {
       a.kv_indptr[0] = 0;
+      if (segs) a.seg_indptr[0] = 0;
       a.qo_indptr[0] = 0;
       a.partial_indptr[0] = 0;
     }
     bool items_over = all.ns > a.max_items || all.qt > a.max_tiles;
     if (items_over) record_error(a.plan, PKV_DEV_CAPACITY, -1);
     a.plan[kBatch] = a.bs;
-    a.plan[kTotalPages] = (int)tot.np;
+    a.plan[kTotalSegs] = (int)tot.np;
     a.plan[kTotalQ] = (int)tot.qo;
     a.plan[kDecodeItems] = items_over ? 0 : (int)all.ns;
     a.plan[kChunkPages] = ichunk;
@@ -502,6 +545,8 @@ int launch_build_metadata(Ctx& c, int batch, const int32_t* seq_lens, const int3
   a.kv_indptr = const_cast<int*>(m.kv_indptr);
   a.kv_indices = const_cast<int*>(m.kv_indices);
   a.kv_last_page_len = const_cast<int*>(m.kv_last_page_len);
+  a.seg_indptr = const_cast<int*>(m.seg_indptr);
+  a.seg_indices = const_cast<int*>(m.seg_indices);
   a.qo_indptr = const_cast<int*>(m.qo_indptr);
   a.kv_len = const_cast<int*>(m.kv_len);
   a.n_splits = const_cast<int*>(m.n_splits);
@@ -516,9 +561,12 @@ int launch_build_metadata(Ctx& c, int batch, const int32_t* seq_lens, const int3
   a.stride = stride;
   a.bs = batch;
   a.num_pages = c.cfg.num_pages;
+  a.page_size = c.cfg.page_size;
+  a.seg_per_page = c.cfg.page_size / kSegSlots;
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
   a.num_kv_heads = c.cfg.num_kv_heads;
   a.stage_pages = decode_stage_pages(c.cfg);
+  a.dec_tc = decode_row_warps(c.cfg) > 1 ? 1 : 0;
   a.units_target = c.decode_ctas * (decode_row_warps(c.cfg) == 1 ? kDecodeTargetWaves : kVerifyTargetWaves);
   a.ext_grid = c.extend_ctas;
   a.partial_cap = c.lay.partial_rows_cap;

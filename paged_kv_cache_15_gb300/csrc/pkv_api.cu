@@ -28,7 +28,7 @@ int check_config(const pkv_config* cfg) {
   if (cfg->num_q_heads % cfg->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int group = cfg->num_q_heads / cfg->num_kv_heads;
   if (group > 16) return PKV_ERR_UNSUPPORTED;
-  if (cfg->page_size != kPageSize) return PKV_ERR_UNSUPPORTED;
+  if (cfg->page_size != kPageSizeSmall && cfg->page_size != kPageSizeLarge) return PKV_ERR_UNSUPPORTED;
   if (cfg->head_dim != 64 && cfg->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (cfg->kv_dtype == PKV_KV_FP8_E4M3 && cfg->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (decode_row_warps(*cfg) == 0) return PKV_ERR_UNSUPPORTED;  // max_qo_len * group > 128
@@ -36,19 +36,26 @@ int check_config(const pkv_config* cfg) {
   const long long slots = (long long)cfg->num_pages * cfg->page_size;
   if (slots > (1ll << 31) - 1) return PKV_ERR_UNSUPPORTED;
   if ((long long)cfg->max_q_tokens * cfg->num_q_heads * cfg->head_dim > (1ll << 40)) return PKV_ERR_UNSUPPORTED;
+  // segment counts (pages times segments per page) must fit an int
+  if ((long long)cfg->max_pages_total * (cfg->page_size / kSegSlots) > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
   return PKV_OK;
+}
+
+// 16-slot segments the batch's pages can hold at most
+long long max_segments(const pkv_config& cfg) {
+  return (long long)cfg.max_pages_total * (cfg.page_size / kSegSlots);
 }
 
 // Persistent-grid sizes: two decode CTAs and one extend CTA per SM, never
 // more than the configuration can ever give them work. Decode items per batch
-// are at most max_pages_total / (minimum chunk) + max_batch (every request
-// adds at most one partial chunk); extend units at most
+// are at most (segments) / (minimum chunk) + max_batch (every request adds at
+// most one partial chunk); extend units at most
 // ceil(max_q_tokens * group / 256) + max_batch, plus as many KV splits as
 // decode items.
 void grid_sizes(const pkv_config& cfg, int num_sms, int* decode_ctas, int* extend_ctas) {
   const long long group = cfg.num_q_heads / cfg.num_kv_heads;
   const long long dec_units =
-      (long long)cfg.num_kv_heads * ((long long)cfg.max_pages_total / kDecodeMinChunkPages + cfg.max_batch + 1);
+      (long long)cfg.num_kv_heads * (max_segments(cfg) / kDecodeMinChunkPages + cfg.max_batch + 1);
   const long long ext_units =
       (long long)cfg.num_kv_heads * (((long long)cfg.max_q_tokens * group + kExtendUnitRows - 1) / kExtendUnitRows +
                                      cfg.max_batch) +
@@ -90,6 +97,9 @@ Layout make_layout(const pkv_config& cfg, int num_sms, bool with_stage) {
   L.ext_splits = take(sizeof(int) * cfg.max_batch);
   L.partial_indptr = take(sizeof(int) * (cfg.max_batch + 1));
   L.token_req = take(sizeof(int) * (size_t)cfg.max_q_tokens);
+  L.seg_per_page = cfg.page_size / kSegSlots;
+  L.seg_indptr = L.seg_per_page > 1 ? take(sizeof(int) * (cfg.max_batch + 1)) : L.kv_indptr;
+  L.seg_indices = L.seg_per_page > 1 ? take(sizeof(int) * (size_t)max_segments(cfg)) : L.kv_indices;
   L.decode_items = take(sizeof(DecodeItem) * (size_t)L.max_decode_items);
   L.extend_tiles = take(sizeof(ExtendTile) * (size_t)L.max_extend_tiles);
   L.partial_o = take(sizeof(uint16_t) * (size_t)cap * cfg.num_q_heads * cfg.head_dim);
@@ -97,10 +107,10 @@ Layout make_layout(const pkv_config& cfg, int num_sms, bool with_stage) {
   L.has_stage = with_stage && cfg.kv_dtype == PKV_KV_FP8_E4M3;
   L.stage_k = L.stage_v = L.stage_idx = 0;
   if (L.has_stage) {
-    const size_t page_bytes = (size_t)cfg.page_size * cfg.num_kv_heads * cfg.head_dim * sizeof(uint16_t);
-    L.stage_k = take(page_bytes * (size_t)cfg.max_pages_total);
-    L.stage_v = take(page_bytes * (size_t)cfg.max_pages_total);
-    L.stage_idx = take(sizeof(int) * (size_t)cfg.max_pages_total);
+    const size_t seg_bytes = (size_t)kSegSlots * cfg.num_kv_heads * cfg.head_dim * sizeof(uint16_t);
+    L.stage_k = take(seg_bytes * (size_t)max_segments(cfg));
+    L.stage_v = take(seg_bytes * (size_t)max_segments(cfg));
+    L.stage_idx = take(sizeof(int) * (size_t)max_segments(cfg));
   }
   L.total = off;
   return L;
@@ -159,6 +169,8 @@ Meta make_meta(const Ctx& c) {
   m.plan = reinterpret_cast<int*>(w + c.lay.plan);
   m.kv_indptr = reinterpret_cast<const int*>(w + c.lay.kv_indptr);
   m.kv_indices = reinterpret_cast<const int*>(w + c.lay.kv_indices);
+  m.seg_indptr = reinterpret_cast<const int*>(w + c.lay.seg_indptr);
+  m.seg_indices = reinterpret_cast<const int*>(w + c.lay.seg_indices);
   m.kv_last_page_len = reinterpret_cast<const int*>(w + c.lay.kv_last_page_len);
   m.qo_indptr = reinterpret_cast<const int*>(w + c.lay.qo_indptr);
   m.kv_len = reinterpret_cast<const int*>(w + c.lay.kv_len);

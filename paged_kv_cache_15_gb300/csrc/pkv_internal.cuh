@@ -16,7 +16,16 @@ namespace pkv {
 // ---------------------------------------------------------------------------
 // Fixed tiling constants
 // ---------------------------------------------------------------------------
-constexpr int kPageSize = 16;           // the only page size the library accepts
+// The kernels gather the KV cache in segments of 16 consecutive slots of one
+// page (one 16-row TMA box per segment and 128-byte column block): a page of
+// 16 tokens is one segment, a page of 128 tokens eight. The metadata build
+// lists every request's segments (seg_indptr / seg_indices, the slot of
+// segment s being seg_indices[s] * 16); with 16-token pages the segment lists
+// are the page lists themselves.
+constexpr int kSegSlots = 16;
+// page sizes the library accepts (tokens per page)
+constexpr int kPageSizeSmall = 16;
+constexpr int kPageSizeLarge = 128;
 // split-KV aims at this many work units per CTA slot: 16-row decode units
 // are light and balance best when fine; the verify shapes' units carry up to
 // 128 rows each and pay more per unit
@@ -41,7 +50,7 @@ enum PlanWord : int {
   kErr = 0,            // first device error (PKV_DEV_*), 0 when clean
   kErrIndex = 1,       // index that raised it
   kBatch = 2,          // batch size of the last build
-  kTotalPages = 3,     // kv_indptr[bs]
+  kTotalSegs = 3,      // seg_indptr[bs]: 16-slot segments of the batch
   kTotalQ = 4,         // qo_indptr[bs]
   kDecodeItems = 5,    // number of (request, split) items on the decode path
   kChunkPages = 6,     // pages per split on the decode path
@@ -54,7 +63,8 @@ enum PlanWord : int {
   kPlanWords = 32
 };
 
-// Work item of the decode path: request, split index, page range [p0, p1).
+// Work item of the decode path: request, split index, segment range [p0, p1)
+// of the request's 16-slot segments.
 struct DecodeItem {
   int b, split, p0, p1;
 };
@@ -75,6 +85,10 @@ struct ExtendTile {
 struct Layout {
   size_t plan, kv_indptr, kv_indices, kv_last_page_len, qo_indptr, kv_len, n_splits, ext_splits, partial_indptr,
       token_req, decode_items, extend_tiles, partial_o, partial_lse, total;
+  // segment lists of pages larger than one segment (seg_per_page > 1);
+  // with one segment per page they alias kv_indptr / kv_indices
+  size_t seg_indptr, seg_indices;
+  int seg_per_page;
   // E4M3 pools on the extend path: bf16 copies of the codes of the batch's
   // pages (K and V, max_pages_total pages each) and the identity page list
   // that reads them; absent (has_stage false) for bf16 pools
@@ -106,8 +120,10 @@ inline const uint64_t* active_tree(const Ctx& c) {
 // Device-side view of the metadata in the workspace.
 struct Meta {
   int* plan;
-  const int* kv_indptr;
+  const int* kv_indptr;    // pages (the public metadata)
   const int* kv_indices;
+  const int* seg_indptr;   // 16-slot segments: what the kernels gather
+  const int* seg_indices;  // segment s of the batch covers slots seg_indices[s] * 16 .. + 15
   const int* kv_last_page_len;
   const int* qo_indptr;
   const int* kv_len;

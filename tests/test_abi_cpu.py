@@ -77,6 +77,8 @@ def _cfg(**kw):
     (dict(num_kv_heads=0), B.PKV_ERR_INVALID_ARG),
     (dict(head_dim=96), B.PKV_ERR_UNSUPPORTED),
     (dict(page_size=32), B.PKV_ERR_UNSUPPORTED),
+    (dict(page_size=64), B.PKV_ERR_UNSUPPORTED),
+    (dict(page_size=256), B.PKV_ERR_UNSUPPORTED),
     (dict(kv_dtype=7), B.PKV_ERR_INVALID_ARG),
     (dict(kv_dtype=B.PKV_KV_FP8_E4M3, head_dim=64), B.PKV_ERR_UNSUPPORTED),
     (dict(num_q_heads=64, num_kv_heads=2), B.PKV_ERR_UNSUPPORTED),  # group 32
@@ -100,3 +102,12 @@ def test_null_arguments_rejected(lib):
     assert L.pkv_destroy(None) == B.PKV_OK
     code = ctypes.c_int32(0)
     assert L.pkv_get_device_error(None, ctypes.byref(code), None) == B.PKV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("page_size", [16, 128])
+def test_supported_page_sizes_accepted(lib, page_size):
+    """Both page sizes pass the configuration checks (without a device the
+    call then stops at the SM-count query with PKV_ERR_CUDA)."""
+    n = ctypes.c_size_t(0)
+    st = B.lib().pkv_workspace_bytes(ctypes.byref(_cfg(page_size=page_size)), ctypes.byref(n))
+    assert st in (B.PKV_OK, B.PKV_ERR_CUDA)

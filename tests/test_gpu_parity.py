@@ -292,6 +292,90 @@ def test_full_size_verify_decode_path_every_row():
     full_check(preset("spec_verify"), spec_mode=B.PKV_SPEC_DECODE)
 
 
+# ------------------------------------------------------------------ 128-token pages
+@pytest.mark.parametrize("name", FULL_PRESETS)
+def test_page_size_128_metadata_and_pools_bit_exact(name):
+    """Every named case at full size in 128-token pages: kv_indptr /
+    kv_indices / kv_last_page_len count 128-token pages, bit for bit against
+    the oracle; the pools after set_kv_buffer likewise."""
+    W = preset(name, page_size=128)
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    d.build_metadata()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    kp, vp = oracle_pools(W)
+    assert np.array_equal(pool_bits(d.k_pool.cpu()), kp)
+    assert np.array_equal(pool_bits(d.v_pool.cpu()), vp)
+    del kp, vp
+    ref = oracle_meta(W)
+    p_indptr, p_indices, p_last, p_qo = B.pkv_get_metadata(d.ctx)
+    n_pages = int(ref["kv_indptr"][-1])
+    assert np.array_equal(workspace_ints(d, p_indptr, W.bs + 1), ref["kv_indptr"])
+    assert np.array_equal(workspace_ints(d, p_indices, n_pages), ref["kv_indices"])
+    assert np.array_equal(workspace_ints(d, p_last, W.bs), ref["kv_last_page_len"])
+    assert np.array_equal(workspace_ints(d, p_qo, W.bs + 1), ref["qo_indptr"])
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_decode", "prefix_extend"])
+def test_page_size_128_full_size_every_row(name):
+    """The Llama-3-8B-shaped decode and the prefix-cached extend at full size
+    in 128-token pages, every row against the oracle."""
+    full_check(preset(name, page_size=128))
+
+
+@pytest.mark.parametrize("case", ["tiny", "fp8_decode", "verify_decode", "verify_prefill", "fp8_extend", "tree",
+                                  "mixed_extend", "d64"])
+def test_page_size_128_parity(case):
+    """128-token pages on every path: decode (bf16 and E4M3), verify on both
+    paths, extend on E4M3 pools, draft trees with sinks, mixed extend batches
+    whose lengths end anywhere inside a page, head_dim 64."""
+    spec = B.PKV_SPEC_PREFILL
+    if case == "tiny":
+        W = preset("tiny_decode", page_size=128)
+    elif case == "fp8_decode":
+        W = preset("long_fp8_decode", bs=4, len_scale=1 / 16, page_size=128)
+    elif case == "verify_decode":
+        W = preset("spec_verify", bs=8, len_scale=0.1, page_size=128)
+        spec = B.PKV_SPEC_DECODE
+    elif case == "verify_prefill":
+        W = preset("spec_verify", bs=8, len_scale=0.1, page_size=128)
+    elif case == "fp8_extend":
+        W = preset("prefix_extend_fp8", bs=3, len_scale=0.2, page_size=128)
+    elif case == "tree":
+        rng = np.random.default_rng(51)
+        W = make_workload("t128", "verify", 5, 32, 4, 128, rng.integers(0, 3000, 5), rng.integers(1, 17, 5),
+                          page_size=128)
+        W.tree_mask = random_tree_masks(W.qo_lens, seed=51)
+        W.sinks = random_sinks(W.num_q_heads, seed=52)
+    elif case == "mixed_extend":
+        W = make_workload("m128", "extend", 6, 32, 8, 128, [0, 127, 128, 129, 1000, 4095], [1, 1, 300, 2, 129, 64],
+                          page_size=128)
+    else:
+        W = make_workload("d128", "extend", 4, 8, 2, 64, [5, 0, 300, 129], [200, 33, 7, 128], page_size=128)
+    full_check(W, spec_mode=spec)
+
+
+def test_page_size_128_row_shorter_than_a_request_recorded():
+    """The page-table row holds 128-token pages: a request of 300 tokens needs
+    3 entries, so a stride of 2 makes it a bad length (recorded, empty)."""
+    W = make_workload("s128", "decode", 3, 8, 2, 64, [99, 299, 200], np.ones(3), page_size=128)
+    d = DeviceBatch(W)
+    table = torch.zeros((W.bs + 2, 2), dtype=torch.int32, device=d.page_table.device)
+    table[:W.bs] = d.page_table[:, :2]
+    d.page_table = table[:W.bs]
+    d.step()
+    torch.cuda.synchronize()
+    assert d.device_error() == B.PKV_DEV_BAD_LENGTH
+    out = d.out.double().cpu().numpy()
+    lse = d.lse.double().cpu().numpy()
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+    W.seq_lens = np.array([W.seq_lens[0], 0, W.seq_lens[2]], dtype=W.seq_lens.dtype)
+    ref_o, ref_lse = oracle_reference(W)
+    check_close(out, ref_o, "o")
+    check_close(lse, ref_lse, "lse")
+
+
 # ------------------------------------------------------------------ device-side data errors
 def test_bad_page_id_recorded_without_fault():
     W = preset("tiny_decode")

@@ -343,6 +343,23 @@ def test_p3_page_size_1_equals_16():
     assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
 
 
+@pytest.mark.parametrize("name", ["tiny_decode", "prefix_extend", "spec_verify"])
+def test_p3_page_size_128_equals_16_equals_1(name):
+    """The same tokens in 128-token pages, in 16-token pages and in one-token
+    pages give the same attention, bit for bit: the presets draw the values of
+    every (request, position) in the same order whatever the page size, and
+    only the pages that hold them differ."""
+    kw = {} if name == "tiny_decode" else dict(bs=3, len_scale=0.05)
+    W16 = preset(name, **kw)
+    W128 = preset(name, page_size=128, **kw)
+    assert W128.page_size == 128 and not np.array_equal(W128.loc, W16.loc)
+    o16, l16 = oracle_reference(W16)
+    o128, l128 = oracle_reference(W128)
+    o1, l1 = _run_layout(W128, *_relayout(W128, None, new_page_size=1))
+    assert np.array_equal(o16, o128) and np.array_equal(l16, l128)
+    assert np.array_equal(o1, o128) and np.array_equal(l1, l128)
+
+
 # ---------------------------------------------------------------- P4 / P5 / P6 closed forms
 def test_p4_single_key():
     W = make_workload("one", "decode", 2, 4, 2, 8, [0, 0], [1, 1], page_size=4)
