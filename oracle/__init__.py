@@ -83,12 +83,12 @@ def _load():
         lib.oracle_build_metadata.argtypes = [ctypes.c_int, ctypes.c_int, i32p, i32p, i32p, ctypes.c_int64,
                                               i32p, i32p, i32p, i32p]
         lib.oracle_set_kv_buffer.restype = None
-        lib.oracle_set_kv_buffer.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, i32p, vp, vp,
-                                             ctypes.c_int, ctypes.c_float, ctypes.c_float]
+        lib.oracle_set_kv_buffer.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p,
+                                             vp, vp, ctypes.c_int, ctypes.c_float, ctypes.c_float]
         lib.oracle_lse_merge.restype = None
         lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]
         lib.oracle_attention.restype = ctypes.c_int
-        lib.oracle_attention.argtypes = [ctypes.c_int] * 6 + [vp, vp, vp, i32p, i32p, i32p, i32p, vp, vp,
+        lib.oracle_attention.argtypes = [ctypes.c_int] * 7 + [vp, vp, vp, i32p, i32p, i32p, i32p, vp, vp,
                                                                ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                                                ctypes.c_int64, i32p, i32p, vp, vp, ctypes.c_int]
         lib.oracle_pool_bytes.restype = ctypes.c_int64
@@ -159,15 +159,18 @@ def build_metadata(seq_lens, page_table, page_size, qo_lens=None):
 
 
 def set_kv_buffer(k_pool, v_pool, loc, k_new, v_new, kv_dtype=KV_BF16, k_inv_scale=1.0, v_inv_scale=1.0):
-    """Scatter in place. Pools: uint16 (bf16 bits) or uint8 (e4m3) arrays [slots, Hkv, D];
-    k_new/v_new: uint16 bf16 bits [n, Hkv, D]; loc: int32 [n]."""
+    """Scatter in place. Pools: uint16 (bf16 bits) or uint8 (e4m3) arrays [slots, Hkv, D]
+    (K) and [slots, Hkv, Dv] (V); k_new/v_new: uint16 bf16 bits [n, Hkv, D] / [n, Hkv, Dv];
+    loc: int32 [n]."""
     lib = _load()
     assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
     kn = np.ascontiguousarray(k_new, dtype=np.uint16)
     vn = np.ascontiguousarray(v_new, dtype=np.uint16)
     lc, lc_p = _i32(loc)
     n, hkv, d = kn.shape
-    lib.oracle_set_kv_buffer(int(kv_dtype), _ptr(k_pool), _ptr(v_pool), hkv, d, lc_p, _ptr(kn), _ptr(vn), n,
+    dv = vn.shape[2] if vn.ndim == 3 else d
+    assert k_pool.shape[-1] == d and v_pool.shape[-1] == dv
+    lib.oracle_set_kv_buffer(int(kv_dtype), _ptr(k_pool), _ptr(v_pool), hkv, d, dv, lc_p, _ptr(kn), _ptr(vn), n,
                              float(k_inv_scale), float(v_inv_scale))
 
 
@@ -186,10 +189,11 @@ def attention(q, k_pool, v_pool, meta, num_q_heads, num_kv_heads, page_size, sm_
               k_scale=1.0, v_scale=1.0, rows=None, nthreads=None, tree_mask=None, sinks=None):
     """fp64 attention over the paged pool.
 
-    q: uint16 bf16 bits [T, Hq, D]; pools: uint16 / uint8 [slots, Hkv, D];
+    q: uint16 bf16 bits [T, Hq, D]; pools: uint16 / uint8, K [slots, Hkv, D]
+    and V [slots, Hkv, Dv] (Dv = D unless K and V heads differ in width);
     meta: dict from build_metadata. rows: None for every (token, head) row —
-    returns o [T, Hq, D], lse [T, Hq] — or an int array [n, 2] of (token, head)
-    pairs — returns o [n, D], lse [n]. tree_mask: None (chain drafts,
+    returns o [T, Hq, Dv], lse [T, Hq] — or an int array [n, 2] of (token, head)
+    pairs — returns o [n, Dv], lse [n]. tree_mask: None (chain drafts,
     bottom-right causal) or uint64 [T]: bit j of token t's word lets it see
     the j-th new token of its request (every cached key stays visible).
     sinks: None or float [Hq], each head's sink logit (a key with that score
@@ -199,6 +203,8 @@ def attention(q, k_pool, v_pool, meta, num_q_heads, num_kv_heads, page_size, sm_
     q = np.ascontiguousarray(q, dtype=np.uint16)
     T, hq, d = q.shape
     assert hq == num_q_heads
+    dv = v_pool.shape[-1]
+    assert k_pool.shape[-1] == d
     bs = meta["kv_indptr"].shape[0] - 1
     kvp, kvp_p = _i32(meta["kv_indptr"])
     kvi, kvi_p = _i32(meta["kv_indices"] if meta["kv_indices"].size else np.zeros(1))
@@ -209,14 +215,14 @@ def attention(q, k_pool, v_pool, meta, num_q_heads, num_kv_heads, page_size, sm_
     if rows is None:
         n_rows = T * hq
         rt_p = rh_p = None
-        out_o = np.zeros((T, hq, d), dtype=np.float64)
+        out_o = np.zeros((T, hq, dv), dtype=np.float64)
         out_lse = np.zeros((T, hq), dtype=np.float64)
     else:
         rows = np.asarray(rows, dtype=np.int32).reshape(-1, 2)
         n_rows = rows.shape[0]
         rt, rt_p = _i32(rows[:, 0])
         rh, rh_p = _i32(rows[:, 1])
-        out_o = np.zeros((n_rows, d), dtype=np.float64)
+        out_o = np.zeros((n_rows, dv), dtype=np.float64)
         out_lse = np.zeros((n_rows,), dtype=np.float64)
     tm = None if tree_mask is None else np.ascontiguousarray(tree_mask, dtype=np.uint64)
     if tm is not None:
@@ -224,7 +230,7 @@ def attention(q, k_pool, v_pool, meta, num_q_heads, num_kv_heads, page_size, sm_
     sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float64)
     if sk is not None:
         assert sk.shape == (hq,)
-    st = lib.oracle_attention(bs, hq, num_kv_heads, d, page_size, int(kv_dtype), _ptr(q), _ptr(k_pool),
+    st = lib.oracle_attention(bs, hq, num_kv_heads, d, dv, page_size, int(kv_dtype), _ptr(q), _ptr(k_pool),
                               _ptr(v_pool), kvp_p, kvi_p, last_p, qoi_p, None if tm is None else _ptr(tm),
                               None if sk is None else _ptr(sk),
                               float(sm_scale), float(k_scale),

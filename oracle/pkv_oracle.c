@@ -17,6 +17,9 @@
  *     definition of scaled dot-product attention, o = softmax(s) V with
  *     s_j = sm_scale * q . k_j, restricted to the keys a query row may see
  *     (bottom-right causal alignment), and lse = ln sum_j exp(s_j).
+ *   - "--attention-backend", section "How SGLang picks a default": some models
+ *     have K and V heads of different widths. q and k then have head_dim
+ *     columns, v and the output head_dim_v; nothing else changes.
  *   - FP8 KV entries are OCP "E4M3FN" (bias 7, 3 mantissa bits, max 448, no
  *     infinities, NaN = S.1111.111), decoded bit by bit from that definition.
  *
@@ -30,7 +33,9 @@
  * brute force and torch SDPA with the same mask, and a chain-shaped tree
  * reproducing the causal result exactly; for sinks, -inf sinks reproducing
  * the result without them exactly, torch SDPA with the sink as an extra key,
- * and the uniform-score closed form.
+ * and the uniform-score closed form; for K and V of different widths, brute
+ * force and torch SDPA with those widths, and zero-padded K/Q columns
+ * reproducing the equal-width result exactly.
  */
 #include <math.h>
 #include <pthread.h>
@@ -180,29 +185,31 @@ int oracle_build_metadata(int bs, int page_size, const int32_t* seq_lens, const 
 /* set_kv_buffer (save_kv_cache)                                             */
 /* ------------------------------------------------------------------------- */
 
-/* Pool layout: [slot][kv_head][head_dim], slot = page * page_size + offset.
+/* Pool layout: [slot][kv_head][width], slot = page * page_size + offset, with
+ * width head_dim for the K pool and head_dim_v for the V pool (the two differ
+ * for models whose K and V heads have different widths).
  * For each new token i: pool[loc[i], :, :] = new[i, :, :].
  * bf16 pool: the same bits. E4M3 pool: e4m3(float(new) * inv_scale), the
  * product taken in binary32 (one rounding), then rounded to E4M3FN. */
-void oracle_set_kv_buffer(int kv_dtype, void* k_pool, void* v_pool, int num_kv_heads, int head_dim,
-                          const int32_t* loc, const uint16_t* k_new, const uint16_t* v_new, int n_tokens,
-                          float k_inv_scale, float v_inv_scale) {
-  int64_t row = (int64_t)num_kv_heads * head_dim;
+static void scatter_rows(int kv_dtype, void* pool, int64_t row, const int32_t* loc, const uint16_t* src_rows,
+                         int n_tokens, float inv_scale) {
   for (int i = 0; i < n_tokens; ++i) {
     int64_t dst = (int64_t)loc[i] * row;
     int64_t src = (int64_t)i * row;
     for (int64_t e = 0; e < row; ++e) {
-      if (kv_dtype == ORACLE_KV_BF16) {
-        ((uint16_t*)k_pool)[dst + e] = k_new[src + e];
-        ((uint16_t*)v_pool)[dst + e] = v_new[src + e];
-      } else {
-        float kx = bf16_bits_to_float(k_new[src + e]) * k_inv_scale;
-        float vx = bf16_bits_to_float(v_new[src + e]) * v_inv_scale;
-        ((uint8_t*)k_pool)[dst + e] = oracle_e4m3_encode(kx);
-        ((uint8_t*)v_pool)[dst + e] = oracle_e4m3_encode(vx);
-      }
+      if (kv_dtype == ORACLE_KV_BF16)
+        ((uint16_t*)pool)[dst + e] = src_rows[src + e];
+      else
+        ((uint8_t*)pool)[dst + e] = oracle_e4m3_encode(bf16_bits_to_float(src_rows[src + e]) * inv_scale);
     }
   }
+}
+
+void oracle_set_kv_buffer(int kv_dtype, void* k_pool, void* v_pool, int num_kv_heads, int head_dim, int head_dim_v,
+                          const int32_t* loc, const uint16_t* k_new, const uint16_t* v_new, int n_tokens,
+                          float k_inv_scale, float v_inv_scale) {
+  scatter_rows(kv_dtype, k_pool, (int64_t)num_kv_heads * head_dim, loc, k_new, n_tokens, k_inv_scale);
+  scatter_rows(kv_dtype, v_pool, (int64_t)num_kv_heads * head_dim_v, loc, v_new, n_tokens, v_inv_scale);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -239,7 +246,7 @@ void oracle_lse_merge(int n_parts, int head_dim, const double* o_parts, const do
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
-  int bs, num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype;
+  int bs, num_q_heads, num_kv_heads, head_dim, head_dim_v, page_size, kv_dtype;
   const uint16_t* q;
   const void* k_pool;
   const void* v_pool;
@@ -253,7 +260,7 @@ typedef struct {
   int64_t n_rows; /* number of (token, q-head) rows to compute */
   const int32_t* row_token; /* NULL: every row in token-major order */
   const int32_t* row_head;
-  double* out_o; /* [n_rows][head_dim] */
+  double* out_o; /* [n_rows][head_dim_v] */
   double* out_lse; /* [n_rows] */
   int nthreads;
   int max_kv_len;
@@ -281,7 +288,8 @@ static int kv_len_of(const attn_job* j, int b) {
  * set in tree_mask[t]: drafts are ordered with every ancestor before its
  * descendants, so bits above the row's own index are ignored. At most 64 new
  * tokens per request. GQA: query head h reads KV head h / (num_q_heads /
- * num_kv_heads). With sinks, head h's sink logit joins the softmax as one
+ * num_kv_heads). Scores contract the head_dim columns of q and k; the output
+ * has the head_dim_v columns of v. With sinks, head h's sink logit joins the softmax as one
  * more score whose value vector is zero: it adds to the normaliser (and the
  * LSE) but not to o. */
 static int key_visible(const uint64_t* tree_mask, uint64_t word, int p, int prefix, int limit) {
@@ -291,7 +299,7 @@ static int key_visible(const uint64_t* tree_mask, uint64_t word, int p, int pref
 }
 
 static int attention_row(const attn_job* j, int t, int h, double* scores, double* qd, double* o, double* lse) {
-  int D = j->head_dim;
+  int D = j->head_dim, DV = j->head_dim_v;
   int b = 0;
   while (b < j->bs && j->qo_indptr[b + 1] <= t) ++b;
   if (b >= j->bs || t < j->qo_indptr[b]) return ORACLE_ERR_ARG;
@@ -308,7 +316,7 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
   int g = h / (j->num_q_heads / j->num_kv_heads);
   const uint16_t* qrow = j->q + ((int64_t)t * j->num_q_heads + h) * D;
   for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_decode(qrow[d]); /* the row's query, widened once */
-  for (int d = 0; d < D; ++d) o[d] = 0.0;
+  for (int d = 0; d < DV; ++d) o[d] = 0.0;
   double sink = j->sinks ? j->sinks[h] : -INFINITY;
   if (n_vis == 0) { /* no visible key: empty request (graph padding) or an empty mask row */
     *lse = sink; /* the sink alone (-inf without one); o stays zero */
@@ -336,8 +344,8 @@ static int attention_row(const attn_job* j, int t, int h, double* scores, double
     double w = exp(scores[p] - m) / z;
     int32_t page = j->kv_indices[j->kv_indptr[b] + p / j->page_size];
     int64_t slot = (int64_t)page * j->page_size + p % j->page_size;
-    int64_t base = (slot * j->num_kv_heads + g) * D;
-    for (int d = 0; d < D; ++d) o[d] += w * kv_value(j->v_pool, j->kv_dtype, base + d, j->v_scale);
+    int64_t base = (slot * j->num_kv_heads + g) * DV;
+    for (int d = 0; d < DV; ++d) o[d] += w * kv_value(j->v_pool, j->kv_dtype, base + d, j->v_scale);
   }
   *lse = m + log(z);
   return ORACLE_OK;
@@ -363,7 +371,7 @@ static void* attention_worker(void* arg) {
       t = (int)(r / j->num_q_heads);
       h = (int)(r % j->num_q_heads);
     }
-    int st = attention_row(j, t, h, scores, qd, j->out_o + r * j->head_dim, j->out_lse + r);
+    int st = attention_row(j, t, h, scores, qd, j->out_o + r * j->head_dim_v, j->out_lse + r);
     if (st != ORACLE_OK) w->status = st;
   }
   free(scores);
@@ -373,16 +381,18 @@ static void* attention_worker(void* arg) {
 
 /* Attention for the requested rows. With row_token == NULL every row of the
  * batch is computed (n_rows must equal qo_indptr[bs] * num_q_heads) and the
- * outputs are laid out [token][q_head][head_dim] / [token][q_head]. Rows are
+ * outputs are laid out [token][q_head][head_dim_v] / [token][q_head]. Rows are
  * independent; threads take them round-robin. tree_mask: NULL, or one word
  * per query token; sinks: NULL, or one logit per query head (see
  * attention_row). */
-int oracle_attention(int bs, int num_q_heads, int num_kv_heads, int head_dim, int page_size, int kv_dtype,
+int oracle_attention(int bs, int num_q_heads, int num_kv_heads, int head_dim, int head_dim_v, int page_size,
+                     int kv_dtype,
                      const uint16_t* q, const void* k_pool, const void* v_pool, const int32_t* kv_indptr,
                      const int32_t* kv_indices, const int32_t* kv_last_page_len, const int32_t* qo_indptr,
                      const uint64_t* tree_mask, const double* sinks, double sm_scale, double k_scale, double v_scale, int64_t n_rows, const int32_t* row_token,
                      const int32_t* row_head, double* out_o, double* out_lse, int nthreads) {
-  if (bs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || page_size <= 0)
+  if (bs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || head_dim_v <= 0 ||
+      page_size <= 0)
     return ORACLE_ERR_ARG;
   if (kv_dtype != ORACLE_KV_BF16 && kv_dtype != ORACLE_KV_FP8_E4M3) return ORACLE_ERR_ARG;
   if (nthreads < 1) nthreads = 1;
@@ -392,6 +402,7 @@ int oracle_attention(int bs, int num_q_heads, int num_kv_heads, int head_dim, in
   job.num_q_heads = num_q_heads;
   job.num_kv_heads = num_kv_heads;
   job.head_dim = head_dim;
+  job.head_dim_v = head_dim_v;
   job.page_size = page_size;
   job.kv_dtype = kv_dtype;
   job.q = q;

@@ -21,6 +21,9 @@ Recipe (seeds are ``torch.Generator`` seeds):
     via torch's float8_e4m3fn cast after dividing by ``max|x| / 448``).
   * seed 4: K then V of the step's new tokens, N(0, 1) bf16, ``[n_new, Hkv, D]``;
     they enter the pool only through ``set_kv_buffer`` at slots ``loc``.
+  * K and V heads may differ in width (``head_dim`` for Q and K, ``head_dim_v``
+    for V and the output); the draws are the same with each pool's own width.
+    The score scale is ``1 / sqrt(head_dim)``.
   * every slot that holds no prefix token (tails of last pages, pages no
     request owns, slots of new tokens before the scatter, the sentinel page)
     is filled with NaN (bf16 0x7FC0, E4M3 0x7F), so a read of an unused slot
@@ -71,6 +74,12 @@ class Workload:
     tree_mask: Optional[np.ndarray] = None
     # attention sinks: None, or fp32 [Hq], each query head's sink logit
     sinks: Optional[np.ndarray] = None
+    # width of the V heads (and of the output rows); 0 means head_dim
+    head_dim_v: int = 0
+
+    @property
+    def dv(self) -> int:
+        return self.head_dim_v or self.head_dim
 
     @property
     def num_slots(self) -> int:
@@ -144,8 +153,10 @@ def chain_tree_masks(qo_lens) -> np.ndarray:
 
 def make_workload(name: str, mode: str, bs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                   prefix_lens, qo_lens, page_size: int = 16, kv_dtype: str = "bf16",
-                  num_pages: Optional[int] = None, pool_slack: float = 0.10) -> Workload:
-    """Build a workload from explicit per-request prefix and new-token counts."""
+                  num_pages: Optional[int] = None, pool_slack: float = 0.10,
+                  head_dim_v: Optional[int] = None) -> Workload:
+    """Build a workload from explicit per-request prefix and new-token counts.
+    ``head_dim_v`` is the width of the V heads (default: ``head_dim``)."""
     prefix = np.asarray(prefix_lens, dtype=np.int64).reshape(bs)
     qo = np.asarray(qo_lens, dtype=np.int64).reshape(bs)
     seq = prefix + qo
@@ -189,18 +200,19 @@ def make_workload(name: str, mode: str, bs: int, num_q_heads: int, num_kv_heads:
     pools = []
     scales = []
     idx = torch.from_numpy(prefix_slots)
-    for seed in (2, 3):
+    dv = head_dim if head_dim_v is None else int(head_dim_v)
+    for seed, width in ((2, head_dim), (3, dv)):
         g = torch.Generator().manual_seed(seed)
-        data = torch.randn((n_prefix, num_kv_heads, head_dim), generator=g, dtype=torch.float32)
+        data = torch.randn((n_prefix, num_kv_heads, width), generator=g, dtype=torch.float32)
         if fp8:
             amax = float(data.abs().max()) if n_prefix else 1.0
             scale = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
-            pool = torch.full((num_slots, num_kv_heads, head_dim), E4M3_NAN, dtype=torch.uint8)
+            pool = torch.full((num_slots, num_kv_heads, width), E4M3_NAN, dtype=torch.uint8)
             codes = (data / scale).to(torch.float8_e4m3fn).view(torch.uint8)
             pool[idx] = codes
         else:
             scale = 1.0
-            pool = torch.full((num_slots, num_kv_heads, head_dim), BF16_NAN, dtype=torch.int16)
+            pool = torch.full((num_slots, num_kv_heads, width), BF16_NAN, dtype=torch.int16)
             pool = pool.view(torch.bfloat16)
             pool[idx] = data.to(torch.bfloat16)
         del data
@@ -210,14 +222,14 @@ def make_workload(name: str, mode: str, bs: int, num_q_heads: int, num_kv_heads:
     g4 = torch.Generator().manual_seed(4)
     n_new = loc.shape[0]
     k_new = _randn_bf16(g4, (n_new, num_kv_heads, head_dim))
-    v_new = _randn_bf16(g4, (n_new, num_kv_heads, head_dim))
+    v_new = _randn_bf16(g4, (n_new, num_kv_heads, dv))
 
     return Workload(name=name, mode=mode, bs=bs, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                     head_dim=head_dim, page_size=page_size, kv_dtype=kv_dtype, num_pages=num_pages,
                     prefix_lens=prefix.astype(np.int32), qo_lens=qo.astype(np.int32), seq_lens=seq.astype(np.int32),
                     page_table=page_table, loc=loc.astype(np.int32), q=q, k_pool=pools[0], v_pool=pools[1],
                     k_new=k_new, v_new=v_new, k_scale=scales[0], v_scale=scales[1],
-                    sm_scale=1.0 / math.sqrt(head_dim))
+                    sm_scale=1.0 / math.sqrt(head_dim), head_dim_v=0 if dv == head_dim else dv)
 
 
 def _randint(gen, lo, hi, n):
@@ -237,13 +249,19 @@ VARIANTS = ("prefix_extend_fp8",)
 
 
 def preset(name: str, bs: Optional[int] = None, len_scale: float = 1.0, page_size: int = 16,
-           kv_dtype: Optional[str] = None) -> Workload:
+           kv_dtype: Optional[str] = None, head_dims: Optional[tuple] = None) -> Workload:
     """The five cases at full size (defaults), or with fewer requests / shorter
     lengths (``len_scale`` multiplies every length bound) for quick parity runs.
     ``page_size`` and ``kv_dtype`` override the case's page size (16) and pool
-    element type; the lengths, pages and values are drawn the same way."""
+    element type; ``head_dims = (head_dim, head_dim_v)`` the widths of the Q/K
+    and V heads (192/128 is the shape of models whose K and V heads differ);
+    the lengths, pages and values are drawn the same way."""
     g = torch.Generator().manual_seed(0)
     ps = page_size
+    dk_over, dv_over = head_dims if head_dims is not None else (None, None)
+
+    def make(nm, mode, n, hq, hkv, d, P, N, **kw):
+        return make_workload(nm, mode, n, hq, hkv, dk_over or d, P, N, head_dim_v=dv_over, **kw)
 
     def kvd(default):
         return kv_dtype if kv_dtype is not None else default
@@ -260,27 +278,25 @@ def preset(name: str, bs: Optional[int] = None, len_scale: float = 1.0, page_siz
             L = L[:bs]
         n = L.shape[0]
         # a 128-page pool of 16-token pages (2,048 slots), the same slots at other page sizes
-        return make_workload(name, "decode", n, 8, 2, 64, L - 1, np.ones(n), page_size=ps,
-                             num_pages=max(128 * 16 // ps, 1 + int(((L + ps - 1) // ps).sum())),
-                             kv_dtype=kvd("bf16"))
+        return make(name, "decode", n, 8, 2, 64, L - 1, np.ones(n), page_size=ps,
+                    num_pages=max(128 * 16 // ps, 1 + int(((L + ps - 1) // ps).sum())), kv_dtype=kvd("bf16"))
     if name == "llama3_8b_decode":
         n = 64 if bs is None else bs
         L = lens(1024, 8192, n)
-        return make_workload(name, "decode", n, 32, 8, 128, L - 1, np.ones(n), page_size=ps, kv_dtype=kvd("bf16"))
+        return make(name, "decode", n, 32, 8, 128, L - 1, np.ones(n), page_size=ps, kv_dtype=kvd("bf16"))
     if name in ("prefix_extend", "prefix_extend_fp8"):
         n = 8 if bs is None else bs
         P = _randint(g, 0, int(round(4096 * len_scale)), n)
         N = lens(128, 2048, n)
         dt = kvd("fp8_e4m3" if name == "prefix_extend_fp8" else "bf16")
-        return make_workload(name, "extend", n, 32, 8, 128, P, N, page_size=ps, kv_dtype=dt)
+        return make(name, "extend", n, 32, 8, 128, P, N, page_size=ps, kv_dtype=dt)
     if name == "spec_verify":
         n = 32 if bs is None else bs
         ctx = lens(2048, 16384, n)
         N = _randint(g, 4, 8, n)
-        return make_workload(name, "verify", n, 64, 4, 128, ctx, N, page_size=ps, kv_dtype=kvd("bf16"))
+        return make(name, "verify", n, 64, 4, 128, ctx, N, page_size=ps, kv_dtype=kvd("bf16"))
     if name == "long_fp8_decode":
         n = 8 if bs is None else bs
         L = lens(32768, 131072, n)
-        return make_workload(name, "decode", n, 32, 8, 128, L - 1, np.ones(n), page_size=ps,
-                             kv_dtype=kvd("fp8_e4m3"))
+        return make(name, "decode", n, 32, 8, 128, L - 1, np.ones(n), page_size=ps, kv_dtype=kvd("fp8_e4m3"))
     raise KeyError(name)

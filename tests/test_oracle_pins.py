@@ -32,7 +32,7 @@ def _golden(name):
     return out
 
 
-def _tiny(mode="extend", kv_dtype="bf16", page_size=4, seed_shift=0, hq=4, hkv=2, d=8):
+def _tiny(mode="extend", kv_dtype="bf16", page_size=4, seed_shift=0, hq=4, hkv=2, d=8, dv=None):
     rng = np.random.default_rng(7 + seed_shift)
     bs = 3
     if mode == "decode":
@@ -41,7 +41,8 @@ def _tiny(mode="extend", kv_dtype="bf16", page_size=4, seed_shift=0, hq=4, hkv=2
     else:
         prefix = rng.integers(0, 30, bs)
         qo = rng.integers(1, 10, bs)
-    return make_workload("tiny", mode, bs, hq, hkv, d, prefix, qo, page_size=page_size, kv_dtype=kv_dtype)
+    return make_workload("tiny", mode, bs, hq, hkv, d, prefix, qo, page_size=page_size, kv_dtype=kv_dtype,
+                         head_dim_v=dv)
 
 
 def _contiguous_kv(W: Workload):
@@ -77,7 +78,7 @@ def _contiguous_kv(W: Workload):
                     vs.append(dec_new(vn[i]))
         new_off += L - P
         out.append((np.array(ks).reshape(L, W.num_kv_heads, W.head_dim),
-                    np.array(vs).reshape(L, W.num_kv_heads, W.head_dim)))
+                    np.array(vs).reshape(L, W.num_kv_heads, W.dv)))
     return out
 
 
@@ -88,8 +89,11 @@ def _q64(W):
 # ---------------------------------------------------------------- P1 brute force
 @pytest.mark.parametrize("mode", ["decode", "extend"])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
-def test_p1_bruteforce_unpaged_loops(mode, kv_dtype):
-    W = _tiny(mode, kv_dtype)
+@pytest.mark.parametrize("dv", [None, 5, 12])
+def test_p1_bruteforce_unpaged_loops(mode, kv_dtype, dv):
+    """dv: V heads of another width than the Q/K heads (P15; the scores
+    contract head_dim columns, the output has dv)."""
+    W = _tiny(mode, kv_dtype, dv=dv)
     o, lse = oracle_reference(W)
     q = _q64(W)
     G = W.num_q_heads // W.num_kv_heads
@@ -108,15 +112,19 @@ def test_p1_bruteforce_unpaged_loops(mode, kv_dtype):
                 m = max(s)
                 e = [math.exp(x - m) for x in s]
                 z = sum(e)
-                ref_o = [sum(e[j] * V[j, g, d] for j in range(vis)) / z for d in range(W.head_dim)]
+                ref_o = [sum(e[j] * V[j, g, d] for j in range(vis)) / z for d in range(W.dv)]
                 ref_lse = m + math.log(z)
                 worst = max(worst, max(abs(a - r) for a, r in zip(o[t, h], ref_o)), abs(lse[t, h] - ref_lse))
+    assert o.shape[-1] == W.dv
     assert worst < 1e-12
 
 
 @pytest.mark.parametrize("mode", ["decode", "extend"])
-def test_p1_bruteforce_torch_sdpa_fp64(mode):
-    W = _tiny(mode, "bf16", seed_shift=3, hq=6, hkv=2)
+@pytest.mark.parametrize("dv", [None, 6])
+def test_p1_bruteforce_torch_sdpa_fp64(mode, dv):
+    """dv: V heads narrower than the Q/K heads (P15); torch's SDPA takes a
+    value width of its own."""
+    W = _tiny(mode, "bf16", seed_shift=3, hq=6, hkv=2, d=10 if dv else 8, dv=dv)
     o, lse = oracle_reference(W)
     q = torch.from_numpy(_q64(W))
     G = W.num_q_heads // W.num_kv_heads
@@ -292,6 +300,66 @@ def test_p14_sinks_empty_request():
     W.sinks = random_sinks(4, seed=5)
     o, lse = oracle_reference(W)
     assert np.all(o[0] == 0.0) and np.allclose(lse[0], W.sinks.astype(np.float64), rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------- P15 K and V heads of different widths
+def _pad_k_columns(W: Workload, extra: int) -> Workload:
+    """The same workload with `extra` zero columns appended to every Q and K
+    head (K pool and new K), V untouched: each score gains only 0 * 0 terms."""
+    import copy
+    W2 = copy.copy(W)
+    pad = lambda t: torch.cat([t, torch.zeros(*t.shape[:-1], extra, dtype=t.dtype)], dim=-1)
+    W2.q = pad(W.q)
+    W2.k_pool = pad(W.k_pool)
+    W2.k_new = pad(W.k_new)
+    W2.head_dim = W.head_dim + extra
+    W2.head_dim_v = W.dv
+    return W2
+
+
+@pytest.mark.parametrize("mode", ["decode", "extend"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_p15_zero_k_columns_reproduce_equal_widths(mode, kv_dtype):
+    """Widening Q and K with zero columns (8 -> 12 while V stays 8) leaves
+    every score, hence every output and LSE, bit-identical; the score scale is
+    kept, as it is an input."""
+    W = _tiny(mode, kv_dtype, seed_shift=12)
+    o0, l0 = oracle_reference(W)
+    W2 = _pad_k_columns(W, 4)
+    assert W2.head_dim == 12 and W2.dv == 8
+    o1, l1 = oracle_reference(W2)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def test_p15_uniform_scores_mean_of_the_narrower_v():
+    """q = 0 with K 12 wide and V 5 wide: o is the mean of the visible V rows
+    (5 columns) and lse = ln(n)."""
+    W = _tiny("extend", "bf16", seed_shift=13, d=12, dv=5)
+    W.q = torch.zeros_like(W.q)
+    o, lse = oracle_reference(W)
+    assert o.shape == (W.total_q, W.num_q_heads, 5)
+    G = W.num_q_heads // W.num_kv_heads
+    qo_indptr = np.concatenate([[0], np.cumsum(W.qo_lens)])
+    for b, (K, V) in enumerate(_contiguous_kv(W)):
+        L, N = int(W.seq_lens[b]), int(W.qo_lens[b])
+        for i in range(N):
+            n = L - N + i + 1
+            for h in range(W.num_q_heads):
+                assert np.allclose(o[qo_indptr[b] + i, h], V[:n, h // G].mean(axis=0), atol=1e-13, rtol=0)
+                assert abs(lse[qo_indptr[b] + i, h] - math.log(n)) < 1e-13
+
+
+def test_p15_set_kv_buffer_each_pool_its_own_width():
+    """K rows land in the 12-wide K pool and V rows in the 5-wide V pool, bit
+    for bit, and nothing else of either pool changes."""
+    W = _tiny("extend", "bf16", seed_shift=14, d=12, dv=5)
+    kp, vp = oracle_pools(W)
+    k0, v0 = pool_bits(W.k_pool), pool_bits(W.v_pool)
+    kn, vn = bf16_bits(W.k_new), bf16_bits(W.v_new)
+    assert kp.shape[-1] == 12 and vp.shape[-1] == 5
+    assert np.array_equal(kp[W.loc], kn) and np.array_equal(vp[W.loc], vn)
+    rest = np.setdiff1d(np.arange(kp.shape[0]), W.loc)
+    assert np.array_equal(kp[rest], k0[rest]) and np.array_equal(vp[rest], v0[rest])
 
 
 # ---------------------------------------------------------------- P2 / P3 layout invariance
