@@ -70,18 +70,19 @@ def work_of(W):
     """Algorithmic work of one forward over workload W.
 
     bytes: K and V of every visible key of every (request, KV head) once, plus
-    Q in, O out, LSE out, page indices. flops: 4 * D per (query row, visible
-    key) pair (QK^T and PV multiply-adds)."""
+    Q in, O out, LSE out, page indices. flops: 2 * (D + Dv) per (query row,
+    visible key) pair (QK^T over the K width and PV over the V width, as
+    multiply-adds); D = Dv = head_dim unless K and V heads differ in width."""
     esz = 1 if W.is_fp8 else 2
     L = W.seq_lens.astype(np.int64)
-    kv_bytes = int(L.sum()) * W.num_kv_heads * W.head_dim * esz * 2
+    kv_bytes = int(L.sum()) * W.num_kv_heads * (W.head_dim + W.dv) * esz
     T = W.total_q
-    io_bytes = T * W.num_q_heads * W.head_dim * 2 * 2 + T * W.num_q_heads * 4
+    io_bytes = T * W.num_q_heads * (W.head_dim + W.dv) * 2 + T * W.num_q_heads * 4
     idx_bytes = int(((L + W.page_size - 1) // W.page_size).sum()) * 4
     N = W.qo_lens.astype(np.int64)
     P = L - N
     pairs = int((N * P + N * (N + 1) // 2).sum())  # visible (row, key) pairs per q-head
-    flops = 4 * W.head_dim * W.num_q_heads * pairs
+    flops = 2 * (W.head_dim + W.dv) * W.num_q_heads * pairs
     return dict(kv_bytes=kv_bytes, bytes=kv_bytes + io_bytes + idx_bytes, flops=flops, pairs=pairs)
 
 
@@ -202,14 +203,14 @@ def oracle_sample(W, budget_s=15.0):
             done_tok += t_hi - t_lo
             reqs.add(b)
             if t_hi == q1:
-                done_kv += L * W.num_kv_heads * W.head_dim * esz * 2
+                done_kv += L * W.num_kv_heads * (W.head_dim + W.dv) * esz
             if time.perf_counter() - t0 > budget_s:
                 break
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
     if W.mode == "extend":
-        val, unit = 4 * W.head_dim * W.num_q_heads * done_pairs / dt / 1e12, "TFLOP/s"
+        val, unit = 2 * (W.head_dim + W.dv) * W.num_q_heads * done_pairs / dt / 1e12, "TFLOP/s"
         what = f"{done_tok} of {W.total_q} query tokens in {len(reqs)} of {W.bs} requests"
     else:
         val, unit = done_kv / dt / 1e9, "GB/s"
@@ -221,7 +222,7 @@ def oracle_sample(W, budget_s=15.0):
 def config_of(W, spec_mode, world):
     """The workload as the JSON line names it (both arms print the same keys)."""
     return {"workload": W.name, "batch": W.bs, "num_q_heads": W.num_q_heads, "num_kv_heads": W.num_kv_heads,
-            "head_dim": W.head_dim, "page_size": W.page_size, "kv_dtype": W.kv_dtype, "mode": W.mode,
+            "head_dim": W.head_dim, "head_dim_v": W.dv, "page_size": W.page_size, "kv_dtype": W.kv_dtype, "mode": W.mode,
             "spec_mode": spec_mode, "total_kv_tokens": int(W.seq_lens.sum()), "total_q_rows": W.total_q,
             "l2": "inputs larger than L2 (K+V pools "
                   f"{2 * W.k_pool.numel() * W.k_pool.element_size() / 1e9:.2f} GB)",
@@ -338,13 +339,13 @@ def timed_steps(d, spec, steps, world):
     return step_s, fwd_s
 
 
-def secondary(name, spec_name, local, steps, world, cpu_budget, page_size=16):
+def secondary(name, spec_name, local, steps, world, cpu_budget, page_size=16, head_dims=None):
     """Short measurement of another workload (no e2e), with the oracle timed
     beside it on a bounded sample (rank 0 of a single-GPU run only)."""
     from paged_kv_cache_15_gb300 import binding as B
     from paged_kv_cache_15_gb300.runner import DeviceBatch
     from paged_kv_cache_15_gb300.workloads import preset
-    W = preset(name, page_size=page_size)
+    W = preset(name, page_size=page_size, head_dims=head_dims)
     spec = B.PKV_SPEC_DECODE if spec_name == "decode" else B.PKV_SPEC_PREFILL
     d = DeviceBatch(W, device=f"cuda:{local}")
 
@@ -367,7 +368,7 @@ def secondary(name, spec_name, local, steps, world, cpu_budget, page_size=16):
            "roofline_frac": roof["frac"], "achieved": roof["achieved"], "achieved_unit": roof["unit"],
            "kernel": roof["kernel"], "path": spec_name if W.mode == "verify" else
            ("decode" if W.mode == "decode" else "extend"),
-           "steps": steps, "page_size": W.page_size, "cpu_baseline": None}
+           "steps": steps, "page_size": W.page_size, "head_dims": [W.head_dim, W.dv], "cpu_baseline": None}
     del d
     torch.cuda.empty_cache()
     if world == 1 and cpu_budget > 0:
@@ -449,17 +450,23 @@ def run_ours(args, W, rank, world, local):
     # --- the other named workloads of the metric, short runs
     others = {}
     if not args.no_secondary:
-        for name, sp, ps in (("tiny_decode", "prefill", 16), ("prefix_extend", "prefill", 16),
-                             ("prefix_extend_fp8", "prefill", 16), ("spec_verify", "decode", 16),
-                             ("spec_verify", "prefill", 16), ("long_fp8_decode", "prefill", 16),
-                             ("llama3_8b_decode", "prefill", 128)):
-            if name == W.name and sp == args.spec_mode and ps == W.page_size:
+        # (workload, speculative attention mode, page size, head widths)
+        for name, sp, ps, hd in (("tiny_decode", "prefill", 16, None), ("prefix_extend", "prefill", 16, None),
+                                 ("prefix_extend_fp8", "prefill", 16, None), ("spec_verify", "decode", 16, None),
+                                 ("spec_verify", "prefill", 16, None), ("long_fp8_decode", "prefill", 16, None),
+                                 ("llama3_8b_decode", "prefill", 128, None),
+                                 ("llama3_8b_decode", "prefill", 16, (192, 128)),
+                                 ("prefix_extend", "prefill", 16, (192, 128))):
+            if name == W.name and sp == args.spec_mode and ps == W.page_size and hd is None and W.dv == W.head_dim:
                 continue
             key = name if name != "spec_verify" else f"spec_verify/{sp}_path"
             if ps != 16:
                 key += f"/page_size_{ps}"
+            if hd is not None:
+                key += f"/head_dims_{hd[0]}_{hd[1]}"
             others[key] = secondary(name, sp, local, args.secondary_steps, world,
-                                    0.0 if args.no_cpu_baseline else args.secondary_cpu_budget, page_size=ps)
+                                    0.0 if args.no_cpu_baseline else args.secondary_cpu_budget, page_size=ps,
+                                    head_dims=hd)
 
     if rank != 0:
         return
@@ -499,6 +506,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--spec-mode", default="prefill", choices=["prefill", "decode"])
     ap.add_argument("--page-size", type=int, default=16, choices=[16, 128])
+    ap.add_argument("--head-dims", type=int, nargs=2, default=None, metavar=("DK", "DV"),
+                    help="widths of the Q/K and V heads (default: the workload's own)")
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
@@ -509,7 +518,8 @@ def main():
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     from paged_kv_cache_15_gb300.workloads import preset
-    W = preset(args.workload, page_size=args.page_size)
+    W = preset(args.workload, page_size=args.page_size,
+               head_dims=tuple(args.head_dims) if args.head_dims else None)
     if args.impl == "reference":
         run_reference(args, W, rank, world)
     else:

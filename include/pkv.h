@@ -28,12 +28,14 @@
  *   forward calls read lengths only on the device, so a sequence of them can be
  *   captured into a CUDA graph and replayed with new lengths of the same batch
  *   size.
- * - KV pool layout ("NHD"): one pool for K and one for V per layer, each
- *   [num_pages * page_size slots][num_kv_heads][head_dim], row-major, with
- *   slot = page * page_size + offset. Elements are bf16, or FP8 E4M3FN bytes
+ * - KV pool layout ("NHD"): one pool for K and one for V per layer,
+ *   [num_pages * page_size slots][num_kv_heads][width], row-major, with
+ *   slot = page * page_size + offset; the width is head_dim for K and
+ *   head_dim_v for V (pkv_config). Elements are bf16, or FP8 E4M3FN bytes
  *   with one fp32 scale per pool (value = code * scale).
- * - Queries and outputs are bf16 [tokens][num_q_heads][head_dim]; LSE is fp32
- *   [tokens][num_q_heads], the natural log of sum_j exp(sm_scale * q . k_j).
+ * - Queries are bf16 [tokens][num_q_heads][head_dim], outputs bf16
+ *   [tokens][num_q_heads][head_dim_v]; LSE is fp32 [tokens][num_q_heads], the
+ *   natural log of sum_j exp(sm_scale * q . k_j).
  *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
  * - Request b has seq_lens[b] = L_b KV tokens (prefix plus this step's new
  *   tokens, whose K/V pkv_set_kv_buffer has already stored) and qo_len_b query
@@ -94,13 +96,16 @@ typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
 /* ---- configuration --------------------------------------------------------
  * Fixed for the life of a context; every capacity bounds a fixed-size
  * metadata buffer in the workspace, so captured graphs can be replayed.
- * Supported: head_dim 64 or 128; page_size 16 or 128 (the 16-token page of
- * the configs the library is tuned on, and the 128-token page that
- * "--attention-backend", section "The obvious fix, and why it fails", names
- * as fa4's native page size); num_q_heads a multiple of num_kv_heads with a
- * group size num_q_heads / num_kv_heads of at most 16; E4M3 (FP8) pools with
- * head_dim 128 on both paths (head_dim 64 with an E4M3 pool returns
- * PKV_ERR_UNSUPPORTED). */
+ * Supported: head_dim 64 or 128 with V heads of the same width, or Q/K heads
+ * of 192 with V heads of 128 (head_dim 192, head_dim_v 128: models whose K and
+ * V heads differ in width, which "--attention-backend", section "How SGLang
+ * picks a default", routes to fa4 on SM100/SM103); page_size 16 or 128 (the
+ * 16-token page of the configs the library is tuned on, and the 128-token page
+ * that the same page, section "The obvious fix, and why it fails", names as
+ * fa4's native page size); num_q_heads a multiple of num_kv_heads with a group
+ * size num_q_heads / num_kv_heads of at most 16; E4M3 (FP8) pools with head_dim
+ * 128 (and V heads of 128) on both paths (other widths with an E4M3 pool
+ * return PKV_ERR_UNSUPPORTED). */
 typedef struct {
   int32_t num_q_heads;
   int32_t num_kv_heads;
@@ -112,6 +117,7 @@ typedef struct {
   int32_t max_pages_total; /* max sum over requests of ceil(seq_len / page_size) */
   int32_t max_q_tokens;    /* max sum over requests of qo_len */
   int32_t max_qo_len;      /* max qo_len of one request on the decode path (verify drafts); 1 for plain decode */
+  int32_t head_dim_v;      /* width of the V heads and of the output rows; 0 means head_dim */
 } pkv_config;
 
 typedef struct pkv_ctx pkv_ctx;
@@ -123,8 +129,9 @@ const char* pkv_status_string(int status);
  * Errors: INVALID_ARG (null), UNSUPPORTED (shape outside the supported set). */
 int pkv_workspace_bytes(const pkv_config* cfg, size_t* bytes_out);
 
-/* Bytes of ONE pool (K or V) of one layer: num_pages * page_size * num_kv_heads
- * * head_dim * element size. */
+/* Bytes of the K pool of one layer: num_pages * page_size * num_kv_heads *
+ * head_dim * element size. The V pool takes the same with head_dim_v in place
+ * of head_dim (the same bytes when the widths are equal). */
 int pkv_pool_bytes(const pkv_config* cfg, size_t* bytes_out);
 
 /* Create a context over caller-owned device workspace (256-byte aligned, at
@@ -171,7 +178,8 @@ int pkv_get_metadata(pkv_ctx* ctx, const int32_t** kv_indptr, const int32_t** kv
 
 /* save_kv_cache: store this step's new K/V rows into the pools,
  *   pool[d_loc[i], h, :] = new[i, h, :]   for i < n_tokens, every KV head h.
- * d_k, d_v: bf16 [n_tokens][num_kv_heads][head_dim]; d_loc: int32 slots.
+ * d_k: bf16 [n_tokens][num_kv_heads][head_dim], d_v: bf16
+ * [n_tokens][num_kv_heads][head_dim_v]; d_loc: int32 slots.
  * bf16 pools receive the same bits; E4M3 pools receive
  * e4m3_rn_satfinite(float(x) * inv_scale) (one fp32 multiply, round to nearest
  * even, finite values beyond +-448 saturate). Slots outside the pool are
@@ -185,8 +193,9 @@ int pkv_set_kv_buffer(pkv_ctx* ctx, void* d_k_pool, void* d_v_pool, const int32_
  * (request, KV head) range is cut into chunks processed in parallel and merged
  * by their log-sum-exp. Handles qo_len up to config.max_qo_len per request
  * (target-verify on the decode path) with the causal rule above.
- * d_q: bf16 [T][num_q_heads][head_dim] (T = sum of qo_len), d_out: bf16 of the
- * same shape, d_lse: fp32 [T][num_q_heads] or NULL. k_scale / v_scale multiply
+ * d_q: bf16 [T][num_q_heads][head_dim] (T = sum of qo_len), d_out: bf16
+ * [T][num_q_heads][head_dim_v] (scores contract head_dim columns, the output
+ * has the V heads' width), d_lse: fp32 [T][num_q_heads] or NULL. k_scale / v_scale multiply
  * E4M3 codes (ignored for bf16 pools). Pointers must be 16-byte aligned.
  * sm_scale must be positive and finite, and so must k_scale and v_scale with
  * an E4M3 pool (INVALID_ARG otherwise). Verify batches follow the draft-tree

@@ -42,7 +42,7 @@ class PkvError(RuntimeError):
 class pkv_config(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "num_q_heads", "num_kv_heads", "head_dim", "page_size", "kv_dtype", "num_pages", "max_batch",
-        "max_pages_total", "max_q_tokens", "max_qo_len")]
+        "max_pages_total", "max_q_tokens", "max_qo_len", "head_dim_v")]
 
 
 _lock = threading.Lock()
@@ -121,9 +121,9 @@ def pkv_status_string(status: int) -> str:
 
 
 def make_config(num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype, num_pages, max_batch, max_pages_total,
-                max_q_tokens, max_qo_len=1) -> pkv_config:
+                max_q_tokens, max_qo_len=1, head_dim_v=0) -> pkv_config:
     return pkv_config(num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype, num_pages, max_batch,
-                      max_pages_total, max_q_tokens, max_qo_len)
+                      max_pages_total, max_q_tokens, max_qo_len, head_dim_v)
 
 
 def pkv_workspace_bytes(cfg: pkv_config) -> int:

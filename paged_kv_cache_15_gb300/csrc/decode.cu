@@ -49,9 +49,12 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D_, bool FP8_, int WK_, int KPW_, int STAGES_, int RT_>
+// DK: width of the Q and K heads; DV: of the V heads and output rows (equal
+// except for models whose K and V heads differ, 192 / 128).
+template <int DK_, int DV_, bool FP8_, int WK_, int KPW_, int STAGES_, int RT_>
 struct DecodeCfg {
-  static constexpr int D = D_;
+  static constexpr int DK = DK_;
+  static constexpr int DV = DV_;
   static constexpr bool FP8 = FP8_;
   // key-major tile: keys along the MMA's M, RT tiles of 8 query rows along N
   static constexpr int RT = RT_;
@@ -66,25 +69,28 @@ struct DecodeCfg {
   static constexpr int kStageKeys = WK * KPW;
   static constexpr int kStagePages = kStageKeys / kSegSlots;
   static constexpr int kElem = FP8 ? 1 : 2;
-  static constexpr int kRowBytes = D * kElem;
-  static constexpr int kColBlocks = kRowBytes / 128;
-  static constexpr int kTileBytes = kStageKeys * kRowBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kRowBytesK = DK * kElem;
+  static constexpr int kRowBytesV = DV * kElem;
+  static constexpr int kColBlocksK = kRowBytesK / 128;
+  static constexpr int kColBlocksV = kRowBytesV / 128;
+  static constexpr int kTileBytesK = kStageKeys * kRowBytesK;  // a stage: K tile, then V tile
+  static constexpr int kTileBytesV = kStageKeys * kRowBytesV;
+  static constexpr int kStageBytes = kTileBytesK + kTileBytesV;
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kMlOffset = kBarOffset + 2 * STAGES * 8;
   static constexpr int kAbortOffset = kMlOffset + WK * 16 * 2 * 4;
   static constexpr int kUnitQOffset = kAbortOffset + 16;  // unit queue: 2 full + 2 empty barriers, 2 ids
   static constexpr int kSmemBytes = kUnitQOffset + 40 + 1024;  // + alignment slack
-  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
+  static_assert(kRowBytesK % 128 == 0 && kRowBytesV % 128 == 0, "rows must be whole 128-byte swizzle spans");
   static_assert(KPW % 16 == 0 && kStageKeys % kSegSlots == 0, "stage must hold whole pages");
-  static_assert(!(WK > 1) || (WK * 16 * D * 4 <= kStageBytes), "merge scratch must fit in one stage");
+  static_assert(!(WK > 1) || (WK * 16 * DV * 4 <= kStageBytes), "merge scratch must fit in one stage");
   static_assert(WK > 1 && RT >= 1 && RT <= 2, "key-major tiles: one or two 8-row tiles, key warps combined");
 };
 
 struct DecodeArgs {
   Meta m;
-  const uint16_t* q;  // bf16 [T][Hq][D]
-  uint16_t* out;      // bf16 [T][Hq][D]
+  const uint16_t* q;  // bf16 [T][Hq][DK]
+  uint16_t* out;      // bf16 [T][Hq][DV]
   float* lse;         // fp32 [T][Hq] or null
   int num_q_heads, num_kv_heads, group;
   float scale_log2;  // sm_scale * k_scale * log2(e)
@@ -192,7 +198,7 @@ template <class C, bool EXTRAS>
 __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                      const __grid_constant__ CUtensorMap tmap_v,
                                                                      DecodeArgs a) {
-  constexpr int D = C::D;
+  constexpr int DK = C::DK, DV = C::DV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
@@ -273,18 +279,19 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             break;
           }
           const int np = min(C::kStagePages, npages - st * C::kStagePages);
-          mbar_arrive_expect_tx(&full[slot], (uint32_t)(np * kSegSlots * C::kRowBytes * 2));
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(np * kSegSlots * (C::kRowBytesK + C::kRowBytesV)));
           uint8_t* kdst = smem + slot * C::kStageBytes;
-          uint8_t* vdst = kdst + C::kTileBytes;
+          uint8_t* vdst = kdst + C::kTileBytesK;
           for (int p = 0; p < np; ++p) {
             const int page = a.m.seg_indices[base + st * C::kStagePages + p];
 #pragma unroll
-            for (int cb = 0; cb < C::kColBlocks; ++cb) {
-              const int x = g * D + cb * (128 / C::kElem);
-              const int off = cb * C::kStageKeys * 128 + p * kSegSlots * 128;
-              tma_load_2d_hint(kdst + off, &tmap_k, x, page * kSegSlots, &full[slot], pol);
-              tma_load_2d_hint(vdst + off, &tmap_v, x, page * kSegSlots, &full[slot], pol);
-            }
+            for (int cb = 0; cb < C::kColBlocksK; ++cb)
+              tma_load_2d_hint(kdst + cb * C::kStageKeys * 128 + p * kSegSlots * 128, &tmap_k,
+                               g * DK + cb * (128 / C::kElem), page * kSegSlots, &full[slot], pol);
+#pragma unroll
+            for (int cb = 0; cb < C::kColBlocksV; ++cb)
+              tma_load_2d_hint(vdst + cb * C::kStageKeys * 128 + p * kSegSlots * 128, &tmap_v,
+                               g * DV + cb * (128 / C::kElem), page * kSegSlots, &full[slot], pol);
           }
           armed |= 1u << slot;
           armed_phase = (armed_phase & ~(1u << slot)) | (phase << slot);
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
       // are half those of a 16-row query tile. Lane (g8 = lane/4, t4 = lane%4)
       // holds rows 8j + 2*t4 + {0,1} of every row tile j.
       constexpr int RT = C::RT;
-      constexpr int MT = D / 16;  // 16-column m-tiles of O^T
+      constexpr int MT = DV / 16;  // 16-column m-tiles of O^T
       const int t4 = lane & 3, g8 = lane >> 2;
       const int prefix = L - qo;
       int lim[RT][2];
@@ -362,15 +369,15 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
       if (tree && qo > 64 && lane == 0 && wk == 0) record_error(plan, PKV_DEV_TREE_TOO_LONG, b);
 
       // Q^T fragments (B operand): column g8 of row tile j is query row 8j + g8
-      uint32_t qf[D / 16][RT][2];
+      uint32_t qf[DK / 16][RT][2];
 #pragma unroll
       for (int j = 0; j < RT; ++j) {
         const int rn = 8 * j + g8;
         const bool vn = rn < rows_valid;
-        const long long qrow = ((long long)(q0 + rn / G) * a.num_q_heads + g * G + rn % G) * D;
+        const long long qrow = ((long long)(q0 + rn / G) * a.num_q_heads + g * G + rn % G) * DK;
         if constexpr (!C::FP8) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < DK / 16; ++kk) {
             const int c0 = kk * 16 + 2 * t4;
             qf[kk][j][0] = vn ? *reinterpret_cast<const uint32_t*>(a.q + qrow + c0) : 0u;
             qf[kk][j][1] = vn ? *reinterpret_cast<const uint32_t*>(a.q + qrow + c0 + 8) : 0u;
@@ -380,7 +387,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           // k-step 2p  : slots {2t,2t+1} <- D 32p+8t+{0,1}, {2t+8,2t+9} <- D 32p+8t+{2,3}
           // k-step 2p+1: slots {2t,2t+1} <- D 32p+8t+{4,5}, {2t+8,2t+9} <- D 32p+8t+{6,7}
 #pragma unroll
-          for (int p = 0; p < D / 32; ++p) {
+          for (int p = 0; p < DK / 32; ++p) {
             const uint4 x = vn ? *reinterpret_cast<const uint4*>(a.q + qrow + p * 32 + 8 * t4) : make_uint4(0, 0, 0, 0);
             qf[2 * p][j][0] = pack_f16(bf16lo(x.x), bf16hi(x.x));
             qf[2 * p][j][1] = pack_f16(bf16lo(x.y), bf16hi(x.y));
@@ -410,18 +417,18 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           aborted = true;
         }
         const uint32_t kbase = smem_u32(smem + slot * C::kStageBytes);
-        const uint32_t vbase = kbase + C::kTileBytes;
+        const uint32_t vbase = kbase + C::kTileBytesK;
         const int stage_key0 = key_begin + st * C::kStageKeys;
         // last page of the request with a partial fill: zero the V rows past L
         const bool tail = (it.p1 == np_req) && (st == nst - 1) && (L % kSegSlots) != 0;
         if (tail) {
           const int r0 = L - stage_key0;
           const int r1 = min(C::kStagePages, npages - st * C::kStagePages) * kSegSlots;
-          uint8_t* vb8 = smem + slot * C::kStageBytes + C::kTileBytes;
-          const int n16 = (r1 - r0) * C::kColBlocks * 8;
+          uint8_t* vb8 = smem + slot * C::kStageBytes + C::kTileBytesK;
+          const int n16 = (r1 - r0) * C::kColBlocksV * 8;
           for (int i = cw * 32 + lane; i < n16; i += C::kConsumerWarps * 32) {
-            const int row = r0 + i / (C::kColBlocks * 8);
-            const int rest = i % (C::kColBlocks * 8);
+            const int row = r0 + i / (C::kColBlocksV * 8);
+            const int rest = i % (C::kColBlocksV * 8);
             const int cb = rest / 8, ch = rest % 8;
             *reinterpret_cast<uint4*>(vb8 + cb * C::kStageKeys * 128 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
           }
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             if constexpr (!C::FP8) {
               const int key = kr0 + (lane & 15);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
+              for (int kk = 0; kk < DK / 16; ++kk) {
                 const int chunk = 2 * kk + (lane >> 4);
                 const uint32_t addr = kbase + (chunk >> 3) * (C::kStageKeys * 128) + swz(key, chunk & 7);
                 uint32_t ka[4];
@@ -452,7 +459,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
               }
             } else {
 #pragma unroll
-              for (int p = 0; p < D / 32; ++p) {
+              for (int p = 0; p < DK / 32; ++p) {
                 const int byte = p * 32 + 8 * t4;
                 uint32_t x0[2], x1[2];
 #pragma unroll
@@ -554,7 +561,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             } else {
               const int key = kr0 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-              for (int mp = 0; mp < D / 32; ++mp) {
+              for (int mp = 0; mp < DV / 32; ++mp) {
                 // 16-byte chunks 2mp (D 32mp..+15) and 2mp+1 (D 32mp+16..+31);
                 // r0: keys 0-7 / chunk 2mp, r1: keys 8-15 / chunk 2mp, r2, r3: chunk 2mp+1.
                 // bytes of r: V[2t][2g], V[2t][2g+1], V[2t+1][2g], V[2t+1][2g+1], so
@@ -605,11 +612,11 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
         const int i = r / G, h = g * G + r % G;
         const long long t = q0 + i;
         if (direct) {
-          orow = a.out + (t * a.num_q_heads + h) * D;
+          orow = a.out + (t * a.num_q_heads + h) * DV;
           lrow = a.lse ? a.lse + t * a.num_q_heads + h : nullptr;
         } else {
           const long long pr = (long long)a.m.partial_indptr[b] + (long long)split * qo + i;
-          orow = a.m.partial_o + (pr * a.num_q_heads + h) * D;
+          orow = a.m.partial_o + (pr * a.num_q_heads + h) * DV;
           lrow = a.m.partial_lse + pr * a.num_q_heads + h;
         }
       };
@@ -618,8 +625,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
       if (nst == 0) {
         // empty key range (padding request): zero output, -inf LSE
         if (wk == 0 && !skip) {
-          for (int idx = lane; idx < rows_valid * (D / 2); idx += 32) {
-            const int r = idx / (D / 2), c2 = idx % (D / 2);
+          for (int idx = lane; idx < rows_valid * (DV / 2); idx += 32) {
+            const int r = idx / (DV / 2), c2 = idx % (DV / 2);
             uint16_t* orow;
             float* lrow;
             out_row(r, orow, lrow);
@@ -630,8 +637,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
         }
       } else {
         named_bar_sync(1, C::kConsumerWarps * 32);  // everyone done reading the held stage
-        float* scr = reinterpret_cast<float*>(smem + slot * C::kStageBytes);  // [WK][16][D]
-        float* my = scr + wk * 16 * D;
+        float* scr = reinterpret_cast<float*>(smem + slot * C::kStageBytes);  // [WK][16][DV]
+        float* my = scr + wk * 16 * DV;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -641,7 +648,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int r = 8 * j + 2 * t4 + e;
-                my[r * D + (kcol(mt, hi) ^ kswz(r))] = o[mt][j][2 * hi + e];
+                my[r * DV + (kcol(mt, hi) ^ kswz(r))] = o[mt][j][2 * hi + e];
               }
         if (g8 == 0) {
 #pragma unroll
@@ -654,12 +661,12 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
             }
         }
         named_bar_sync(1, C::kConsumerWarps * 32);
-        // each consumer thread finishes float4 pieces of the rows x D tile
+        // each consumer thread finishes float4 pieces of the rows x DV tile
         const int nthr = C::kConsumerWarps * 32;
         const int ctid = cw * 32 + lane;
         const int nrows = skip ? 0 : min(rows_valid, C::kRows);
-        for (int idx = ctid; idx < nrows * (D / 4); idx += nthr) {
-          const int r = idx / (D / 4), c4 = idx % (D / 4);
+        for (int idx = ctid; idx < nrows * (DV / 4); idx += nthr) {
+          const int r = idx / (DV / 4), c4 = idx % (DV / 4);
           float mw[C::WK], lw[C::WK];
           float M = -INFINITY;
 #pragma unroll
@@ -678,7 +685,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < C::WK; ++k) {
-            const float4 x = *reinterpret_cast<const float4*>(scr + (k * 16 + r) * D + ((c4 * 4) ^ kswz(r)));
+            const float4 x = *reinterpret_cast<const float4*>(scr + (k * 16 + r) * DV + ((c4 * 4) ^ kswz(r)));
             acc.x += x.x * wgt[k];
             acc.y += x.y * wgt[k];
             acc.z += x.z * wgt[k];
@@ -743,13 +750,14 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
                float v_scale, void* out, float* lse, cudaStream_t st) {
   CUtensorMap tk, tv;
   const CUtensorMapDataType dt = C::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t inner = (uint64_t)c.cfg.num_kv_heads * C::D;
+  const uint64_t inner_k = (uint64_t)c.cfg.num_kv_heads * C::DK;
+  const uint64_t inner_v = (uint64_t)c.cfg.num_kv_heads * C::DV;
   const uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
   const uint32_t box_inner = 128 / C::kElem;
-  if (encode_tmap_2d(&tk, dt, const_cast<void*>(k_pool), inner, slots, inner * C::kElem, box_inner, kSegSlots,
+  if (encode_tmap_2d(&tk, dt, const_cast<void*>(k_pool), inner_k, slots, inner_k * C::kElem, box_inner, kSegSlots,
                      CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
-  if (encode_tmap_2d(&tv, dt, const_cast<void*>(v_pool), inner, slots, inner * C::kElem, box_inner, kSegSlots,
+  if (encode_tmap_2d(&tv, dt, const_cast<void*>(v_pool), inner_v, slots, inner_v * C::kElem, box_inner, kSegSlots,
                      CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
   DecodeArgs a;
@@ -774,13 +782,17 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
 }
 
 // Tile shapes: one or two 8-row key-major tiles per unit; four key warps
-// split each stage's keys.
-using DecBf16D128_1 = DecodeCfg<128, false, 4, 16, 3, 1>;
-using DecBf16D128_2 = DecodeCfg<128, false, 4, 16, 3, 2>;
-using DecBf16D64_1 = DecodeCfg<64, false, 4, 16, 4, 1>;
-using DecBf16D64_2 = DecodeCfg<64, false, 4, 16, 4, 2>;
-using DecFp8D128_1 = DecodeCfg<128, true, 4, 32, 3, 1>;
-using DecFp8D128_2 = DecodeCfg<128, true, 4, 32, 3, 2>;
+// split each stage's keys. With 192-wide K heads (bf16) a stage is 40 KB, so
+// two stages keep two CTAs on an SM.
+using DecBf16D128_1 = DecodeCfg<128, 128, false, 4, 16, 3, 1>;
+using DecBf16D128_2 = DecodeCfg<128, 128, false, 4, 16, 3, 2>;
+using DecBf16D64_1 = DecodeCfg<64, 64, false, 4, 16, 4, 1>;
+using DecBf16D64_2 = DecodeCfg<64, 64, false, 4, 16, 4, 2>;
+using DecFp8D128_1 = DecodeCfg<128, 128, true, 4, 32, 3, 1>;
+using DecFp8D128_2 = DecodeCfg<128, 128, true, 4, 32, 3, 2>;
+using DecBf16D192_1 = DecodeCfg<192, 128, false, 4, 16, 2, 1>;
+using DecBf16D192_2 = DecodeCfg<192, 128, false, 4, 16, 2, 2>;
+
 
 }  // namespace
 
@@ -823,6 +835,9 @@ int launch_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool,
   } else if (fp8 && D == 128) {
     if (rt1) PKV_RUN(DecFp8D128_1);
     PKV_RUN(DecFp8D128_2);
+  } else if (!fp8 && D == 192) {
+    if (rt1) PKV_RUN(DecBf16D192_1);
+    PKV_RUN(DecBf16D192_2);
   }
 #undef PKV_RUN
   return PKV_ERR_UNSUPPORTED;
@@ -847,7 +862,8 @@ int launch_split_merge(Ctx& c, void* out, float* lse, int max_rows_per_head, boo
   if (rows <= 0) return PKV_OK;
   const int word = extend_path ? kSplitExtend : kSplitDecode;
   cudaError_t e;
-  if (c.cfg.head_dim == 128)
+  // partial and output rows have the V heads' width
+  if (head_dim_v(c.cfg) == 128)
     e = launch_pdl(split_merge_kernel<128>, dim3((unsigned)grid), dim3(256), 0, st, a, max_rows_per_head, word,
                    extend_path ? 1 : 0);
   else

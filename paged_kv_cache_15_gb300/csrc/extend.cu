@@ -177,22 +177,27 @@ __device__ __forceinline__ UnitKV unit_kv(const ExtendTile& u) {
   return k;
 }
 
-template <int D_, int NK_, int NV_>
+// DK: width of the Q and K heads; DV: of the V heads and the output rows
+// (equal except for models whose K and V heads differ, 192 / 128).
+template <int DK_, int DV_, int NK_, int NV_>
 struct ExtCfg {
-  static constexpr int D = D_;
+  static constexpr int DK = DK_;
+  static constexpr int DV = DV_;
   static constexpr int NK = NK_;  // K ring depth
   static constexpr int NV = NV_;  // V ring depth
   static constexpr int kThreads = 352;
   static constexpr int kProducerWarp = 8;   // K tiles
   static constexpr int kMmaWarp = 9;
   static constexpr int kVProducerWarp = 10;  // V tiles
-  static constexpr int kColBlocks = D / 64;               // 128-byte swizzle spans per row
-  static constexpr int kQBytes = kExtendRows * D * 2;     // one Q tile: [cb][128 rows][128 B]
-  static constexpr int kTileBytes = kExtendKeys * D * 2;  // one K or V tile
+  static constexpr int kColBlocksK = DK / 64;                // 128-byte swizzle spans per Q or K row
+  static constexpr int kColBlocksV = DV / 64;                // per V row
+  static constexpr int kQBytes = kExtendRows * DK * 2;       // one Q tile: [cb][128 rows][128 B]
+  static constexpr int kTileBytesK = kExtendKeys * DK * 2;   // one K tile
+  static constexpr int kTileBytesV = kExtendKeys * DV * 2;   // one V tile
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kQBytes;
-  static constexpr int kVOff = kKOff + NK * kTileBytes;
-  static constexpr int kBarOff = kVOff + NV * kTileBytes;
+  static constexpr int kVOff = kKOff + NK * kTileBytesK;
+  static constexpr int kBarOff = kVOff + NV * kTileBytesV;
   static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6 + 4 + 2;
   static constexpr int kMergeOff = kBarOff + kNumBars * 8;           // dual units: tile B's (m, l) per row
   static constexpr int kTmemSlotOff = kMergeOff + 2 * kExtendRows * 4;
@@ -200,7 +205,7 @@ struct ExtCfg {
   static constexpr int kSmemBytes = kAbortOff + 8 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(D <= 128, "O needs at most 128 TMEM columns per tile");
+  static_assert(DV <= 128, "O needs at most 128 TMEM columns per tile");
 };
 
 struct ExtendArgs {
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
                                                                    const __grid_constant__ CUtensorMap tmap_v,
                                                                    const __grid_constant__ CUtensorMap tmap_q,
                                                                    ExtendArgs a) {
-  constexpr int D = C::D;
+  constexpr int DK = C::DK, DV = C::DV;
   constexpr int NK = C::NK, NV = C::NV;
   constexpr int kPagesPerTile = kExtendKeys / kSegSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     tc_fence_before();
   }
   // K/V stages start as zeros so rows of a partly loaded tile are finite
-  for (int i = tid; i < (NK + NV) * C::kTileBytes / 16; i += C::kThreads)
+  for (int i = tid; i < (NK * C::kTileBytesK + NV * C::kTileBytesV) / 16; i += C::kThreads)
     reinterpret_cast<uint4*>(smem + C::kKOff)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   __syncthreads();
@@ -335,6 +340,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     uint64_t* empty = is_v ? v_empty : k_empty;
     const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
     const int ring_off = is_v ? C::kVOff : C::kKOff;
+    const int width = is_v ? DV : DK;  // elements of a K or V row of one head
+    const int tile_bytes = is_v ? C::kTileBytesV : C::kTileBytesK;
     // the whole warp runs the loop; lane p loads the tile's p-th page index and
     // one elected lane issues the copies
     if (elect_one()) {
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
               mbar_arrive_expect_tx(&q_full[x], (uint32_t)C::kQBytes);
               const int tok = a.m.qo_indptr[u.b] + (u.row0 + x * kExtendRows) / G;
 #pragma unroll
-              for (int cb = 0; cb < C::kColBlocks; ++cb)
+              for (int cb = 0; cb < C::kColBlocksK; ++cb)
                 tma_load_3d(smem + C::kQOff + x * C::kQBytes + cb * (kExtendRows * 128), &tmap_q, cb * 64, g * G,
                             tok, &q_full[x]);
             }
@@ -417,15 +424,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           break;
         }
         const bool leader = elect_one();
-        if (leader) mbar_arrive_expect_tx(&full[st], (uint32_t)(npg * kSegSlots * D * 2));
-        uint8_t* dst = smem + ring_off + st * C::kTileBytes;
+        if (leader) mbar_arrive_expect_tx(&full[st], (uint32_t)(npg * kSegSlots * width * 2));
+        uint8_t* dst = smem + ring_off + st * tile_bytes;
 #pragma unroll
         for (int p = 0; p < kPagesPerTile; ++p) {
           const int pg = __shfl_sync(0xffffffffu, grp, ((e & 3) << 3) + p);
           if (p < npg && leader) {
-#pragma unroll
-            for (int cb = 0; cb < C::kColBlocks; ++cb)
-              tma_load_2d_hint(dst + cb * (kExtendKeys * 128) + p * (kSegSlots * 128), tmap, g * D + cb * 64,
+            for (int cb = 0; cb < width / 64; ++cb)
+              tma_load_2d_hint(dst + cb * (kExtendKeys * 128) + p * (kSegSlots * 128), tmap, g * width + cb * 64,
                                pg * kSegSlots, &full[st], pol);
           }
         }
@@ -448,7 +454,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     // instruction. Descriptors: the start-address field is the low bits, so a
     // byte offset b inside the tile adds b >> 4.
     constexpr uint32_t idesc_qk = umma_idesc_bf16(kExtendRows, kExtendKeys, false, false);
-    constexpr uint32_t idesc_pv = umma_idesc_bf16(kExtendRows, D, false, true);
+    constexpr uint32_t idesc_pv = umma_idesc_bf16(kExtendRows, DV, false, true);
     const uint64_t q_desc0 = umma_desc_sw128(smem_base + C::kQOff, 16, 1024);
     const uint64_t k_desc0 = umma_desc_sw128(smem_base + C::kKOff, 16, 1024);
     const uint64_t v_desc0 = umma_desc_sw128(smem_base + C::kVOff, kExtendKeys * 128, 1024);
@@ -463,9 +469,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     // S_X = Q_qx K^T for the K tile in ring slot ks
     auto issue_qk = [&](int x, int qx, int ks) {
       const uint64_t qd = q_desc0 + (uint32_t)((qx * C::kQBytes) >> 4);
-      const uint64_t kd = k_desc0 + (uint32_t)((ks * C::kTileBytes) >> 4);
+      const uint64_t kd = k_desc0 + (uint32_t)((ks * C::kTileBytesK) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < DK / 16; ++kk) {
         const uint32_t qo = ((kk >> 2) * (kExtendRows * 128) + (kk & 3) * 32) >> 4;
         const uint32_t ko = ((kk >> 2) * (kExtendKeys * 128) + (kk & 3) * 32) >> 4;
         umma_bf16_warp(tmem + x * 128, qd + qo, kd + ko, idesc_qk, kk > 0);
@@ -476,7 +482,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     // epilogue waits for it); an earlier PV_X is known complete once the
     // s_full commit that follows it has fired
     auto issue_pv = [&](int x, int vs, bool first, bool last) {
-      const uint64_t vd = v_desc0 + (uint32_t)((vs * C::kTileBytes) >> 4);
+      const uint64_t vd = v_desc0 + (uint32_t)((vs * C::kTileBytesV) >> 4);
 #pragma unroll
       for (int kk = 0; kk < kExtendKeys / 16; ++kk)
         umma_bf16_ts_warp(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
@@ -637,12 +643,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           }
         } else if (valid) {
           if (split) {
-            for (int c = 0; c < D; c += 8)
-              *reinterpret_cast<uint4*>(a.m.partial_o + prow * D + c) = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < DV; c += 8)
+              *reinterpret_cast<uint4*>(a.m.partial_o + prow * DV + c) = make_uint4(0, 0, 0, 0);
             a.m.partial_lse[prow] = -INFINITY;
           } else {
-            for (int c = 0; c < D; c += 8)
-              *reinterpret_cast<uint4*>(a.out + orow * D + c) = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < DV; c += 8)
+              *reinterpret_cast<uint4*>(a.out + orow * DV + c) = make_uint4(0, 0, 0, 0);
             // no key: the LSE is the sink's alone
             if (a.lse) a.lse[orow] = (EXTRAS && a.sinks) ? a.sinks[g * G + R % G] : -INFINITY;
           }
@@ -655,11 +661,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       // previous epilogue saw its last PV complete
       if (ukv.uses_q(x) && !q_by_tma(u, x)) {
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {  // 128 bytes of the row at a time
+        for (int h = 0; h < DK / 64; ++h) {  // 128 bytes of the row at a time
           uint4 v[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            v[c] = valid ? __ldg(reinterpret_cast<const uint4*>(a.q + orow * D) + h * 8 + c) : make_uint4(0, 0, 0, 0);
+            v[c] = valid ? __ldg(reinterpret_cast<const uint4*>(a.q + orow * DK) + h * 8 + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(qtile + h * (kExtendRows * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v[c];
@@ -695,11 +701,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           }
           const int r0 = L - j * kExtendKeys;
           const int r1 = (np - j * kPagesPerTile) * kSegSlots;
-          uint8_t* vt = smem + C::kVOff + vs * C::kTileBytes;
-          const int n16 = (r1 - r0) * C::kColBlocks * 8;
+          uint8_t* vt = smem + C::kVOff + vs * C::kTileBytesV;
+          const int n16 = (r1 - r0) * C::kColBlocksV * 8;
           for (int i = r; i < n16; i += 128) {
-            const int row = r0 + i / (C::kColBlocks * 8);
-            const int rest = i % (C::kColBlocks * 8);
+            const int row = r0 + i / (C::kColBlocksV * 8);
+            const int rest = i % (C::kColBlocksV * 8);
             *reinterpret_cast<uint4*>(vt + (rest >> 3) * (kExtendKeys * 128) + row * 128 + (rest & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
@@ -763,7 +769,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           const float alpha = move && l > 0.f ? fast_exp2(m_ref - mt) : 1.f;
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) {
               uint32_t o[32];
               tmem_ld32(lane_base + o_col + c * 32, o);
               tmem_wait_ld();
@@ -843,7 +849,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       wa *= inv;
       wb *= inv;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_base + o_col + c * 32, o);
         if (ukv.dual) {
@@ -873,7 +879,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = pack_bf16(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
           {
-            uint16_t* dst = split ? a.m.partial_o + prow * D + c * 32 : a.out + orow * D + c * 32;
+            uint16_t* dst = split ? a.m.partial_o + prow * DV + c * 32 : a.out + orow * DV + c * 32;
             if (split || a.out_32B) {
               st_global_32B(dst, v);
               st_global_32B(dst + 16, v + 8);
@@ -964,16 +970,19 @@ template <class C>
 int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
                float v_scale, void* out, float* lse, cudaStream_t st, bool dplan) {
   CUtensorMap tk, tv;
-  const uint64_t inner = (uint64_t)c.cfg.num_kv_heads * C::D;
+  const uint64_t inner_k = (uint64_t)c.cfg.num_kv_heads * C::DK;
+  const uint64_t inner_v = (uint64_t)c.cfg.num_kv_heads * C::DV;
   uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
   const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
   if (fp8) {
+    // E4M3 pools have K and V heads of one width (the configuration check)
+    static_assert(C::DK == C::DV || C::DK != 128, "E4M3 staging copies K and V rows of one width");
     // widen the batch's E4M3 segments into the workspace copy and read that
     if (!c.lay.has_stage) return PKV_ERR_UNSUPPORTED;
     uint16_t* sk = reinterpret_cast<uint16_t*>(c.ws + c.lay.stage_k);
     uint16_t* sv = reinterpret_cast<uint16_t*>(c.ws + c.lay.stage_v);
     int* idx = reinterpret_cast<int*>(c.ws + c.lay.stage_idx);
-    const int seg_elems = kSegSlots * c.cfg.num_kv_heads * C::D;
+    const int seg_elems = kSegSlots * c.cfg.num_kv_heads * C::DK;
     if (launch_pdl(fp8_stage_kernel, dim3((unsigned)(c.num_sms * 4)), dim3(256), 0, st,
                    static_cast<const uint8_t*>(k_pool), static_cast<const uint8_t*>(v_pool), sk, sv, idx,
                    make_meta(c).seg_indices, static_cast<const int*>(make_meta(c).plan), seg_elems, k_scale,
@@ -983,11 +992,11 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
     v_pool = sv;
     slots = (uint64_t)c.cfg.max_pages_total * (c.cfg.page_size / kSegSlots) * kSegSlots;
   }
-  if (encode_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(k_pool), inner, slots, inner * 2, 64,
-                     kSegSlots, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+  if (encode_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(k_pool), inner_k, slots, inner_k * 2,
+                     64, kSegSlots, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
-  if (encode_tmap_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(v_pool), inner, slots, inner * 2, 64,
-                     kSegSlots, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+  if (encode_tmap_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(v_pool), inner_v, slots, inner_v * 2,
+                     64, kSegSlots, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
   ExtendArgs a;
   a.m = make_meta(c);
@@ -1015,9 +1024,9 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   if (kExtendRows % a.group == 0) {
     const uint32_t box_tok = kExtendRows / a.group;
     const uint64_t tokens = (uint64_t)(c.cfg.max_q_tokens > (int)box_tok ? c.cfg.max_q_tokens : (int)box_tok);
-    if (encode_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(q), C::D,
-                       (uint64_t)c.cfg.num_q_heads, tokens, (uint64_t)C::D * 2,
-                       (uint64_t)c.cfg.num_q_heads * C::D * 2, 64, (uint32_t)a.group, box_tok,
+    if (encode_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(q), C::DK,
+                       (uint64_t)c.cfg.num_q_heads, tokens, (uint64_t)C::DK * 2,
+                       (uint64_t)c.cfg.num_q_heads * C::DK * 2, 64, (uint32_t)a.group, box_tok,
                        CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
       return PKV_ERR_CUDA;
     a.q_tma = 1;
@@ -1038,9 +1047,13 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
 int run_tc(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
            float v_scale, void* out, float* lse, cudaStream_t st, bool dplan) {
   if (c.cfg.head_dim == 128)
-    return run_extend<ExtCfg<128, 3, 2>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
+    return run_extend<ExtCfg<128, 128, 3, 2>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
   if (c.cfg.head_dim == 64)
-    return run_extend<ExtCfg<64, 4, 4>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
+    return run_extend<ExtCfg<64, 64, 4, 4>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
+  // 192-wide Q/K heads with 128-wide V heads: two 48 KB Q tiles, so the rings
+  // hold two 48 KB K tiles and one 32 KB V tile
+  if (c.cfg.head_dim == 192)
+    return run_extend<ExtCfg<192, 128, 2, 1>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
   return PKV_ERR_UNSUPPORTED;
 }
 

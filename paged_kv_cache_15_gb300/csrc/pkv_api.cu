@@ -29,13 +29,17 @@ int check_config(const pkv_config* cfg) {
   const int group = cfg->num_q_heads / cfg->num_kv_heads;
   if (group > 16) return PKV_ERR_UNSUPPORTED;
   if (cfg->page_size != kPageSizeSmall && cfg->page_size != kPageSizeLarge) return PKV_ERR_UNSUPPORTED;
-  if (cfg->head_dim != 64 && cfg->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (cfg->kv_dtype == PKV_KV_FP8_E4M3 && cfg->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (cfg->head_dim_v < 0) return PKV_ERR_INVALID_ARG;
+  // head widths: 64/64, 128/128, and 192/128 (K and V heads of different widths)
+  const int dk = cfg->head_dim, dv = head_dim_v(*cfg);
+  if (!((dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128))) return PKV_ERR_UNSUPPORTED;
+  // E4M3 pools: 128-wide heads (an E4M3 row of 128 codes is one 128-byte span)
+  if (cfg->kv_dtype == PKV_KV_FP8_E4M3 && dk != 128) return PKV_ERR_UNSUPPORTED;
   if (decode_row_warps(*cfg) == 0) return PKV_ERR_UNSUPPORTED;  // max_qo_len * group > 128
   // slot indices and pool element offsets must fit the kernels' index types
   const long long slots = (long long)cfg->num_pages * cfg->page_size;
   if (slots > (1ll << 31) - 1) return PKV_ERR_UNSUPPORTED;
-  if ((long long)cfg->max_q_tokens * cfg->num_q_heads * cfg->head_dim > (1ll << 40)) return PKV_ERR_UNSUPPORTED;
+  if ((long long)cfg->max_q_tokens * cfg->num_q_heads * dk > (1ll << 40)) return PKV_ERR_UNSUPPORTED;
   // segment counts (pages times segments per page) must fit an int
   if ((long long)cfg->max_pages_total * (cfg->page_size / kSegSlots) > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
   return PKV_OK;
@@ -102,14 +106,15 @@ Layout make_layout(const pkv_config& cfg, int num_sms, bool with_stage) {
   L.seg_indices = L.seg_per_page > 1 ? take(sizeof(int) * (size_t)max_segments(cfg)) : L.kv_indices;
   L.decode_items = take(sizeof(DecodeItem) * (size_t)L.max_decode_items);
   L.extend_tiles = take(sizeof(ExtendTile) * (size_t)L.max_extend_tiles);
-  L.partial_o = take(sizeof(uint16_t) * (size_t)cap * cfg.num_q_heads * cfg.head_dim);
+  L.partial_o = take(sizeof(uint16_t) * (size_t)cap * cfg.num_q_heads * head_dim_v(cfg));
   L.partial_lse = take(sizeof(float) * (size_t)cap * cfg.num_q_heads);
   L.has_stage = with_stage && cfg.kv_dtype == PKV_KV_FP8_E4M3;
   L.stage_k = L.stage_v = L.stage_idx = 0;
   if (L.has_stage) {
-    const size_t seg_bytes = (size_t)kSegSlots * cfg.num_kv_heads * cfg.head_dim * sizeof(uint16_t);
-    L.stage_k = take(seg_bytes * (size_t)max_segments(cfg));
-    L.stage_v = take(seg_bytes * (size_t)max_segments(cfg));
+    const size_t seg_k = (size_t)kSegSlots * cfg.num_kv_heads * cfg.head_dim * sizeof(uint16_t);
+    const size_t seg_v = (size_t)kSegSlots * cfg.num_kv_heads * head_dim_v(cfg) * sizeof(uint16_t);
+    L.stage_k = take(seg_k * (size_t)max_segments(cfg));
+    L.stage_v = take(seg_v * (size_t)max_segments(cfg));
     L.stage_idx = take(sizeof(int) * (size_t)max_segments(cfg));
   }
   L.total = off;
@@ -438,9 +443,9 @@ int pkv_describe(pkv_ctx* ctx, char* buf, size_t n) {
     snprintf(dec, sizeof dec, "split-KV TMA+mma.sync key-major, up to %d rows/unit, %d pages/stage, grid %d",
              rows <= 8 ? 8 : 16, decode_stage_pages(c), ctx->decode_ctas);
   snprintf(buf, n,
-           "pkv sm_103a: heads %d/%d (group %d) head_dim %d page_size %d kv %s pool_pages %d | decode: %s | "
+           "pkv sm_103a: heads %d/%d (group %d) head_dim %d/%d page_size %d kv %s pool_pages %d | decode: %s | "
            "extend: tcgen05 %dx%d tiles, grid %d | SMs %d",
-           c.num_q_heads, c.num_kv_heads, group, c.head_dim, c.page_size,
+           c.num_q_heads, c.num_kv_heads, group, c.head_dim, head_dim_v(c), c.page_size,
            c.kv_dtype == PKV_KV_FP8_E4M3 ? "fp8_e4m3" : "bf16", c.num_pages, dec, kExtendRows, kExtendKeys,
            ctx->extend_ctas, ctx->num_sms);
   return PKV_OK;

@@ -112,6 +112,9 @@ struct Ctx {
   const float* sinks = nullptr;    // per-query-head sink logits (pkv_set_attention_sinks), or null
 };
 
+// Width of the V heads and of the output rows (head_dim_v, 0 meaning head_dim).
+inline int head_dim_v(const pkv_config& c) { return c.head_dim_v > 0 ? c.head_dim_v : c.head_dim; }
+
 // The tree mask the next forward applies: only after a build in a verify mode.
 inline const uint64_t* active_tree(const Ctx& c) {
   return (c.mode == PKV_MODE_TARGET_VERIFY || c.mode == PKV_MODE_DRAFT_EXTEND) ? c.tree : nullptr;
@@ -133,7 +136,7 @@ struct Meta {
   const int* token_req;
   const DecodeItem* decode_items;
   const ExtendTile* extend_tiles;
-  uint16_t* partial_o;  // bf16 [rows][Hq][D]: normalised partial outputs of split units
+  uint16_t* partial_o;  // bf16 [rows][Hq][Dv]: normalised partial outputs of split units
   float* partial_lse;
 };
 

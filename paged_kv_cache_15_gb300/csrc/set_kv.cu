@@ -8,7 +8,9 @@
 //
 // HBM-bound copy: every thread moves one 16-byte vector (8 elements) of K and
 // the matching vector of V; consecutive threads cover consecutive bytes of a
-// [token][kv_head][head_dim] row, so loads and stores are fully coalesced.
+// [token][kv_head][width] row, so loads and stores are fully coalesced. When
+// the V heads are narrower than the K heads, the threads past a V row's end
+// move only their K vector.
 #include "pkv_internal.cuh"
 
 namespace pkv {
@@ -38,8 +40,8 @@ __global__ void __launch_bounds__(kThreads) set_kv_kernel(void* __restrict__ k_p
                                                           const int* __restrict__ loc,
                                                           const uint4* __restrict__ k_new,
                                                           const uint4* __restrict__ v_new, long long n_vec,
-                                                          int vec_per_token, long long num_slots, float k_inv,
-                                                          float v_inv, int* plan) {
+                                                          int vec_per_token, int vec_per_token_v,
+                                                          long long num_slots, float k_inv, float v_inv, int* plan) {
   // launched with programmatic serialization: the next kernel may start
   // launching now, and this one touches memory only after the previous grid
   // (which may have produced the new K/V or the slots) has finished
@@ -54,15 +56,18 @@ __global__ void __launch_bounds__(kThreads) set_kv_kernel(void* __restrict__ k_p
       if (within == 0) record_error(plan, PKV_DEV_BAD_SLOT, (int)tok);
       continue;
     }
-    uint4 kx = __ldcs(k_new + u);
-    uint4 vx = __ldcs(v_new + u);
-    long long dst = slot * vec_per_token + within;
+    // K row: vec_per_token vectors; V row: vec_per_token_v (at most as many)
+    const uint4 kx = __ldcs(k_new + u);
+    const long long dst = slot * vec_per_token + within;
+    const bool has_v = within < vec_per_token_v;
+    const long long vsrc = tok * vec_per_token_v + within;
+    const long long vdst = slot * vec_per_token_v + within;
     if constexpr (kFp8) {
       reinterpret_cast<uint2*>(k_pool)[dst] = quant8(kx, k_inv);
-      reinterpret_cast<uint2*>(v_pool)[dst] = quant8(vx, v_inv);
+      if (has_v) reinterpret_cast<uint2*>(v_pool)[vdst] = quant8(__ldcs(v_new + vsrc), v_inv);
     } else {
       reinterpret_cast<uint4*>(k_pool)[dst] = kx;
-      reinterpret_cast<uint4*>(v_pool)[dst] = vx;
+      if (has_v) reinterpret_cast<uint4*>(v_pool)[vdst] = __ldcs(v_new + vsrc);
     }
   }
 }
@@ -72,7 +77,9 @@ __global__ void __launch_bounds__(kThreads) set_kv_kernel(void* __restrict__ k_p
 int launch_set_kv_buffer(Ctx& c, void* k_pool, void* v_pool, const int32_t* loc, const void* k, const void* v,
                          int n, float k_inv, float v_inv, cudaStream_t st) {
   if (n == 0) return PKV_OK;
+  // the K heads are at least as wide as the V heads (check_config)
   int vec_per_token = c.cfg.num_kv_heads * c.cfg.head_dim / 8;
+  int vec_per_token_v = c.cfg.num_kv_heads * head_dim_v(c.cfg) / 8;
   long long n_vec = (long long)n * vec_per_token;
   long long blocks = (n_vec + kThreads - 1) / kThreads;
   long long cap = (long long)c.num_sms * 16;
@@ -82,10 +89,10 @@ int launch_set_kv_buffer(Ctx& c, void* k_pool, void* v_pool, const int32_t* loc,
   cudaError_t e;
   if (c.cfg.kv_dtype == PKV_KV_FP8_E4M3)
     e = launch_pdl(set_kv_kernel<true>, dim3(grid), dim3(kThreads), 0, st, k_pool, v_pool, loc, (const uint4*)k,
-                   (const uint4*)v, n_vec, vec_per_token, num_slots, k_inv, v_inv, plan);
+                   (const uint4*)v, n_vec, vec_per_token, vec_per_token_v, num_slots, k_inv, v_inv, plan);
   else
     e = launch_pdl(set_kv_kernel<false>, dim3(grid), dim3(kThreads), 0, st, k_pool, v_pool, loc, (const uint4*)k,
-                   (const uint4*)v, n_vec, vec_per_token, num_slots, k_inv, v_inv, plan);
+                   (const uint4*)v, n_vec, vec_per_token, vec_per_token_v, num_slots, k_inv, v_inv, plan);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -23,7 +23,7 @@ def config_for(W: Workload, max_batch=None, max_pages_total=None, max_q_tokens=N
     return B.make_config(W.num_q_heads, W.num_kv_heads, W.head_dim, W.page_size,
                          B.PKV_KV_FP8_E4M3 if W.is_fp8 else B.PKV_KV_BF16, W.num_pages,
                          max_batch or max(W.bs, 1), max_pages_total or max(pages, 1),
-                         max_q_tokens or max(W.total_q, 1), max_qo_len)
+                         max_q_tokens or max(W.total_q, 1), max_qo_len, head_dim_v=W.head_dim_v)
 
 
 class DeviceBatch:
@@ -43,7 +43,8 @@ class DeviceBatch:
         self.seq_lens = torch.from_numpy(W.seq_lens).to(dev)
         self.qo_lens = None if W.mode == "decode" else torch.from_numpy(W.qo_lens).to(dev)
         self.page_table = torch.from_numpy(W.page_table).to(dev)
-        self.out = torch.empty_like(self.q)
+        # output rows have the V heads' width
+        self.out = torch.empty((W.total_q, W.num_q_heads, W.dv), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((W.total_q, W.num_q_heads), dtype=torch.float32, device=dev)
         self.mode = MODE_OF[W.mode]
         # draft-tree mask words (uint64, carried as int64 bits)

@@ -84,6 +84,13 @@ def _cfg(**kw):
     (dict(num_q_heads=64, num_kv_heads=2), B.PKV_ERR_UNSUPPORTED),  # group 32
     (dict(max_qo_len=9, num_q_heads=64, num_kv_heads=4), B.PKV_ERR_UNSUPPORTED),  # 9 x 16 rows > 128
     (dict(max_batch=0), B.PKV_ERR_INVALID_ARG),
+    # K and V heads of different widths: only 192 / 128, bf16 pools
+    (dict(head_dim_v=-1), B.PKV_ERR_INVALID_ARG),
+    (dict(head_dim=128, head_dim_v=64), B.PKV_ERR_UNSUPPORTED),
+    (dict(head_dim=192, head_dim_v=64), B.PKV_ERR_UNSUPPORTED),
+    (dict(head_dim=192), B.PKV_ERR_UNSUPPORTED),  # 192-wide V heads
+    (dict(head_dim=64, head_dim_v=128), B.PKV_ERR_UNSUPPORTED),
+    (dict(kv_dtype=B.PKV_KV_FP8_E4M3, head_dim=192, head_dim_v=128), B.PKV_ERR_UNSUPPORTED),
 ])
 def test_config_rejected_before_any_device_call(lib, kw, status):
     n = ctypes.c_size_t(0)
@@ -102,6 +109,20 @@ def test_null_arguments_rejected(lib):
     assert L.pkv_destroy(None) == B.PKV_OK
     code = ctypes.c_int32(0)
     assert L.pkv_get_device_error(None, ctypes.byref(code), None) == B.PKV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("widths", [(64, 0), (128, 0), (128, 128), (192, 128)])
+def test_supported_head_widths_accepted(lib, widths):
+    """Equal widths (head_dim_v 0 or equal) and 192-wide Q/K heads with
+    128-wide V heads pass the configuration checks."""
+    n = ctypes.c_size_t(0)
+    st = B.lib().pkv_workspace_bytes(ctypes.byref(_cfg(head_dim=widths[0], head_dim_v=widths[1])), ctypes.byref(n))
+    assert st in (B.PKV_OK, B.PKV_ERR_CUDA)
+
+
+def test_pool_bytes_is_the_k_pool(lib):
+    cfg = B.make_config(32, 8, 192, 16, B.PKV_KV_BF16, 10, 1, 1, 1, head_dim_v=128)
+    assert B.pkv_pool_bytes(cfg) == 10 * 16 * 8 * 192 * 2
 
 
 @pytest.mark.parametrize("page_size", [16, 128])

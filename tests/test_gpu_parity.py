@@ -806,3 +806,68 @@ def test_merge_at_the_split_cap(mode):
 def test_verify_prefill_path_long_context_split():
     W = make_workload("vlong", "verify", 4, 64, 4, 128, [20000, 300, 12000, 5000], [8, 4, 6, 7])
     full_check(W, spec_mode=B.PKV_SPEC_PREFILL)
+
+
+# ------------------------------------------------------------------ K and V heads of different widths
+# Q/K heads 192 wide, V heads (and output rows) 128 wide: the shape that
+# "--attention-backend", section "How SGLang picks a default", routes to a
+# dedicated backend on SM100/SM103.
+W192 = (192, 128)
+
+
+def _widths_case(case):
+    rng = np.random.default_rng(60)
+    if case == "decode_g4":  # one 8-row key-major tile
+        return preset("llama3_8b_decode", bs=12, len_scale=0.2, head_dims=W192), B.PKV_SPEC_PREFILL
+    if case == "decode_g16_ragged":  # two 8-row tiles; empty, one-key and page-tail lengths
+        return make_workload("w16", "decode", 7, 32, 2, 192, [0, 0, 15, 16, 1000, 3333, 77], np.ones(7),
+                             head_dim_v=128), B.PKV_SPEC_PREFILL
+    if case == "extend":
+        return preset("prefix_extend", bs=3, len_scale=0.25, head_dims=W192), B.PKV_SPEC_PREFILL
+    if case == "extend_g16_q_tma":  # Q tiles by TMA (the group divides 128), three column blocks
+        return make_workload("we16", "extend", 3, 32, 2, 192, [3000, 17, 0], [300, 129, 1],
+                             head_dim_v=128), B.PKV_SPEC_PREFILL
+    if case == "extend_g6_q_copied":  # the softmax warps copy Q rows (group 6)
+        return make_workload("we6", "extend", 3, 12, 2, 192, [500, 0, 64], [77, 200, 5],
+                             head_dim_v=128), B.PKV_SPEC_PREFILL
+    if case in ("verify_decode", "verify_prefill"):
+        W = preset("spec_verify", bs=6, len_scale=0.1, head_dims=W192)
+        return W, B.PKV_SPEC_DECODE if case == "verify_decode" else B.PKV_SPEC_PREFILL
+    if case == "page_size_128":
+        return preset("prefix_extend", bs=3, len_scale=0.25, page_size=128, head_dims=W192), B.PKV_SPEC_PREFILL
+    if case in ("tree_sinks_decode", "tree_sinks_prefill"):
+        W = make_workload("wt", "verify", 5, 32, 4, 192, rng.integers(50, 900, 5), rng.integers(2, 16, 5),
+                          head_dim_v=128)
+        W.tree_mask = random_tree_masks(W.qo_lens, seed=61)
+        W.sinks = random_sinks(W.num_q_heads, seed=62)
+        return W, B.PKV_SPEC_DECODE if case == "tree_sinks_decode" else B.PKV_SPEC_PREFILL
+    raise KeyError(case)
+
+
+@pytest.mark.parametrize("case", ["decode_g4", "decode_g16_ragged", "extend", "extend_g16_q_tma",
+                                  "extend_g6_q_copied", "verify_decode", "verify_prefill", "page_size_128",
+                                  "tree_sinks_decode", "tree_sinks_prefill"])
+def test_head_widths_192_128_parity(case):
+    """Every row against the oracle with 192-wide Q/K heads and 128-wide V
+    heads, on both paths: scores over 192 columns, outputs of 128."""
+    W, spec = _widths_case(case)
+    d = full_check(W, spec_mode=spec)
+    assert d.out.shape[-1] == 128
+
+
+def test_head_widths_192_128_pools_bit_exact():
+    """set_kv_buffer writes 192-wide K rows and 128-wide V rows, bit for bit,
+    every other slot untouched."""
+    W = make_workload("wp", "extend", 5, 16, 8, 192, [0, 40, 7, 100, 3], [37, 16, 1, 200, 90], head_dim_v=128)
+    d = DeviceBatch(W)
+    d.set_kv_buffer()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    kp, vp = oracle_pools(W)
+    assert np.array_equal(pool_bits(d.k_pool.cpu()), kp)
+    assert np.array_equal(pool_bits(d.v_pool.cpu()), vp)
+
+
+def test_head_widths_192_128_full_size_decode_every_row():
+    """The Llama-3-8B-shaped decode batch at full size with 192/128 heads."""
+    full_check(preset("llama3_8b_decode", head_dims=W192))
