@@ -506,6 +506,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--spec-mode", default="prefill", choices=["prefill", "decode"])
     ap.add_argument("--page-size", type=int, default=16, choices=[16, 128])
+    ap.add_argument("--kv-dtype", default=None, choices=["bf16", "fp8_e4m3"],
+                    help="pool element type (default: the workload's own)")
     ap.add_argument("--head-dims", type=int, nargs=2, default=None, metavar=("DK", "DV"),
                     help="widths of the Q/K and V heads (default: the workload's own)")
     ap.add_argument("--ref-budget", type=float, default=15.0)
@@ -518,7 +520,7 @@ def main():
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     from paged_kv_cache_15_gb300.workloads import preset
-    W = preset(args.workload, page_size=args.page_size,
+    W = preset(args.workload, page_size=args.page_size, kv_dtype=args.kv_dtype,
                head_dims=tuple(args.head_dims) if args.head_dims else None)
     if args.impl == "reference":
         run_reference(args, W, rank, world)

@@ -208,10 +208,10 @@ int pkv_forward_decode(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, cons
 /* forward_extend: causal attention of each request's query block (its
  * qo_len new tokens) against its cached prefix plus the new tokens, on the
  * tensor cores. Same arguments and layouts as pkv_forward_decode. With an
- * E4M3 pool the call first dequantises the batch's pages into a bf16 copy in
- * the workspace (code * scale, rounded once to bf16: at most 2^-9 relative
- * per element), then runs the same kernel on it; the workspace of an E4M3
- * context holds that copy (pkv_workspace_bytes counts it). */
+ * E4M3 pool the kernel widens each tile's codes to f16 in shared memory
+ * (exact) and runs its MMAs in f16, Q and P rounded to f16, k_scale folded
+ * into the score scale and v_scale into the output, as the decode path does;
+ * the workspace holds no copy of the pool. */
 int pkv_forward_extend(pkv_ctx* ctx, const void* d_q, const void* d_k_pool, const void* d_v_pool, float sm_scale,
                        float k_scale, float v_scale, void* d_out, float* d_lse, void* stream);
 

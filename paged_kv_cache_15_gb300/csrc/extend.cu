@@ -44,9 +44,14 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Bounds on one tile's row sum of p = 2^(s * scale - m_ref) between which the
-// reference m_ref stays put (see the softmax role).
+// reference m_ref stays put (see the softmax role). With bf16 P any p up to
+// 2^16 is representable; with f16 P (E4M3 pools) p stays at most 2^15, below
+// the f16 maximum, and a row's first mass at least 2^-8, so its largest p
+// is a normal f16 number.
 constexpr float kSumHigh = 65536.0f;               // 2^16
 constexpr float kSumLow = 5.421010862427522e-20f;  // 2^-64
+constexpr float kSumHighF16 = 32768.0f;            // 2^15
+constexpr float kSumLowF16 = 0.00390625f;          // 2^-8
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
@@ -126,16 +131,33 @@ __device__ __forceinline__ float max32(const uint32_t* sr, float m) {
   return max3f(fmaxf(a0, a1), a2, a3);
 }
 
-// p = exp2(s * scale - ref) for 32 raw scores: packed bf16 pairs into pk,
-// running sums in four packed accumulators.
+// p = exp2(s * scale - ref) for 32 raw scores: packed bf16 (F16: f16) pairs
+// into pk, running sums in four packed accumulators.
+template <bool F16>
 __device__ __forceinline__ void exp32(const uint32_t* sr, uint64_t sc2, uint64_t nref2, uint32_t* pk, uint64_t* acc) {
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
     const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nref2);
     const float p0 = fast_exp2(f2_lo(x)), p1 = fast_exp2(f2_hi(x));
     acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
-    pk[c >> 1] = pack_bf16(p0, p1);
+    pk[c >> 1] = F16 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
   }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// 8 bf16 -> 8 f16 (round to nearest even; exact for the normal range)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v) {
+  auto cv = [](uint32_t w) { return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); };
+  return make_uint4(cv(v.x), cv(v.y), cv(v.z), cv(v.w));
 }
 
 // The two tiles' KV ranges inside a unit, and the order in which the unit's
@@ -179,12 +201,18 @@ __device__ __forceinline__ UnitKV unit_kv(const ExtendTile& u) {
 
 // DK: width of the Q and K heads; DV: of the V heads and the output rows
 // (equal except for models whose K and V heads differ, 192 / 128).
-template <int DK_, int DV_, int NK_, int NV_>
+// FP8: E4M3 pools. TMA brings the codes into raw rings (RK / RV tiles of one
+// byte per code), the K and V producer warps widen them to f16 (exactly) into
+// the operand rings, and the MMAs run in f16 with Q and P rounded to f16.
+template <int DK_, int DV_, int NK_, int NV_, bool FP8_ = false, int RK_ = 0, int RV_ = 0>
 struct ExtCfg {
   static constexpr int DK = DK_;
   static constexpr int DV = DV_;
   static constexpr int NK = NK_;  // K ring depth
   static constexpr int NV = NV_;  // V ring depth
+  static constexpr bool FP8 = FP8_;
+  static constexpr int RK = RK_;  // raw E4M3 K tiles in flight
+  static constexpr int RV = RV_;
   static constexpr int kThreads = 352;
   static constexpr int kProducerWarp = 8;   // K tiles
   static constexpr int kMmaWarp = 9;
@@ -197,8 +225,11 @@ struct ExtCfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kQBytes;
   static constexpr int kVOff = kKOff + NK * kTileBytesK;
-  static constexpr int kBarOff = kVOff + NV * kTileBytesV;
-  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6 + 4 + 2;
+  static constexpr int kRawTileBytes = kExtendKeys * 128;  // 128 E4M3 codes per row
+  static constexpr int kRawKOff = kVOff + NV * kTileBytesV;
+  static constexpr int kRawVOff = kRawKOff + RK * kRawTileBytes;
+  static constexpr int kBarOff = kRawVOff + RV * kRawTileBytes;
+  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6 + 4 + 2 + RK + RV;
   static constexpr int kMergeOff = kBarOff + kNumBars * 8;           // dual units: tile B's (m, l) per row
   static constexpr int kTmemSlotOff = kMergeOff + 2 * kExtendRows * 4;
   static constexpr int kAbortOff = kTmemSlotOff + 8;
@@ -206,6 +237,8 @@ struct ExtCfg {
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(DV <= 128, "O needs at most 128 TMEM columns per tile");
+  static_assert(!FP8 || (DK == 128 && DV == 128 && RK >= 1 && RV >= 1), "E4M3 rows are one 128-byte span");
+  static_assert(FP8 || (RK == 0 && RV == 0), "raw rings only for E4M3 pools");
 };
 
 struct ExtendArgs {
@@ -215,6 +248,7 @@ struct ExtendArgs {
   float* lse;
   int num_q_heads, num_kv_heads, group;
   float scale_log2;
+  float v_scale;     // multiplies the output rows (the V pool's scale of an E4M3 pool; 1 for bf16)
   int q_tma;         // 1 when the group divides 128: a Q tile is one TMA box of 128/G tokens x G heads
   int q_box_tokens;  // 128 / group
   int out_32B;       // out is 32-byte aligned: output rows are written with 32-byte stores
@@ -273,6 +307,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   uint64_t* q_written = q_empty + 2;    // [2] softmax warps wrote Q_X (tiles not loaded by TMA)
   uint64_t* b_done = q_written + 2;     // dual unit: tile B's O is final and its (m, l) are in smem
   uint64_t* a_read = b_done + 1;        // dual unit: tile A has read tile B's O and (m, l)
+  uint64_t* raw_full = a_read + 1;      // E4M3: [RK] raw K tiles, then [RV] raw V tiles, landed
   float* s_merge = reinterpret_cast<float*>(smem + C::kMergeOff);  // [2][128]: m, l of tile B's rows
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
@@ -292,6 +327,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     }
     mbar_init(b_done, 4);  // one arrival per softmax warp
     mbar_init(a_read, 4);
+    // K / V operand tiles: the producer's arrival (with the TMA bytes, or
+    // after widening E4M3 codes)
     for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -300,6 +337,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
+    for (int s = 0; s < C::RK + C::RV; ++s) mbar_init(&raw_full[s], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -330,7 +368,161 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     return a.q_tma != 0 && a.m.qo_indptr[u.b] + (u.row0 + x * kExtendRows) / G + a.q_box_tokens <= total_q;
   };
 
-  if (warp == C::kProducerWarp || warp == C::kVProducerWarp) {
+  if (C::FP8 && (warp == C::kProducerWarp || warp == C::kVProducerWarp)) {
+    // ------------------------------------------------------------ E4M3 producers
+    // Warp 8 streams K, warp 10 V. TMA lands each tile's codes in the raw ring
+    // (one 16-row x 128-byte box per page, 128-byte swizzle); the warp widens
+    // the rows of the loaded pages to f16 (exact) into the operand ring, in
+    // the operand layout (two 64-column blocks, 128-byte swizzle), and marks
+    // the operand tile full. A raw slot is requested again as soon as the warp
+    // has read it, R tiles ahead of the widening. Warp 8 also hands Q over.
+    const bool is_v = warp == C::kVProducerWarp;
+    const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
+    if (elect_one()) prefetch_tmap(tmap);
+    const int R = is_v ? C::RV : C::RK;
+    const int depth = is_v ? NV : NK;
+    uint64_t* rfull = is_v ? raw_full + C::RK : raw_full;
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* empty = is_v ? v_empty : k_empty;
+    uint8_t* raw_ring = smem + (is_v ? C::kRawVOff : C::kRawKOff);
+    const uint32_t raw_base = smem_u32(raw_ring);
+    const uint32_t op_base = smem_u32(smem + (is_v ? C::kVOff : C::kKOff));
+    constexpr int kOpTile = kExtendKeys * 128 * 2;  // one f16 tile of 128-wide rows
+    const uint64_t pol_stream = policy_evict_first();  // the bf16 producers' choice, below
+    const uint64_t pol_reuse = policy_evict_normal();
+    uint32_t jt = 0;  // operand tiles so far
+    uint32_t rt = 0, ct = 0;  // raw tiles requested / widened so far
+    uint32_t qcount[2] = {0, 0}, qtcount[2] = {0, 0};
+    bool stop = false;
+    const int c = lane & 7, r0 = lane >> 3;  // 16-code chunk and first row of this lane
+    for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
+      const ExtendTile u = load_unit(a, w / a.num_kv_heads);
+      const int g = w % a.num_kv_heads;
+      const UnitKV ukv = unit_kv(u);
+      const int np = a.m.seg_indptr[u.b + 1] - a.m.seg_indptr[u.b];
+      const int page_base = a.m.seg_indptr[u.b];
+      const bool reused = !a.dplan && (a.m.qo_indptr[u.b + 1] - a.m.qo_indptr[u.b]) * G > kExtendUnitRows;
+      const uint64_t pol = reused ? pol_reuse : pol_stream;
+      auto seq_tile = [&](int e) {
+        if (!ukv.dual) return ukv.s0 + e;
+        const int m = min(ukv.n0, ukv.n1);
+        const int step = e < 2 * m ? e >> 1 : e - m;
+        const int x = e < 2 * m ? (e & 1) : (ukv.n0 > ukv.n1 ? 0 : 1);
+        return ukv.start(x) + step;
+      };
+      const int len = ukv.len();
+      // page indices of 4 consecutive tiles: lane 8k + p holds page p of tile e0 + k
+      auto load_group = [&](int e0) {
+        const int e = e0 + (lane >> 3), p = lane & 7;
+        if (e >= len) return 0;
+        const int jj = seq_tile(e);
+        return p < np - jj * kPagesPerTile ? __ldg(a.m.seg_indices + page_base + jj * kPagesPerTile + p) : 0;
+      };
+      int grp = load_group(0);
+      int grp_next = load_group(4);
+      int issued = 0;
+      // request raw tile `issued` of the unit into raw slot rt % R (read already)
+      auto issue = [&]() {
+        const int e = issued;
+        if (e > 0 && (e & 3) == 0) {
+          grp = grp_next;
+          grp_next = load_group(e + 4);
+        }
+        const int j = seq_tile(e);
+        const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
+        const int rs = (int)(rt % R);
+        const bool leader = elect_one();
+        if (leader) mbar_arrive_expect_tx(&rfull[rs], (uint32_t)(npg * kSegSlots * 128));
+        uint8_t* dst = raw_ring + rs * C::kRawTileBytes;
+#pragma unroll
+        for (int p = 0; p < kPagesPerTile; ++p) {
+          const int pg = __shfl_sync(0xffffffffu, grp, ((e & 3) << 3) + p);
+          if (p < npg && leader)
+            tma_load_2d_hint(dst + p * (kSegSlots * 128), tmap, g * 128, pg * kSegSlots, &rfull[rs], pol);
+        }
+        ++rt;
+        ++issued;
+      };
+      for (int k = 0; k < R && issued < len; ++k) issue();
+      if (!is_v) {
+        // Q of the unit: written (f16) by the softmax warps once the previous
+        // unit's last QK on the tile has finished, then handed to the MMA warp
+        // (the first raw tiles are in flight meanwhile)
+        for (int x = 0; x < 2 && !stop; ++x) {
+          if (!ukv.uses_q(x)) continue;
+          if (!mbar_wait_warp(&q_empty[x], (qcount[x] & 1) ^ 1, plan, s_abort) ||
+              !mbar_wait_warp(&q_written[x], qtcount[x] & 1, plan, s_abort)) {
+            stop = true;
+            break;
+          }
+          ++qtcount[x];
+          ++qcount[x];
+          if (elect_one()) mbar_arrive(&q_full[x]);
+        }
+        if (stop) break;
+      }
+      for (int e = 0; e < len; ++e, ++jt) {
+        const int rs = (int)(ct % R);
+        if (!mbar_wait_warp(&rfull[rs], (ct / R) & 1, plan, s_abort)) {
+          stop = true;
+          break;
+        }
+        ++ct;
+        const int j = seq_tile(e);
+        const int npg = min(kPagesPerTile, np - j * kPagesPerTile);
+        const int st = jt % depth;
+        if (!mbar_wait_warp(&empty[st], ((jt / depth) & 1) ^ 1, plan, s_abort)) {
+          stop = true;
+          break;
+        }
+        const uint32_t src = raw_base + rs * C::kRawTileBytes;
+        const uint32_t out_blk = op_base + st * kOpTile + (c >> 2) * (kExtendKeys * 128);
+        // lane: chunk c (codes 16c .. 16c + 15) of rows r0 + 4k; one 16-byte
+        // chunk in, f16 chunks 2c and 2c + 1 of column block c / 4 out. Four
+        // rows a group, the next group's chunks loaded before this one is widened.
+        auto ld = [&](int k) {
+          const int r = r0 + 4 * k;
+          return lds128(src + r * 128 + ((c ^ (r & 7)) << 4));
+        };
+        auto widen = [&](int k, const uint4& x) {
+          const int r = r0 + 4 * k;
+          const uint4 lo = make_uint4(e4m3x2_to_f16x2((uint16_t)(x.x & 0xffffu)), e4m3x2_to_f16x2((uint16_t)(x.x >> 16)),
+                                      e4m3x2_to_f16x2((uint16_t)(x.y & 0xffffu)), e4m3x2_to_f16x2((uint16_t)(x.y >> 16)));
+          const uint4 hi = make_uint4(e4m3x2_to_f16x2((uint16_t)(x.z & 0xffffu)), e4m3x2_to_f16x2((uint16_t)(x.z >> 16)),
+                                      e4m3x2_to_f16x2((uint16_t)(x.w & 0xffffu)), e4m3x2_to_f16x2((uint16_t)(x.w >> 16)));
+          const uint32_t row = out_blk + r * 128;
+          sts128(row + ((((2 * c) & 7) ^ (r & 7)) << 4), lo);
+          sts128(row + ((((2 * c + 1) & 7) ^ (r & 7)) << 4), hi);
+        };
+        const int nk = npg * 4;  // groups of four rows (a multiple of 4)
+        uint4 x[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) x[v] = ld(v);
+        for (int k0 = 0; k0 < nk; k0 += 4) {
+          uint4 y[4];
+          const bool more = k0 + 4 < nk;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) y[v] = more ? ld(k0 + 4 + v) : x[v];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) widen(k0 + v, x[v]);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) x[v] = y[v];
+        }
+        // the f16 tile is read by the tensor core (async proxy), and the raw
+        // slot is refilled by TMA next
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[st]);
+        if (issued < len) issue();
+      }
+    }
+    if (stop && lane == 0) *s_abort = 1;
+    // never leave the CTA with a TMA still writing into shared memory: raw
+    // tiles requested and not yet waited for (these waits ignore the abort
+    // flag on purpose)
+    for (uint32_t t = ct; t < rt; ++t) mbar_wait(&rfull[t % R], (t / R) & 1, plan);
+    __syncwarp();
+  } else if (warp == C::kProducerWarp || warp == C::kVProducerWarp) {
     // ------------------------------------------------------------ producers
     // one warp streams K tiles, the other V tiles, each through its own ring,
     // so a full V ring never holds back the next K tile
@@ -348,7 +540,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       prefetch_tmap(tmap);
       if (!is_v && a.q_tma) prefetch_tmap(&tmap_q);
     }
-    const uint64_t pol = policy_evict_first();
+    // L2 priority of the K/V tiles: a request whose rows span several units
+    // has every one of them read its K/V tiles, so those lines stay at normal
+    // priority for the other units (on the prefix-cached extend batch DRAM
+    // traffic fell from 3.4x to 0.96x the algorithmic bytes); K/V that only
+    // one unit reads streams through at evict-first priority (verify batches
+    // ran 10 % slower at normal priority)
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_reuse = policy_evict_normal();
     uint32_t jt = 0;
     uint32_t armed = 0, armed_ph = 0;
     uint32_t qcount[2] = {0, 0};   // Q tiles issued per X (phase of q_full / q_empty)
@@ -360,10 +559,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       const UnitKV ukv = unit_kv(u);
       const int np = a.m.seg_indptr[u.b + 1] - a.m.seg_indptr[u.b];
       const int page_base = a.m.seg_indptr[u.b];
-      if (!is_v) {
-        // the unit's Q tiles, each once the previous unit's last QK on it has
-        // finished: by TMA (a box of 128/G tokens x the group's G heads), or
-        // forwarded from the softmax warps that wrote it
+      const bool reused = !a.dplan && (a.m.qo_indptr[u.b + 1] - a.m.qo_indptr[u.b]) * G > kExtendUnitRows;
+      const uint64_t pol = reused ? pol_reuse : pol_stream;
+      // the unit's Q tiles (K producer), each once the previous unit's last QK
+      // on it has finished: by TMA (a box of 128/G tokens x the group's G
+      // heads), or forwarded from the softmax warps that wrote it
+      auto fill_q = [&]() {
         for (int x = 0; x < 2; ++x) {
           if (!ukv.uses_q(x)) continue;
           if (!mbar_wait_warp(&q_empty[x], (qcount[x] & 1) ^ 1, plan, s_abort)) {
@@ -389,6 +590,9 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           }
           ++qcount[x];
         }
+      };
+      if (!is_v) {
+        fill_q();
         if (stop) break;
       }
       // e-th KV tile of the unit's sequence
@@ -453,8 +657,10 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     // The whole warp runs the loop and one elected lane issues each tcgen05
     // instruction. Descriptors: the start-address field is the low bits, so a
     // byte offset b inside the tile adds b >> 4.
-    constexpr uint32_t idesc_qk = umma_idesc_bf16(kExtendRows, kExtendKeys, false, false);
-    constexpr uint32_t idesc_pv = umma_idesc_bf16(kExtendRows, DV, false, true);
+    constexpr uint32_t idesc_qk = C::FP8 ? umma_idesc_f16(kExtendRows, kExtendKeys, false, false)
+                                         : umma_idesc_bf16(kExtendRows, kExtendKeys, false, false);
+    constexpr uint32_t idesc_pv = C::FP8 ? umma_idesc_f16(kExtendRows, DV, false, true)
+                                         : umma_idesc_bf16(kExtendRows, DV, false, true);
     const uint64_t q_desc0 = umma_desc_sw128(smem_base + C::kQOff, 16, 1024);
     const uint64_t k_desc0 = umma_desc_sw128(smem_base + C::kKOff, 16, 1024);
     const uint64_t v_desc0 = umma_desc_sw128(smem_base + C::kVOff, kExtendKeys * 128, 1024);
@@ -668,7 +874,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
             v[c] = valid ? __ldg(reinterpret_cast<const uint4*>(a.q + orow * DK) + h * 8 + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(qtile + h * (kExtendRows * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v[c];
+            *reinterpret_cast<uint4*>(qtile + h * (kExtendRows * 128) + r * 128 + ((c ^ (r & 7)) << 4)) =
+                C::FP8 ? bf16x8_to_f16x8(v[c]) : v[c];
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -736,8 +943,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
           for (int cc = 0; cc < kExtendKeys / 32; cc += 2) {
             uint32_t sr[64];
             load_s(cc, sr);
-            exp32(sr, sc2, nref2, pk + cc * 16, acc);
-            exp32(sr + 32, sc2, nref2, pk + cc * 16 + 16, acc);
+            exp32<C::FP8>(sr, sc2, nref2, pk + cc * 16, acc);
+            exp32<C::FP8>(sr + 32, sc2, nref2, pk + cc * 16 + 16, acc);
           }
           const uint64_t accs = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
           return f2_lo(accs) + f2_hi(accs);
@@ -753,7 +960,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         // so the whole warp takes this branch when any of its rows needs it;
         // the other rows keep their reference and get the same P again. A row
         // that sees no key of this tile (limit < key0) never needs it.
-        const bool need = (!(tsum <= kSumHigh) || (l == 0.f && tsum < kSumLow)) && limit >= key0;
+        constexpr float kHigh = C::FP8 ? kSumHighF16 : kSumHigh, kLow = C::FP8 ? kSumLowF16 : kSumLow;
+        const bool need = (!(tsum <= kHigh) || (l == 0.f && tsum < kLow)) && limit >= key0;
         if (__any_sync(0xffffffffu, need)) {
           float mx = -INFINITY;
 #pragma unroll
@@ -839,6 +1047,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
         m_ref = m;
       }
       float inv = l > 0.f ? 1.f / l : 0.f;
+      if constexpr (C::FP8) inv *= a.v_scale;  // V codes times the pool's scale
       if constexpr (EXTRAS) {
         // final rows of a model with sinks: the head's sink joins the normaliser
         if (!split && valid && a.sinks) {
@@ -920,83 +1129,22 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   }
 }
 
-// E4M3 pools on the extend path: the batch's 16-slot segments, in
-// seg_indices order, dequantised (code * scale, rounded once to bf16) into a
-// compact copy whose segment i is the batch's i-th segment, plus the identity
-// list idx[i] = i through which the extend kernel reads it. One thread
-// converts 16 codes (one 16-byte vector) of K and of V.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint16_t v, float scale) {
-  const uint32_t h = e4m3x2_to_f16x2(v);  // exact
-  float lo, hi;
-  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h & 0xffffu)));
-  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h >> 16)));
-  return pack_bf16(lo * scale, hi * scale);
-}
-
-__global__ void __launch_bounds__(256) fp8_stage_kernel(const uint8_t* __restrict__ kp, const uint8_t* __restrict__ vp,
-                                                        uint16_t* __restrict__ sk, uint16_t* __restrict__ sv,
-                                                        int* __restrict__ idx, const int* __restrict__ seg_indices,
-                                                        const int* __restrict__ plan, int seg_elems, float k_scale,
-                                                        float v_scale) {
-  pdl_launch_dependents();
-  pdl_wait();  // the segment list comes from the metadata build before this launch
-  const int np = plan[kTotalSegs];
-  const int vec = seg_elems / 16;
-  const long long n = (long long)np * vec;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const int pi = (int)(i / vec), w = (int)(i % vec);
-    const long long src = (long long)seg_indices[pi] * seg_elems + (long long)w * 16;
-    const long long dst = (long long)pi * seg_elems + (long long)w * 16;
-    const uint4 k = *reinterpret_cast<const uint4*>(kp + src);
-    const uint4 v = *reinterpret_cast<const uint4*>(vp + src);
-    const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
-    uint32_t ko[8], vo[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      ko[2 * j] = e4m3x2_to_bf16x2_scaled((uint16_t)(kw[j] & 0xffffu), k_scale);
-      ko[2 * j + 1] = e4m3x2_to_bf16x2_scaled((uint16_t)(kw[j] >> 16), k_scale);
-      vo[2 * j] = e4m3x2_to_bf16x2_scaled((uint16_t)(vw[j] & 0xffffu), v_scale);
-      vo[2 * j + 1] = e4m3x2_to_bf16x2_scaled((uint16_t)(vw[j] >> 16), v_scale);
-    }
-    *reinterpret_cast<uint4*>(sk + dst) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
-    *reinterpret_cast<uint4*>(sk + dst + 8) = make_uint4(ko[4], ko[5], ko[6], ko[7]);
-    *reinterpret_cast<uint4*>(sv + dst) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
-    *reinterpret_cast<uint4*>(sv + dst + 8) = make_uint4(vo[4], vo[5], vo[6], vo[7]);
-    if (w == 0) idx[pi] = pi;
-  }
-}
-
 template <class C>
 int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
                float v_scale, void* out, float* lse, cudaStream_t st, bool dplan) {
   CUtensorMap tk, tv;
   const uint64_t inner_k = (uint64_t)c.cfg.num_kv_heads * C::DK;
   const uint64_t inner_v = (uint64_t)c.cfg.num_kv_heads * C::DV;
-  uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
-  const bool fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3;
-  if (fp8) {
-    // E4M3 pools have K and V heads of one width (the configuration check)
-    static_assert(C::DK == C::DV || C::DK != 128, "E4M3 staging copies K and V rows of one width");
-    // widen the batch's E4M3 segments into the workspace copy and read that
-    if (!c.lay.has_stage) return PKV_ERR_UNSUPPORTED;
-    uint16_t* sk = reinterpret_cast<uint16_t*>(c.ws + c.lay.stage_k);
-    uint16_t* sv = reinterpret_cast<uint16_t*>(c.ws + c.lay.stage_v);
-    int* idx = reinterpret_cast<int*>(c.ws + c.lay.stage_idx);
-    const int seg_elems = kSegSlots * c.cfg.num_kv_heads * C::DK;
-    if (launch_pdl(fp8_stage_kernel, dim3((unsigned)(c.num_sms * 4)), dim3(256), 0, st,
-                   static_cast<const uint8_t*>(k_pool), static_cast<const uint8_t*>(v_pool), sk, sv, idx,
-                   make_meta(c).seg_indices, static_cast<const int*>(make_meta(c).plan), seg_elems, k_scale,
-                   v_scale) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    k_pool = sk;
-    v_pool = sv;
-    slots = (uint64_t)c.cfg.max_pages_total * (c.cfg.page_size / kSegSlots) * kSegSlots;
-  }
-  if (encode_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(k_pool), inner_k, slots, inner_k * 2,
-                     64, kSegSlots, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+  const uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
+  // boxes of 16 slots x 128 bytes: 64 bf16 elements, or 128 E4M3 codes (the
+  // whole row of a 128-wide head)
+  const CUtensorMapDataType dt = C::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t esz = C::FP8 ? 1 : 2;
+  if (encode_tmap_2d(&tk, dt, const_cast<void*>(k_pool), inner_k, slots, inner_k * esz, 128 / esz, kSegSlots,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
-  if (encode_tmap_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(v_pool), inner_v, slots, inner_v * 2,
-                     64, kSegSlots, CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+  if (encode_tmap_2d(&tv, dt, const_cast<void*>(v_pool), inner_v, slots, inner_v * esz, 128 / esz, kSegSlots,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
     return PKV_ERR_CUDA;
   ExtendArgs a;
   a.m = make_meta(c);
@@ -1006,9 +1154,10 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   a.num_q_heads = c.cfg.num_q_heads;
   a.num_kv_heads = c.cfg.num_kv_heads;
   a.group = c.cfg.num_q_heads / c.cfg.num_kv_heads;
-  // an E4M3 pool's scales are already in the dequantised copy
-  a.scale_log2 = sm_scale * kLog2e;
-  if (fp8) a.m.seg_indices = reinterpret_cast<const int*>(c.ws + c.lay.stage_idx);
+  // E4M3 codes are widened exactly: the K pool's scale joins the score scale
+  // and the V pool's scale multiplies the output
+  a.scale_log2 = sm_scale * (C::FP8 ? k_scale : 1.f) * kLog2e;
+  a.v_scale = C::FP8 ? v_scale : 1.f;
   a.out_32B = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
   a.tree = active_tree(c);
   a.sinks = c.sinks;
@@ -1021,7 +1170,8 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   memset(&tq, 0, sizeof(tq));
   a.q_tma = 0;
   a.q_box_tokens = 0;
-  if (kExtendRows % a.group == 0) {
+  // (E4M3 pools: the softmax warps copy Q, converting it to f16 on the way)
+  if (!C::FP8 && kExtendRows % a.group == 0) {
     const uint32_t box_tok = kExtendRows / a.group;
     const uint64_t tokens = (uint64_t)(c.cfg.max_q_tokens > (int)box_tok ? c.cfg.max_q_tokens : (int)box_tok);
     if (encode_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(q), C::DK,
@@ -1046,6 +1196,13 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
 
 int run_tc(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float sm_scale, float k_scale,
            float v_scale, void* out, float* lse, cudaStream_t st, bool dplan) {
+  if (c.cfg.kv_dtype == PKV_KV_FP8_E4M3) {
+    // E4M3 pools (128-wide heads): f16 operand rings of two K and two V tiles,
+    // one raw tile of codes in flight for each
+    if (c.cfg.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    return run_extend<ExtCfg<128, 128, 2, 2, true, 1, 1>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out,
+                                                          lse, st, dplan);
+  }
   if (c.cfg.head_dim == 128)
     return run_extend<ExtCfg<128, 128, 3, 2>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
   if (c.cfg.head_dim == 64)
@@ -1053,7 +1210,7 @@ int run_tc(Ctx& c, const void* q, const void* k_pool, const void* v_pool, float 
   // 192-wide Q/K heads with 128-wide V heads: two 48 KB Q tiles, so the rings
   // hold two 48 KB K tiles and one 32 KB V tile
   if (c.cfg.head_dim == 192)
-    return run_extend<ExtCfg<192, 128, 2, 1>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
+    return run_extend<ExtCfg<192, 128, 1, 2>>(c, q, k_pool, v_pool, sm_scale, k_scale, v_scale, out, lse, st, dplan);
   return PKV_ERR_UNSUPPORTED;
 }
 

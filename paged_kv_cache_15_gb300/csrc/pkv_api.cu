@@ -72,7 +72,7 @@ void grid_sizes(const pkv_config& cfg, int num_sms, int* decode_ctas, int* exten
   if (*extend_ctas < 1) *extend_ctas = 1;
 }
 
-Layout make_layout(const pkv_config& cfg, int num_sms, bool with_stage) {
+Layout make_layout(const pkv_config& cfg, int num_sms) {
   Layout L;
   int dctas, ectas;
   grid_sizes(cfg, num_sms, &dctas, &ectas);
@@ -108,15 +108,6 @@ Layout make_layout(const pkv_config& cfg, int num_sms, bool with_stage) {
   L.extend_tiles = take(sizeof(ExtendTile) * (size_t)L.max_extend_tiles);
   L.partial_o = take(sizeof(uint16_t) * (size_t)cap * cfg.num_q_heads * head_dim_v(cfg));
   L.partial_lse = take(sizeof(float) * (size_t)cap * cfg.num_q_heads);
-  L.has_stage = with_stage && cfg.kv_dtype == PKV_KV_FP8_E4M3;
-  L.stage_k = L.stage_v = L.stage_idx = 0;
-  if (L.has_stage) {
-    const size_t seg_k = (size_t)kSegSlots * cfg.num_kv_heads * cfg.head_dim * sizeof(uint16_t);
-    const size_t seg_v = (size_t)kSegSlots * cfg.num_kv_heads * head_dim_v(cfg) * sizeof(uint16_t);
-    L.stage_k = take(seg_k * (size_t)max_segments(cfg));
-    L.stage_v = take(seg_v * (size_t)max_segments(cfg));
-    L.stage_idx = take(sizeof(int) * (size_t)max_segments(cfg));
-  }
   L.total = off;
   return L;
 }
@@ -219,7 +210,7 @@ int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint
 int static_config_ok(const pkv_config* cfg) { return check_config(cfg); }
 
 size_t static_layout_bytes(const pkv_config& cfg, int num_sms, Layout* lay) {
-  *lay = make_layout(cfg, num_sms, false);  // decode only: no extend staging
+  *lay = make_layout(cfg, num_sms);
   return lay->total;
 }
 
@@ -260,7 +251,7 @@ int pkv_workspace_bytes(const pkv_config* cfg, size_t* bytes_out) {
   if (!bytes_out) return PKV_ERR_INVALID_ARG;
   int dev, sms;
   if (device_sms(&dev, &sms) != PKV_OK) return PKV_ERR_CUDA;
-  *bytes_out = make_layout(*cfg, sms, true).total;
+  *bytes_out = make_layout(*cfg, sms).total;
   return PKV_OK;
 }
 
@@ -281,7 +272,7 @@ int pkv_create(const pkv_config* cfg, void* d_workspace, size_t workspace_bytes,
   if (reinterpret_cast<uintptr_t>(d_workspace) & 255) return PKV_ERR_INVALID_ARG;
   int dev, sms;
   if (device_sms(&dev, &sms) != PKV_OK) return PKV_ERR_CUDA;
-  Layout lay = make_layout(*cfg, sms, true);
+  Layout lay = make_layout(*cfg, sms);
   if (workspace_bytes < lay.total) return PKV_ERR_CAPACITY;
   if (get_encoder() != PKV_OK) return PKV_ERR_CUDA;
   pkv_ctx* c = new (std::nothrow) pkv_ctx();

@@ -871,3 +871,14 @@ def test_head_widths_192_128_pools_bit_exact():
 def test_head_widths_192_128_full_size_decode_every_row():
     """The Llama-3-8B-shaped decode batch at full size with 192/128 heads."""
     full_check(preset("llama3_8b_decode", head_dims=W192))
+
+
+def test_fp8_workspace_holds_no_copy_of_the_pool():
+    """The E4M3 extend path widens codes in shared memory: an E4M3 context
+    needs exactly the workspace of the same configuration with bf16 pools,
+    however many pages it may touch."""
+    W = preset("long_fp8_decode", bs=2, len_scale=1 / 16)
+    cfg8 = config_for(W, max_pages_total=1 << 20)
+    cfg16 = config_for(W, max_pages_total=1 << 20)
+    cfg16.kv_dtype = B.PKV_KV_BF16
+    assert B.pkv_workspace_bytes(cfg8) == B.pkv_workspace_bytes(cfg16)
