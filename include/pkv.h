@@ -73,6 +73,8 @@ extern "C" {
 #define PKV_DEV_BAD_SLOT 4     /* set_kv_buffer loc outside [0, num_pages * page_size) */
 #define PKV_DEV_QO_TOO_LONG 5  /* decode path: qo_len beyond config.max_qo_len */
 #define PKV_DEV_TREE_TOO_LONG 6 /* draft-tree mask set and a request has more than 64 new tokens */
+#define PKV_DEV_TIMEOUT 16     /* a wait inside a kernel ran past the wait limit (pkv_set_wait_limit); the
+                                  CTA that waited gave up its remaining work, so the outputs are incomplete */
 
 /* ---- enumerations -------------------------------------------------------- */
 /* ForwardMode of the batch ("[SGLang] Hybrid Attention", section
@@ -257,6 +259,22 @@ int pkv_set_tree_mask(pkv_ctx* ctx, const uint64_t* d_tree_mask);
  * alive while forwards that use it run; a captured graph replays with
  * whatever it then holds. */
 int pkv_set_attention_sinks(pkv_ctx* ctx, const float* d_sinks);
+
+/* Bound on every wait inside the kernels (a warp waiting for a tile, a
+ * result or a free buffer), in nanoseconds; 0 restores the default of 2 s.
+ * A wait that runs past it records PKV_DEV_TIMEOUT: the CTA then stops
+ * issuing work, waits (again bounded) for its copies in flight, releases its
+ * tensor memory and exits, so the context stays usable; the outputs of that
+ * launch are incomplete. The limit is kept in the context's workspace and
+ * applies to every launch after this call. Synchronises `stream`. */
+int pkv_set_wait_limit(pkv_ctx* ctx, uint32_t limit_ns, void* stream);
+
+/* Test support for the bounded waits: with enable != 0, CTA 0 of every later
+ * forward arms the barrier of its first K/V tile load but never issues the
+ * copy, so the waits on that tile run out after the wait limit and the
+ * timeout path runs (nothing faults; the other CTAs work normally). enable
+ * = 0 turns it off. Synchronises `stream`. */
+int pkv_test_hold_first_load(pkv_ctx* ctx, int enable, void* stream);
 
 /* Synchronise `stream`, read the device error word into *code (PKV_DEV_*) and
  * clear it. Returns PKV_ERR_DEVICE when *code != PKV_DEV_OK. */

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CAPACITY, PKV_ERR_CUDA, PKV_ERR_DEVICE = range(6)
 (PKV_DEV_OK, PKV_DEV_BAD_LENGTH, PKV_DEV_BAD_PAGE, PKV_DEV_CAPACITY, PKV_DEV_BAD_SLOT, PKV_DEV_QO_TOO_LONG,
  PKV_DEV_TREE_TOO_LONG) = range(7)
+PKV_DEV_TIMEOUT = 16
 PKV_MODE_EXTEND, PKV_MODE_DECODE, PKV_MODE_IDLE, PKV_MODE_TARGET_VERIFY, PKV_MODE_DRAFT_EXTEND = range(5)
 PKV_SPEC_PREFILL, PKV_SPEC_DECODE = 0, 1
 PKV_PATH_INVALID, PKV_PATH_DECODE, PKV_PATH_EXTEND = -1, 0, 1
@@ -30,7 +31,8 @@ PKV_KV_BF16, PKV_KV_FP8_E4M3 = 0, 1
 EXPORTS = ("pkv_status_string", "pkv_workspace_bytes", "pkv_pool_bytes", "pkv_create", "pkv_destroy",
            "pkv_select_backend", "pkv_build_metadata", "pkv_get_metadata", "pkv_set_kv_buffer",
            "pkv_forward_decode", "pkv_forward_extend", "pkv_forward", "pkv_get_device_error", "pkv_describe",
-           "pkv_forward_decode_static", "pkv_set_tree_mask", "pkv_set_attention_sinks")
+           "pkv_forward_decode_static", "pkv_set_tree_mask", "pkv_set_attention_sinks", "pkv_set_wait_limit",
+           "pkv_test_hold_first_load")
 
 
 class PkvError(RuntimeError):
@@ -80,6 +82,8 @@ def lib():
                                            ctypes.c_float, ctypes.c_float, vp, vp, vp]),
             "pkv_set_tree_mask": (ctypes.c_int, [vp, vp]),
             "pkv_set_attention_sinks": (ctypes.c_int, [vp, vp]),
+            "pkv_set_wait_limit": (ctypes.c_int, [vp, ctypes.c_uint32, vp]),
+            "pkv_test_hold_first_load": (ctypes.c_int, [vp, ctypes.c_int, vp]),
             "pkv_get_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), vp]),
             "pkv_describe": (ctypes.c_int, [vp, ctypes.c_char_p, sz]),
             "pkv_forward_decode_static": (ctypes.c_int, [cfgp, i32, vp, vp, i32, vp, vp, vp, ctypes.c_float,
@@ -200,6 +204,17 @@ def pkv_set_attention_sinks(ctx, sinks) -> None:
     """Per-query-head sink logits (fp32 device tensor [num_q_heads]) for the
     forwards that follow, or None to turn sinks off."""
     _check(lib().pkv_set_attention_sinks(ctx, _ptr(sinks)), "pkv_set_attention_sinks")
+
+
+def pkv_set_wait_limit(ctx, limit_ns: int, stream=None) -> None:
+    """Bound on every wait inside the kernels, in ns (0: the 2 s default)."""
+    _check(lib().pkv_set_wait_limit(ctx, int(limit_ns), _stream(stream)), "pkv_set_wait_limit")
+
+
+def pkv_test_hold_first_load(ctx, enable: bool, stream=None) -> None:
+    """Test support: CTA 0 of later forwards never issues its first K/V load,
+    so its waits run out after the wait limit."""
+    _check(lib().pkv_test_hold_first_load(ctx, 1 if enable else 0, _stream(stream)), "pkv_test_hold_first_load")
 
 
 def pkv_get_device_error(ctx, stream=None) -> int:

@@ -256,6 +256,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
       // each id is published to the consumer warps through the queue.
       int w = (int)blockIdx.x < n_units ? (int)blockIdx.x : -1;
       bool stop = false;
+      // test support: CTA 0 arms its first stage but never loads it
+      const bool hold_first = blockIdx.x == 0 && __ldcg(plan + kHoldLoad) != 0;
       for (int iu = 0; !stop; ++iu) {
         const int q = iu & 1;
         if (!mbar_wait_ab(&uq_empty[q], ((iu >> 1) & 1) ^ 1, plan, s_abort)) {
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) decode_splitkv_ker
           mbar_arrive_expect_tx(&full[slot], (uint32_t)(np * kSegSlots * (C::kRowBytesK + C::kRowBytesV)));
           uint8_t* kdst = smem + slot * C::kStageBytes;
           uint8_t* vdst = kdst + C::kTileBytesK;
-          for (int p = 0; p < np; ++p) {
+          for (int p = 0; p < np && !(hold_first && iu == 0 && st == 0); ++p) {
             const int page = a.m.seg_indices[base + st * C::kStagePages + p];
 #pragma unroll
             for (int cb = 0; cb < C::kColBlocksK; ++cb)

@@ -229,7 +229,7 @@ struct ExtCfg {
   static constexpr int kRawKOff = kVOff + NV * kTileBytesV;
   static constexpr int kRawVOff = kRawKOff + RK * kRawTileBytes;
   static constexpr int kBarOff = kRawVOff + RV * kRawTileBytes;
-  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6 + 4 + 2 + RK + RV;
+  static constexpr int kNumBars = 2 + 2 * NK + 2 * NV + 6 + 4 + 2 + RK + RV + 1;
   static constexpr int kMergeOff = kBarOff + kNumBars * 8;           // dual units: tile B's (m, l) per row
   static constexpr int kTmemSlotOff = kMergeOff + 2 * kExtendRows * 4;
   static constexpr int kAbortOff = kTmemSlotOff + 8;
@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
   uint64_t* b_done = q_written + 2;     // dual unit: tile B's O is final and its (m, l) are in smem
   uint64_t* a_read = b_done + 1;        // dual unit: tile A has read tile B's O and (m, l)
   uint64_t* raw_full = a_read + 1;      // E4M3: [RK] raw K tiles, then [RV] raw V tiles, landed
+  uint64_t* mma_drain = raw_full + C::RK + C::RV;  // after an abort: the MMAs issued so far have finished
   float* s_merge = reinterpret_cast<float*>(smem + C::kMergeOff);  // [2][128]: m, l of tile B's rows
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
@@ -338,6 +339,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < C::RK + C::RV; ++s) mbar_init(&raw_full[s], 1);
+    mbar_init(mma_drain, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -395,6 +397,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     uint32_t qcount[2] = {0, 0}, qtcount[2] = {0, 0};
     bool stop = false;
     const int c = lane & 7, r0 = lane >> 3;  // 16-code chunk and first row of this lane
+    // test support: CTA 0 arms its first raw K tile but never loads it
+    const bool hold_first = !is_v && blockIdx.x == 0 && __ldcg(plan + kHoldLoad) != 0;
     for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
       const ExtendTile u = load_unit(a, w / a.num_kv_heads);
       const int g = w % a.num_kv_heads;
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 #pragma unroll
         for (int p = 0; p < kPagesPerTile; ++p) {
           const int pg = __shfl_sync(0xffffffffu, grp, ((e & 3) << 3) + p);
-          if (p < npg && leader)
+          if (p < npg && leader && !(hold_first && rt == 0))
             tma_load_2d_hint(dst + p * (kSegSlots * 128), tmap, g * 128, pg * kSegSlots, &rfull[rs], pol);
         }
         ++rt;
@@ -553,6 +557,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
     uint32_t qcount[2] = {0, 0};   // Q tiles issued per X (phase of q_full / q_empty)
     uint32_t qtcount[2] = {0, 0};  // of those, written by the softmax warps (phase of q_written)
     bool stop = false;
+    // test support: CTA 0 arms its first K tile but never loads it
+    const bool hold_first = !is_v && blockIdx.x == 0 && __ldcg(plan + kHoldLoad) != 0;
     for (int w = blockIdx.x; w < n_units && !stop; w += gridDim.x) {
       const ExtendTile u = load_unit(a, w / a.num_kv_heads);
       const int g = w % a.num_kv_heads;
@@ -633,7 +639,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
 #pragma unroll
         for (int p = 0; p < kPagesPerTile; ++p) {
           const int pg = __shfl_sync(0xffffffffu, grp, ((e & 3) << 3) + p);
-          if (p < npg && leader) {
+          if (p < npg && leader && !(hold_first && jt == 0)) {
             for (int cb = 0; cb < width / 64; ++cb)
               tma_load_2d_hint(dst + cb * (kExtendKeys * 128) + p * (kSegSlots * 128), tmap, g * width + cb * 64,
                                pg * kSegSlots, &full[st], pol);
@@ -785,7 +791,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) extend_tc_kernel(const __grid_
       for (int x = 0; x < 2; ++x)
         if (ukv.uses_q(x)) ++ucount[x];
     }
-    if (!ok && lane == 0) *s_abort = 1;
+    if (!ok) {
+      if (lane == 0) *s_abort = 1;
+      // MMAs issued before the abort finish before the tensor memory they
+      // write is freed (this wait ignores the abort flag on purpose)
+      umma_commit_warp(mma_drain);
+      mbar_wait(mma_drain, 0, plan);
+    }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
     const int x = warp >> 2;          // tile of this warpgroup

@@ -405,6 +405,25 @@ int pkv_set_attention_sinks(pkv_ctx* ctx, const float* d_sinks) {
   return PKV_OK;
 }
 
+// One int32 plan word of the context, written from the host; synchronises the stream.
+static int write_plan_word(pkv_ctx* ctx, int word, int32_t value, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(ctx->ws + ctx->lay.plan + sizeof(int32_t) * word, &value, sizeof(value),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_set_wait_limit(pkv_ctx* ctx, uint32_t limit_ns, void* stream) {
+  if (!ctx) return PKV_ERR_INVALID_ARG;
+  return write_plan_word(ctx, kWaitLimitNs, (int32_t)limit_ns, stream);
+}
+
+int pkv_test_hold_first_load(pkv_ctx* ctx, int enable, void* stream) {
+  if (!ctx) return PKV_ERR_INVALID_ARG;
+  return write_plan_word(ctx, kHoldLoad, enable ? 1 : 0, stream);
+}
+
 int pkv_get_device_error(pkv_ctx* ctx, int32_t* code, void* stream) {
   if (!ctx || !code) return PKV_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

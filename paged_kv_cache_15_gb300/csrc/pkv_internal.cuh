@@ -40,8 +40,8 @@ constexpr int kExtendUnitRows = 256;    // an extend work unit holds two tiles (
 constexpr int kExtendKeys = 128;        // keys per extend KV tile
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s bound on any mbarrier wait
 
-// Device error codes beyond the public PKV_DEV_* values
-constexpr int kDevTimeout = 16;
+// A bounded wait ran out (the public PKV_DEV_TIMEOUT)
+constexpr int kDevTimeout = PKV_DEV_TIMEOUT;
 
 // ---------------------------------------------------------------------------
 // Plan header (int32 words at the start of the workspace)
@@ -60,6 +60,8 @@ enum PlanWord : int {
   kSplitDecode = 10,   // requests with more than one split on the decode path
   kSplitExtend = 11,   // requests split along their KV range on the extend path
   kDecodeNext = 12,    // decode units claimed past the first wave (zeroed after every decode)
+  kWaitLimitNs = 14,   // bound on every mbarrier wait in ns (0: kWaitTimeoutNs), pkv_set_wait_limit
+  kHoldLoad = 15,      // test support: CTA 0 never issues its first K/V load (pkv_test_hold_first_load)
   kPlanWords = 32
 };
 
@@ -237,15 +239,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The wait bound of the context (read once a wait has not succeeded at once).
+__device__ __forceinline__ unsigned long long wait_limit_ns(const int* plan) {
+  const unsigned v = (unsigned)__ldcg(plan + kWaitLimitNs);
+  return v ? (unsigned long long)v : kWaitTimeoutNs;
+}
+
 // Wait for the phase with the given parity to complete. Bounded: gives up
-// after kWaitTimeoutNs, records kDevTimeout and returns false.
+// after the context's wait limit, records kDevTimeout and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* plan) {
   if (mbar_try_wait(bar, parity)) return true;
-  unsigned long long t0 = global_ns();
+  const unsigned long long t0 = global_ns(), limit = wait_limit_ns(plan);
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitTimeoutNs) {
+    if (global_ns() - t0 > limit) {
       record_error(plan, kDevTimeout, 0);
       return false;
     }
@@ -256,12 +264,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* p
 // (another role timed out), so one failure stops every waiter quickly.
 __device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t parity, int* plan, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
-  unsigned long long t0 = global_ns();
+  const unsigned long long t0 = global_ns(), limit = wait_limit_ns(plan);
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitTimeoutNs) {
+    if (global_ns() - t0 > limit) {
       record_error(plan, kDevTimeout, 0);
       return false;
     }
