@@ -756,11 +756,13 @@ int run_decode(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   const uint64_t inner_v = (uint64_t)c.cfg.num_kv_heads * C::DV;
   const uint64_t slots = (uint64_t)c.cfg.num_pages * c.cfg.page_size;
   const uint32_t box_inner = 128 / C::kElem;
+  // L2 fills no wider than one head's row of an E4M3 pool (128 bytes)
+  const CUtensorMapL2promotion promo = C::FP8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   if (encode_tmap_2d(&tk, dt, const_cast<void*>(k_pool), inner_k, slots, inner_k * C::kElem, box_inner, kSegSlots,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+                     CU_TENSOR_MAP_SWIZZLE_128B, promo) != PKV_OK)
     return PKV_ERR_CUDA;
   if (encode_tmap_2d(&tv, dt, const_cast<void*>(v_pool), inner_v, slots, inner_v * C::kElem, box_inner, kSegSlots,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+                     CU_TENSOR_MAP_SWIZZLE_128B, promo) != PKV_OK)
     return PKV_ERR_CUDA;
   DecodeArgs a;
   a.m = make_meta(c);

@@ -1152,11 +1152,13 @@ int run_extend(Ctx& c, const void* q, const void* k_pool, const void* v_pool, fl
   // whole row of a 128-wide head)
   const CUtensorMapDataType dt = C::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t esz = C::FP8 ? 1 : 2;
+  // L2 fills no wider than one head's row of an E4M3 pool (128 bytes)
+  const CUtensorMapL2promotion promo = C::FP8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   if (encode_tmap_2d(&tk, dt, const_cast<void*>(k_pool), inner_k, slots, inner_k * esz, 128 / esz, kSegSlots,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+                     CU_TENSOR_MAP_SWIZZLE_128B, promo) != PKV_OK)
     return PKV_ERR_CUDA;
   if (encode_tmap_2d(&tv, dt, const_cast<void*>(v_pool), inner_v, slots, inner_v * esz, 128 / esz, kSegSlots,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != PKV_OK)
+                     CU_TENSOR_MAP_SWIZZLE_128B, promo) != PKV_OK)
     return PKV_ERR_CUDA;
   ExtendArgs a;
   a.m = make_meta(c);

@@ -163,8 +163,12 @@ int decode_row_warps(const pkv_config& cfg);
 int decode_stage_pages(const pkv_config& cfg);
 
 // Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
+// promo: the L2 fill granularity of a copy. Pool rows of one head are 256
+// bytes wide for bf16 (128 elements) and 128 for E4M3, the neighbouring head
+// following; a fill wider than the row brings in the next head's bytes too.
 int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t outer,
-                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz,
+                   CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
                    CUtensorMapSwizzle swz);
