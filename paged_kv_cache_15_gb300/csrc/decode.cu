@@ -735,15 +735,25 @@ __global__ void __launch_bounds__(256, 3) split_merge_kernel(DecodeArgs a, int m
   const int rows = a.m.plan[kTotalQ] * a.num_q_heads;
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nwarps) {
+  // each warp takes a contiguous run of rows (consecutive heads of a token),
+  // so a token's request and split count are looked up once for its heads
+  // rather than once per row through a chain of dependent loads
+  const int per = (rows + nwarps - 1) / nwarps;
+  const int row0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * per;
+  const int row1 = min(rows, row0 + per);
+  int cur_t = -1, b = 0, nsplit = 0, q0 = 0, qo = 0, pbase = 0;
+  for (int row = row0; row < row1; ++row) {
     const int t = row / a.num_q_heads, h = row - t * a.num_q_heads;
-    const int b = a.m.token_req[t];
-    const int nsplit = extend_path ? a.m.ext_splits[b] : a.m.n_splits[b];
-    if (nsplit <= 1) continue;
-    const int q0 = a.m.qo_indptr[b];
-    const int qo = a.m.qo_indptr[b + 1] - q0;
-    if (qo * a.group > max_rows_per_head) continue;
-    merge_row<D>(a, a.m.partial_indptr[b], qo, t - q0, h, nsplit, (long long)row, lane);
+    if (t != cur_t) {
+      cur_t = t;
+      b = a.m.token_req[t];
+      nsplit = extend_path ? a.m.ext_splits[b] : a.m.n_splits[b];
+      q0 = a.m.qo_indptr[b];
+      qo = a.m.qo_indptr[b + 1] - q0;
+      pbase = a.m.partial_indptr[b];
+    }
+    if (nsplit <= 1 || qo * a.group > max_rows_per_head) continue;
+    merge_row<D>(a, pbase, qo, t - q0, h, nsplit, (long long)row, lane);
   }
 }
 
