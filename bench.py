@@ -44,10 +44,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # workload (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the
 # kernel's source file is unchanged (src_sha: first 16 hex digits of its sha256).
 NCU_TRAFFIC = {
-    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1386555136},
-    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "90ddbc63da199bd9", "bytes_per_launch": 1504556032},
-    ("extend_tc", "prefix_extend"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 967569664},
-    ("extend_tc", "spec_verify/prefill_path"): {"src_sha": "e1098ac520879201", "bytes_per_launch": 599880704},
+    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "5d8a90375cabd980", "bytes_per_launch": 1386525440},
+    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "5d8a90375cabd980", "bytes_per_launch": 1471781632},
+    ("extend_tc", "prefix_extend"): {"src_sha": "a645927089a35229", "bytes_per_launch": 271852032},
+    ("extend_tc", "prefix_extend_fp8"): {"src_sha": "a645927089a35229", "bytes_per_launch": 193205760},
+    ("extend_tc", "spec_verify/decode_path"): {"src_sha": "a645927089a35229", "bytes_per_launch": 599808000},
+    ("extend_tc", "spec_verify/prefill_path"): {"src_sha": "a645927089a35229", "bytes_per_launch": 599735296},
 }
 
 
