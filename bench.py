@@ -13,7 +13,7 @@ KV GB/s of the step (algorithmic K+V bytes read / step time); extend workloads
 report TFLOP/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--spec-mode prefill|decode]
+                    [--impl ours|reference] [--spec-mode prefill|decode] [--batch N]
 
 With --gpus N > 1 (launched by torch.distributed.run), every rank runs its own
 replica of the workload on its own GPU ("replicas only": the path has no
@@ -44,8 +44,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # workload (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the
 # kernel's source file is unchanged (src_sha: first 16 hex digits of its sha256).
 NCU_TRAFFIC = {
-    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "5d8a90375cabd980", "bytes_per_launch": 1386525440},
-    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "5d8a90375cabd980", "bytes_per_launch": 1471781632},
+    ("decode_splitkv", "llama3_8b_decode"): {"src_sha": "8e2560c6c19b5067", "bytes_per_launch": 1386290688},
+    ("decode_splitkv", "long_fp8_decode"): {"src_sha": "8e2560c6c19b5067", "bytes_per_launch": 1471689728},
     ("extend_tc", "prefix_extend"): {"src_sha": "a645927089a35229", "bytes_per_launch": 271852032},
     ("extend_tc", "prefix_extend_fp8"): {"src_sha": "a645927089a35229", "bytes_per_launch": 193205760},
     ("extend_tc", "spec_verify/decode_path"): {"src_sha": "a645927089a35229", "bytes_per_launch": 599808000},
@@ -572,6 +572,7 @@ def main():
                     help="pool element type (default: the workload's own)")
     ap.add_argument("--head-dims", type=int, nargs=2, default=None, metavar=("DK", "DV"),
                     help="widths of the Q/K and V heads (default: the workload's own)")
+    ap.add_argument("--batch", type=int, default=None, help="requests in the batch (default: the workload's own)")
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
@@ -582,7 +583,7 @@ def main():
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     from paged_kv_cache_15_gb300.workloads import preset
-    W = preset(args.workload, page_size=args.page_size, kv_dtype=args.kv_dtype,
+    W = preset(args.workload, bs=args.batch, page_size=args.page_size, kv_dtype=args.kv_dtype,
                head_dims=tuple(args.head_dims) if args.head_dims else None)
     if args.impl == "reference":
         run_reference(args, W, rank, world)

@@ -109,9 +109,10 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 // Combine the nsplit partial rows of one (token, query head) row:
 //   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s.
-// One warp per row, lanes across head_dim. Lane s reads split s's LSE in the
-// same round trip as the first kMergeBatch partial rows (their addresses do
-// not depend on the weights); the weights then come from a warp max and sum.
+// One warp per row, lanes across head_dim. Lane s reads the LSEs of splits s
+// and s + 32 in the same round trip as the first kMergeBatch partial rows
+// (their addresses do not depend on the weights); the weights then come from a
+// warp max and sum.
 // Partials were written by other CTAs, so they are read through L2
 // (ld.global.cg), never from a stale L1 line.
 constexpr int kMergeBatch = 8;
@@ -152,21 +153,26 @@ __device__ __forceinline__ void merge_row(const DecodeArgs& a, long long pbase, 
 #pragma unroll
   for (int sp = 0; sp < kMergeBatch; ++sp)
     if (sp < nsplit) x[sp] = part(sp);
-  static_assert(kMaxSplitsPerRequest <= 32, "one split per lane");
+  static_assert(kMaxSplitsPerRequest <= 64, "two splits per lane");
   const float l0 = lane < nsplit ? lse_of(lane) : -INFINITY;
-  float M = l0;
+  const float l1 = lane + 32 < nsplit ? lse_of(lane + 32) : -INFINITY;
+  float M = fmaxf(l0, l1);
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float w0 = M != -INFINITY && lane < nsplit ? fast_exp2((l0 - M) * kLog2e) : 0.f;
-  float Z = w0;
+  float w1 = M != -INFINITY && lane + 32 < nsplit ? fast_exp2((l1 - M) * kLog2e) : 0.f;
+  float Z = w0 + w1;
   for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
   const float invZ = Z > 0.f ? 1.f / Z : 0.f;
   w0 *= invZ;
+  w1 *= invZ;
+  // split sp's weight: lane sp % 32 holds it, in w0 below 32 and w1 above
+  auto weight = [&](int sp) { return __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31); };
   float acc[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) acc[j] = 0.f;
 #pragma unroll
   for (int sp = 0; sp < kMergeBatch; ++sp)
-    if (sp < nsplit) V::fma(acc, __shfl_sync(0xffffffffu, w0, sp), x[sp]);
+    if (sp < nsplit) V::fma(acc, weight(sp), x[sp]);
   for (int s0 = kMergeBatch; s0 < nsplit; s0 += kMergeBatch) {
 #pragma unroll
     for (int sp = 0; sp < kMergeBatch; ++sp)
@@ -174,7 +180,7 @@ __device__ __forceinline__ void merge_row(const DecodeArgs& a, long long pbase, 
 #pragma unroll
     for (int sp = 0; sp < kMergeBatch; ++sp) {
       if (s0 + sp >= nsplit) break;
-      V::fma(acc, __shfl_sync(0xffffffffu, w0, s0 + sp), x[sp]);
+      V::fma(acc, weight(s0 + sp), x[sp]);
     }
   }
   float lse = Z > 0.f ? M + __logf(Z) : -INFINITY;

@@ -85,6 +85,8 @@ struct MetaArgs {
   // path's KV splits
   int dec_tc;
   int units_target;      // decode work units to aim for
+  int dec_ctas;          // CTAs of the persistent decode grid
+  int fp8;               // E4M3 pools
   int ext_grid;          // CTAs of the extend kernel (units are dealt to them by a fixed stride)
   int partial_cap;
   int max_pages_total;
@@ -276,6 +278,74 @@ __device__ int extend_split_tiles(const MetaArgs& a, int chunk, const Sums& tot)
   return ct_lo + (kExtCandidates - 1 - (int)(best % kExtCandidates));
 }
 
+// Decode chunk size. The persistent decode grid takes (item, KV head) units
+// in order as its CTAs free up, and in a batch of a few long requests nearly
+// every unit is one whole chunk long: the step then lasts about
+// ceil(units / CTAs) chunks, and a chunk that leaves the last round of units
+// nearly empty idles most of the grid for one chunk's time. The candidates run
+// up from the smallest admissible chunk in whole pipeline stages; each costs
+// the larger of ceil(units / CTAs) chunks and an even share of all the pages,
+// both with a fixed cost per unit; the cheapest wins, ties going to the
+// smaller chunk. Thread t prices candidate t % 64 over every fourth request.
+// Which batches are priced: a bf16 unit is bound by memory, and when CTAs
+// fall idle at the end the ones still running take over most of their share
+// of the bandwidth, so there the smallest chunk stands unless its units do
+// not fill the grid kDecPriceRounds times; an E4M3 unit is bound by its
+// widening and MMA work, the running CTAs cannot speed up, and every such
+// batch is priced. Verify shapes on the tile kernel split by their own rule,
+// and batches of many requests (whose short last splits fill any round) are
+// not priced. Called by every thread of the block; identical in every CTA.
+constexpr int kDecCandidates = 64;
+constexpr int kDecUnitCostPages = 2;
+constexpr int kDecPriceMaxBatch = 256;
+constexpr int kDecPriceRounds = 4;
+static_assert(kThreads % kDecCandidates == 0 && kDecCandidates == 64, "two warps of candidates");
+
+__device__ int decode_chunk_pages(const MetaArgs& a, int chunk0, const Sums& tot) {
+  if (a.dec_tc || a.bs > kDecPriceMaxBatch || tot.np == 0) return chunk0;
+  if (!a.fp8) {
+    // units of the smallest chunk: a request takes ceil(np / chunk0) splits,
+    // at most np / chunk0 + 1, so a bound on the sum needs no pass
+    const long long ctas = a.dec_ctas > 0 ? a.dec_ctas : 1;
+    const long long units_lo = tot.np / chunk0 * a.num_kv_heads;
+    if (units_lo >= kDecPriceRounds * ctas) return chunk0;
+  }
+  __shared__ int s_items[kExtGroups][kDecCandidates];
+  __shared__ unsigned long long s_key[2];
+  const int ci = threadIdx.x % kDecCandidates, grp = threadIdx.x / kDecCandidates;
+  const long long cp = (long long)chunk0 + (long long)ci * a.stage_pages;
+  int items = 0;
+  for (int b = grp; b < a.bs; b += kExtGroups) {
+    int L, qo;
+    bool bad;
+    lengths(a, b, L, qo, bad);
+    const int np = segs_of(L);
+    items += np > 0 ? (int)((np + cp - 1) / cp) : 1;
+  }
+  s_items[grp][ci] = items;
+  __syncthreads();
+  if (threadIdx.x < kDecCandidates) {
+    long long units = 0;
+#pragma unroll
+    for (int g = 0; g < kExtGroups; ++g) units += s_items[g][ci];
+    units *= a.num_kv_heads;
+    const long long ctas = a.dec_ctas > 0 ? a.dec_ctas : 1;
+    const long long rounds = (units + ctas - 1) / ctas;
+    const long long share = (tot.np * a.num_kv_heads + units * kDecUnitCostPages + ctas - 1) / ctas;
+    long long cost = rounds * (cp + kDecUnitCostPages);
+    if (cost < share) cost = share;
+    unsigned long long key = (unsigned long long)cost * kDecCandidates + ci;
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, key, o);
+      if (y < key) key = y;
+    }
+    if ((threadIdx.x & 31) == 0) s_key[threadIdx.x >> 5] = key;
+  }
+  __syncthreads();
+  const unsigned long long best = s_key[0] < s_key[1] ? s_key[0] : s_key[1];
+  return chunk0 + (int)(best % kDecCandidates) * a.stage_pages;
+}
+
 // Exclusive block scan of six ints; returns this thread's prefix and the tile total.
 constexpr int kScanN = 6;
 struct ScanV {
@@ -339,7 +409,7 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   // keep sum over split requests of nsplit*qo below the partial buffer
   long long chunk = (tot.np * a.num_kv_heads + a.units_target - 1) / a.units_target;
   if (chunk < kDecodeMinChunkPages) chunk = kDecodeMinChunkPages;
-  // at most kMaxSplitsPerRequest splits of any request (the merge reads them one per lane)
+  // at most kMaxSplitsPerRequest splits of any request (the merge reads two per lane)
   const long long cmax = (tot.maxnp + kMaxSplitsPerRequest - 1) / kMaxSplitsPerRequest;
   if (chunk < cmax) chunk = cmax;
   long long room = (long long)a.partial_cap - tot.qo;
@@ -349,7 +419,8 @@ __global__ void __launch_bounds__(kThreads) build_metadata_kernel(MetaArgs a) {
   }
   chunk = (chunk + a.stage_pages - 1) / a.stage_pages * a.stage_pages;
   if (chunk > (1 << 30)) chunk = 1 << 30;
-  int ichunk = (int)chunk;
+  // the pricing only moves the chunk up, which keeps every bound above
+  const int ichunk = decode_chunk_pages(a, (int)chunk, tot);
   const int ext_ct = extend_split_tiles(a, ichunk, tot);
 
   if (over) {
@@ -568,6 +639,8 @@ int launch_build_metadata(Ctx& c, int batch, const int32_t* seq_lens, const int3
   a.stage_pages = decode_stage_pages(c.cfg);
   a.dec_tc = decode_row_warps(c.cfg) > 1 ? 1 : 0;
   a.units_target = c.decode_ctas * (decode_row_warps(c.cfg) == 1 ? kDecodeTargetWaves : kVerifyTargetWaves);
+  a.dec_ctas = c.decode_ctas;
+  a.fp8 = c.cfg.kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 0;
   a.ext_grid = c.extend_ctas;
   a.partial_cap = c.lay.partial_rows_cap;
   a.max_pages_total = c.cfg.max_pages_total;

@@ -31,9 +31,9 @@ constexpr int kPageSizeLarge = 128;
 // 128 rows each and pay more per unit
 constexpr int kDecodeTargetWaves = 8;
 constexpr int kVerifyTargetWaves = 4;
-// decode splits of one request at most: the merge reads one per lane (so at
-// most 32), and on long requests fewer, longer splits stream faster
-constexpr int kMaxSplitsPerRequest = 24;
+// decode splits of one request at most: the merge reads two per lane (so at
+// most 64); a lone long request then still spreads over the whole grid
+constexpr int kMaxSplitsPerRequest = 64;
 constexpr int kDecodeMinChunkPages = 8; // never cut a (request, head) range finer than 128 keys
 constexpr int kExtendRows = 128;        // query rows (token x head-in-group) per extend tile
 constexpr int kExtendUnitRows = 256;    // an extend work unit holds two tiles (A, B) sharing K/V

@@ -790,8 +790,9 @@ def test_extend_output_buffer_only_16_byte_aligned():
 @pytest.mark.parametrize("mode", ["decode", "verify"])
 def test_merge_at_the_split_cap(mode):
     """One 100k-token request alone in the batch: the plan would cut its KV
-    range into hundreds of splits but stops at the cap of 24 per request (the
-    merge reads one split per lane), and the merge combines all of them."""
+    range into hundreds of splits but stops at the cap of 64 per request (the
+    merge reads two splits per lane), and the merge combines all of them,
+    more than one lane's worth included."""
     if mode == "decode":
         W = make_workload("m32d", "decode", 1, 8, 1, 128, [100000], [1])
         d = full_check(W)
@@ -800,7 +801,20 @@ def test_merge_at_the_split_cap(mode):
         d = full_check(W, spec_mode=B.PKV_SPEC_PREFILL)
     # the plan words open the workspace; word 5 counts the (request, split) items
     plan = workspace_ints(d, d.attn.workspace.data_ptr(), 16)
-    assert plan[5] == 24
+    assert 32 < plan[5] <= 64
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_lone_long_request_spreads_over_the_grid(kv_dtype):
+    """A batch of one 131k-token request with eight KV heads: 24 splits would
+    give 192 units for a grid of two CTAs per SM, so the plan cuts it into
+    more than 32 (up to 64) and the merge's second split per lane is used;
+    sinks ride along. Every row against the oracle."""
+    W = make_workload("lone", "decode", 1, 32, 8, 128, [131071], [1], kv_dtype=kv_dtype)
+    W.sinks = random_sinks(W.num_q_heads, seed=15)
+    d = full_check(W)
+    plan = workspace_ints(d, d.attn.workspace.data_ptr(), 16)
+    assert 32 < plan[5] <= 64
 
 
 def test_verify_prefill_path_long_context_split():
