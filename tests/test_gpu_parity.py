@@ -565,9 +565,10 @@ def test_extend_nan_unused_slots_never_read():
 
 @pytest.mark.parametrize("case", ["small", "g16", "long_prefix", "verify_prefill", "with_sinks"])
 def test_extend_fp8_pool(case):
-    """E4M3 pools on the extend path: the batch's pages are widened into a
-    bf16 copy of the codes, k_scale goes into the score scale and v_scale
-    into the output; every row against the oracle's exact E4M3 decoding."""
+    """E4M3 pools on the extend path: the producer warps widen each tile's
+    codes to f16 in shared memory (no copy of the pool), k_scale goes into
+    the score scale and v_scale into the output; every row against the
+    oracle's exact E4M3 decoding."""
     spec = B.PKV_SPEC_PREFILL
     if case == "small":
         W = make_workload("e8", "extend", 3, 8, 2, 128, [10, 0, 300], [20, 130, 7], kv_dtype="fp8_e4m3")
