@@ -364,13 +364,13 @@ def timed_steps(d, spec, steps, world):
     return step_s, fwd_s
 
 
-def secondary(name, spec_name, local, steps, world, cpu_budget, page_size=16, head_dims=None):
+def secondary(name, spec_name, local, steps, world, cpu_budget, page_size=16, head_dims=None, bs=None):
     """Short measurement of another workload (no e2e), with the oracle timed
     beside it on a bounded sample (rank 0 of a single-GPU run only)."""
     from paged_kv_cache_15_gb300 import binding as B
     from paged_kv_cache_15_gb300.runner import DeviceBatch
     from paged_kv_cache_15_gb300.workloads import preset
-    W = preset(name, page_size=page_size, head_dims=head_dims)
+    W = preset(name, bs=bs, page_size=page_size, head_dims=head_dims)
     spec = B.PKV_SPEC_DECODE if spec_name == "decode" else B.PKV_SPEC_PREFILL
     d = DeviceBatch(W, device=f"cuda:{local}")
 
@@ -393,7 +393,8 @@ def secondary(name, spec_name, local, steps, world, cpu_budget, page_size=16, he
            "roofline_frac": roof["frac"], "achieved": roof["achieved"], "achieved_unit": roof["unit"],
            "kernel": roof["kernel"], "path": spec_name if W.mode == "verify" else
            ("decode" if W.mode == "decode" else "extend"),
-           "steps": steps, "page_size": W.page_size, "head_dims": [W.head_dim, W.dv], "cpu_baseline": None}
+           "steps": steps, "page_size": W.page_size, "head_dims": [W.head_dim, W.dv], "batch": W.bs,
+           "cpu_baseline": None}
     del d
     torch.cuda.empty_cache()
     if world == 1 and cpu_budget > 0:
@@ -509,23 +510,30 @@ def run_ours(args, W, rank, world, local):
     # --- the other named workloads of the metric, short runs
     others = {}
     if not args.no_secondary:
-        # (workload, speculative attention mode, page size, head widths)
-        for name, sp, ps, hd in (("tiny_decode", "prefill", 16, None), ("prefix_extend", "prefill", 16, None),
-                                 ("prefix_extend_fp8", "prefill", 16, None), ("spec_verify", "decode", 16, None),
-                                 ("spec_verify", "prefill", 16, None), ("long_fp8_decode", "prefill", 16, None),
-                                 ("llama3_8b_decode", "prefill", 128, None),
-                                 ("llama3_8b_decode", "prefill", 16, (192, 128)),
-                                 ("prefix_extend", "prefill", 16, (192, 128))):
-            if name == W.name and sp == args.spec_mode and ps == W.page_size and hd is None and W.dv == W.head_dim:
+        # (workload, speculative attention mode, page size, head widths, batch)
+        for name, sp, ps, hd, nb in (("tiny_decode", "prefill", 16, None, None),
+                                     ("prefix_extend", "prefill", 16, None, None),
+                                     ("prefix_extend_fp8", "prefill", 16, None, None),
+                                     ("spec_verify", "decode", 16, None, None),
+                                     ("spec_verify", "prefill", 16, None, None),
+                                     ("long_fp8_decode", "prefill", 16, None, None),
+                                     ("long_fp8_decode", "prefill", 16, None, 1),
+                                     ("llama3_8b_decode", "prefill", 128, None, None),
+                                     ("llama3_8b_decode", "prefill", 16, (192, 128), None),
+                                     ("prefix_extend", "prefill", 16, (192, 128), None)):
+            if (name == W.name and sp == args.spec_mode and ps == W.page_size and hd is None and nb is None
+                    and W.dv == W.head_dim and args.batch is None):
                 continue
             key = name if name != "spec_verify" else f"spec_verify/{sp}_path"
             if ps != 16:
                 key += f"/page_size_{ps}"
             if hd is not None:
                 key += f"/head_dims_{hd[0]}_{hd[1]}"
+            if nb is not None:
+                key += f"/batch_{nb}"
             others[key] = secondary(name, sp, local, args.secondary_steps, world,
                                     0.0 if args.no_cpu_baseline else args.secondary_cpu_budget, page_size=ps,
-                                    head_dims=hd)
+                                    head_dims=hd, bs=nb)
 
     if rank != 0:
         return
